@@ -1,0 +1,176 @@
+/*
+ * fp4idx.h -- C ABI of the GB300 FP4 indexer library (libfp4idx.so).
+ *
+ * The DeepSeek-V4 sparse-attention indexer, as described on three SGLang pull
+ * request pages:
+ *   [P1] "dsv4.1-amd: KV cache layouts, FP4 indexer, compressor and router kernels"
+ *   [P2] "[AMD] Enable FP4 indexer for Deepseek V4"
+ *   [P3] "[AMD] DeepSeek-V4.1-Flash on MI350X (gfx950)"
+ * Write side: each compressed bf16 index-K row of 128 goes through RMSNorm, RoPE
+ * (dims 0..63), a 128-point Hadamard rotation and e2m1 quantisation with one
+ * UE8M0 scale per 32 elements, into a paged cache split into a 64-byte payload
+ * tensor and a 4-byte scale tensor.  Read side: paged-MQA logits
+ *   logits[t,s] = sum_h w[t,h] * ReLU(q_fp4[t,h] . k_fp4[s]),  s < context_lens[t],
+ * then a per-row top-k of compressed-token indices, ascending.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers (cudaMalloc / torch CUDA memory on the current
+ *     device) unless marked "host".  Arrays are dense, row-major, 16-byte aligned.
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Ownership stays with the caller.  The library never allocates, frees or
+ *     synchronises; every call only enqueues kernels on `stream` (a cudaStream_t,
+ *     NULL = the legacy default stream) and returns.  Calls are safe inside CUDA
+ *     graph capture.
+ *   - Return value: FP4IDX_OK, or an fp4idx_status for a problem the host can see
+ *     (null pointer, bad size, misalignment, unsupported shape, too small a
+ *     workspace, a failed launch).  Nothing is enqueued when a call fails.
+ *   - status_dev (nullable, one int32 in device memory, zero it before use): the
+ *     kernels record the first data-dependent error they meet (a page id outside
+ *     [0, num_pages), a slot past the cache, a position outside the RoPE table, a
+ *     context length above the stated maximum, a pipeline wait that ran out).
+ *     They skip the offending access and never trap.
+ *   - Fixed shapes: head_dim 128, 64 indexer heads, 64 tokens per cache page.
+ *
+ * Cache layout (split, [P2] Motivation): per physical page p and token j < 64,
+ *   payload[p][c][j][0..15]  (uint8, [num_pages,4,64,16]; 64 B per token)
+ *   scale  [p][c][j]         (uint8, [num_pages,4,64];    4 B per token)
+ * c = 32-element block (element 32c+2b in the low nibble of byte b, 32c+2b+1 in
+ * the high nibble), scale byte = e + 127 where the block is e2m1(x * 2^-e).
+ * Slot of token j on page p: p*64 + j.
+ * Query layout (this library's own, shaped like one K page with heads in place
+ * of tokens): q_payload[t][c][h][0..15] ([T,4,64,16]), q_scale[t][c][h] ([T,4,64]).
+ */
+#ifndef FP4IDX_H
+#define FP4IDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP4IDX_HEAD_DIM 128
+#define FP4IDX_NUM_HEADS 64
+#define FP4IDX_PAGE_TOKENS 64
+#define FP4IDX_FP8_PAGE_BYTES (64 * 128 + 64 * 4)
+#define FP4IDX_MAX_TOPK 4096
+#define FP4IDX_MAX_CONTEXT 65536
+
+typedef enum {
+  FP4IDX_OK = 0,
+  FP4IDX_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer, k out of range */
+  FP4IDX_ERR_UNSUPPORTED = 2,  /* a shape the kernels do not implement (heads != 64, ...) */
+  FP4IDX_ERR_CUDA = 3,         /* a CUDA launch or attribute call failed */
+  FP4IDX_ERR_WORKSPACE = 4,    /* schedule/workspace buffer smaller than the size query says */
+  FP4IDX_ERR_BAD_PAGE = 5,     /* device: page id / slot outside the cache */
+  FP4IDX_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its iteration limit */
+  FP4IDX_ERR_BAD_POSITION = 7, /* device: RoPE position outside [0, max_pos) */
+  FP4IDX_ERR_BAD_LENGTH = 8,   /* device: context length < 0 or above max_context / page-table width */
+  FP4IDX_ERR_SCHEDULE = 9      /* schedule built for another row count or grid */
+} fp4idx_status;
+
+/* Human-readable name of a status code (static string). */
+const char* fp4idx_status_string(int status);
+
+/* Number of SMs of the current device (host out-pointer). */
+int fp4idx_num_sms(int32_t* num_sms_out);
+
+/*
+ * K store -- the fused writer of [P2] Modifications / FP4 kernel adapters
+ * ("fused RMSNorm, RoPE, Hadamard, FP4 quantization, and paged cache writes")
+ * into the split layout of [P2] Motivation; round-to-nearest-even per [P1] Summary.
+ *   k          [n_rows,128] bf16   compressed index-K rows
+ *   positions  [n_rows] int32      RoPE position of each row, in [0, max_pos)
+ *   slots      [n_rows] int32      destination slot page*64+j; slot < 0 = padding, skipped
+ *   norm_w     [128] bf16          RMSNorm weight ([P2] compressor.py BF16 mirror)
+ *   eps                            RMSNorm epsilon (1e-6 for DeepSeek-V4)
+ *   cos_sin    [max_pos,64] bf16   row p: cos(p f_i) for i<32, then sin(p f_i)
+ *   payload    [num_pages,4,64,16] uint8, scale [num_pages,4,64] uint8 (written)
+ * Device errors: BAD_PAGE (slot >= num_pages*64), BAD_POSITION; the row is skipped.
+ */
+int fp4idx_store_k(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                   const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
+                   uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status_dev, void* stream);
+
+/*
+ * K store into the FP8 "fused" indexer layout, 132 bytes per token ([P2] Device
+ * memory and sizing: the FP8 footprint the FP4 entry replaces).  Same chain up to
+ * the Hadamard, then one fp32 scale per token s = amax/448 (1 if amax = 0) and
+ * e4m3 = RNE-satfinite(x / s).  Page layout (fp8_pages, [num_pages, 8448] uint8):
+ * bytes [j*128, j*128+128) = token j's e4m3 values, bytes [8192 + 4j, 8192 + 4j + 4)
+ * = its fp32 scale.  Arguments and errors as fp4idx_store_k.
+ */
+int fp4idx_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                       const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
+                       uint8_t* fp8_pages, int64_t num_pages, int32_t* status_dev, void* stream);
+
+/*
+ * Q quant -- [P2] Modifications / fp4_indexer_hip.py "Q RoPE/Hadamard/FP4
+ * quantization" and [P1] Summary's query packer: RoPE at q_positions[t], Hadamard,
+ * e2m1 + UE8M0/32.  No RMSNorm on the query side.
+ *   q [n_rows, n_heads, 128] bf16;  q_positions [n_rows] int32
+ *   q_payload [n_rows,4,64,16] uint8, q_scale [n_rows,4,64] uint8 (written)
+ * n_heads must be 64 (UNSUPPORTED otherwise).  Device error: BAD_POSITION.
+ */
+int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
+                   const uint16_t* cos_sin, int32_t max_pos, uint8_t* q_payload, uint8_t* q_scale,
+                   int32_t* status_dev, void* stream);
+
+/*
+ * Schedule -- the length-balanced split of the logits work over the GPU
+ * ([P1] Summary: an in-tree decode schedule whose registers do not grow with the
+ * row count; [P2] Attention runtime: schedules built during graph capture and
+ * reused across all C4 layers of a forward).  One small device kernel: no host
+ * sync, capturable, a pure function of (context_lens, row_seq, n_rows, num_ctas),
+ * so a schedule built once serves every layer of the same batch.
+ *   context_lens [n_rows] int32  visible compressed tokens of each query row
+ *                                (padded rows: 0; prefill rows: floor((p+1)/4))
+ *   row_seq      [n_rows] int32  sequence (page-table row) of each query row; rows
+ *                                of one sequence that are adjacent share K tiles
+ *   num_ctas                     grid the logits kernel will use (0 = SM count)
+ *   schedule     device buffer of at least fp4idx_schedule_workspace_bytes(n_rows, num_ctas)
+ */
+size_t fp4idx_schedule_workspace_bytes(int64_t max_rows, int32_t num_ctas);
+int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int64_t n_rows,
+                          int32_t num_ctas, void* schedule, size_t schedule_bytes, void* stream);
+
+/*
+ * Paged-MQA logits + top-k -- [P2] Modifications: "Dispatch decode and prefill
+ * FP4 paged-MQA logits" over the split cache through a guarded page table; padded
+ * rows keep context length 0 ([P2] Attention runtime); the selection is sorted
+ * and ordered by position ([P3] Changes, Historical results).
+ *   q_payload/q_scale   output of fp4idx_quant_q for the n_rows rows
+ *   w                   [n_rows,64] fp32 head weights
+ *   payload/scale       the split K cache, num_pages pages
+ *   page_table          [num_seqs, max_pages] int32 physical page of logical page i
+ *   row_seq, context_lens  as given to fp4idx_build_schedule (same arrays)
+ *   max_context         host-known upper bound of context_lens (<= FP4IDX_MAX_CONTEXT)
+ *   k                   1..FP4IDX_MAX_TOPK
+ *   schedule            built by fp4idx_build_schedule for these rows
+ *   workspace           >= fp4idx_logits_workspace_bytes(n_rows, max_context, k) bytes
+ *                       (may be 0 bytes when logits_out is given)
+ *   topk_idx  [n_rows,k] int32 (written): the k highest-logit token indices of each
+ *             row in ascending order; all of them when context_len <= k; -1 pads.
+ *   logits_out [n_rows, logits_stride] fp32 (nullable): when given, receives
+ *             logits[t,s] for s < context_lens[t] (the rest is not written).
+ * Device errors: BAD_PAGE (page id out of range: the tile is skipped),
+ * BAD_LENGTH, TIMEOUT, SCHEDULE.
+ */
+size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int32_t k);
+int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                       int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                       const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                       const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
+                       size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                       float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream);
+
+/* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
+ * a test/diagnostic helper, not for the hot path. */
+int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4IDX_H */

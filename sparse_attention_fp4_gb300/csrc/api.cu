@@ -1,0 +1,175 @@
+// C ABI of libfp4idx.so: argument validation, then kernel launches on the caller's
+// stream.  No allocation, no synchronisation (except fp4idx_read_status).
+#include <cstdio>
+
+#include "fp4idx_internal.cuh"
+#include "schedule.cuh"
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4IDX_OK : FP4IDX_ERR_CUDA; }
+
+int device_sms(int32_t* n) { return fp4idx_num_sms(n); }
+
+inline int64_t logits_row_stride(int32_t max_context) { return ((int64_t)max_context + 3) / 4 * 4; }
+
+int check_store_args(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                     const uint16_t* norm_w, const uint16_t* cos_sin, int32_t max_pos, int64_t num_pages) {
+  if (n_rows < 0 || num_pages < 0 || max_pos <= 0) return FP4IDX_ERR_INVALID_ARG;
+  if (num_pages > (int64_t)INT32_MAX / fp4idx::kPage) return FP4IDX_ERR_UNSUPPORTED;  // slots are int32
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!k || !positions || !slots || !norm_w || !cos_sin) return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(norm_w) || !aligned16(cos_sin) || !aligned4(positions) || !aligned4(slots))
+    return FP4IDX_ERR_INVALID_ARG;
+  return FP4IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp4idx_status_string(int status) {
+  switch (status) {
+    case FP4IDX_OK: return "ok";
+    case FP4IDX_ERR_INVALID_ARG: return "invalid argument";
+    case FP4IDX_ERR_UNSUPPORTED: return "unsupported shape";
+    case FP4IDX_ERR_CUDA: return "CUDA error";
+    case FP4IDX_ERR_WORKSPACE: return "workspace too small";
+    case FP4IDX_ERR_BAD_PAGE: return "page id or slot outside the cache";
+    case FP4IDX_ERR_TIMEOUT: return "pipeline wait timed out";
+    case FP4IDX_ERR_BAD_POSITION: return "RoPE position outside the table";
+    case FP4IDX_ERR_BAD_LENGTH: return "context length out of range";
+    case FP4IDX_ERR_SCHEDULE: return "schedule does not match the call";
+    default: return "unknown status";
+  }
+}
+
+int fp4idx_num_sms(int32_t* num_sms_out) {
+  if (!num_sms_out) return FP4IDX_ERR_INVALID_ARG;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4IDX_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FP4IDX_ERR_CUDA;
+  *num_sms_out = n;
+  return FP4IDX_OK;
+}
+
+int fp4idx_store_k(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                   const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
+                   uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status_dev, void* stream) {
+  int st = check_store_args(k, n_rows, positions, slots, norm_w, cos_sin, max_pos, num_pages);
+  if (st != FP4IDX_OK || n_rows == 0) return st;
+  if (!payload || !scale || !aligned16(payload)) return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_store_k(k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, payload,
+                                          scale, num_pages, status_dev, as_stream(stream)));
+}
+
+int fp4idx_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                       const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
+                       uint8_t* fp8_pages, int64_t num_pages, int32_t* status_dev, void* stream) {
+  int st = check_store_args(k, n_rows, positions, slots, norm_w, cos_sin, max_pos, num_pages);
+  if (st != FP4IDX_OK || n_rows == 0) return st;
+  if (!fp8_pages || !aligned16(fp8_pages)) return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_store_k_fp8(k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos,
+                                              fp8_pages, num_pages, status_dev, as_stream(stream)));
+}
+
+int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
+                   const uint16_t* cos_sin, int32_t max_pos, uint8_t* q_payload, uint8_t* q_scale,
+                   int32_t* status_dev, void* stream) {
+  if (n_rows < 0 || max_pos <= 0) return FP4IDX_ERR_INVALID_ARG;
+  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!q || !q_positions || !cos_sin || !q_payload || !q_scale) return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(cos_sin) || !aligned16(q_payload) || !aligned4(q_positions))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_quant_q(q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, status_dev,
+                                          as_stream(stream)));
+}
+
+size_t fp4idx_schedule_workspace_bytes(int64_t max_rows, int32_t num_ctas) {
+  (void)num_ctas;
+  if (max_rows < 0 || max_rows > INT32_MAX - 1) return 0;
+  return fp4idx::sched_bytes(max_rows);
+}
+
+int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int64_t n_rows, int32_t num_ctas,
+                          void* schedule, size_t schedule_bytes, void* stream) {
+  if (n_rows < 0 || n_rows > INT32_MAX - 1 || num_ctas < 0) return FP4IDX_ERR_INVALID_ARG;
+  if (!schedule || !aligned16(schedule)) return FP4IDX_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!context_lens || !row_seq || !aligned4(context_lens) || !aligned4(row_seq)))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (schedule_bytes < fp4idx::sched_bytes(n_rows)) return FP4IDX_ERR_WORKSPACE;
+  if (num_ctas == 0) {
+    int st = device_sms(&num_ctas);
+    if (st != FP4IDX_OK) return st;
+  }
+  return from_cuda(fp4idx::launch_build_schedule(context_lens, row_seq, (int32_t)n_rows, num_ctas, schedule,
+                                                 as_stream(stream)));
+}
+
+size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int32_t k) {
+  (void)k;
+  if (max_rows < 0 || max_context < 0) return 0;
+  return (size_t)max_rows * (size_t)logits_row_stride(max_context) * sizeof(float);
+}
+
+int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                       int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                       const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                       const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
+                       size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                       float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream) {
+  if (n_rows < 0 || n_rows > INT32_MAX - 1 || num_pages < 0 || num_seqs < 0 || max_pages < 0)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
+  if (k < 1 || k > FP4IDX_MAX_TOPK || max_context < 0) return FP4IDX_ERR_INVALID_ARG;
+  if (max_context > FP4IDX_MAX_CONTEXT) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!q_payload || !q_scale || !w || !payload || !scale || !page_table || !row_seq || !context_lens || !schedule ||
+      !topk_idx)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(q_payload) || !aligned16(q_scale) || !aligned16(w) || !aligned16(payload) || !aligned16(scale) ||
+      !aligned4(page_table) || !aligned4(row_seq) || !aligned4(context_lens) || !aligned16(schedule) ||
+      !aligned4(topk_idx))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  if (schedule_bytes < fp4idx::sched_bytes(n_rows)) return FP4IDX_ERR_WORKSPACE;
+  float* buf;
+  int64_t stride;
+  if (logits_out) {
+    if (logits_stride < max_context || !aligned4(logits_out)) return FP4IDX_ERR_INVALID_ARG;
+    buf = logits_out;
+    stride = logits_stride;
+  } else {
+    stride = logits_row_stride(max_context);
+    if (!workspace || !aligned16(workspace)) return FP4IDX_ERR_INVALID_ARG;
+    if (workspace_bytes < fp4idx_logits_workspace_bytes(n_rows, max_context, k)) return FP4IDX_ERR_WORKSPACE;
+    buf = reinterpret_cast<float*>(workspace);
+  }
+  int32_t grid = 0;
+  int st = device_sms(&grid);
+  if (st != FP4IDX_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = fp4idx::launch_logits_mxf4(q_payload, q_scale, w, (int32_t)n_rows, payload, scale, num_pages,
+                                             page_table, num_seqs, max_pages, row_seq, context_lens, max_context,
+                                             schedule, grid, buf, stride, status_dev, s);
+  if (e != cudaSuccess) return FP4IDX_ERR_CUDA;
+  return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_idx,
+                                       status_dev, s));
+}
+
+int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream) {
+  if (!status_dev || !host_out) return FP4IDX_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemcpyAsync(host_out, status_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FP4IDX_ERR_CUDA;
+  return from_cuda(cudaStreamSynchronize(s));
+}
+
+}  // extern "C"

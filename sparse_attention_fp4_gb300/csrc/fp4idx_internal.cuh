@@ -1,0 +1,44 @@
+// Internal declarations shared by the translation units of libfp4idx.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp4idx.h"
+
+namespace fp4idx {
+
+constexpr int kHeadDim = 128;
+constexpr int kHeads = 64;
+constexpr int kPage = 64;
+constexpr int kRope = 64;
+
+// First data-dependent error wins; never traps.
+__device__ __forceinline__ void record_error(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------- launchers (host)
+cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                           const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
+                           uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status,
+                           cudaStream_t stream);
+cudaError_t launch_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
+                               const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
+                               uint8_t* pages, int64_t num_pages, int32_t* status, cudaStream_t stream);
+cudaError_t launch_quant_q(const uint16_t* q, int64_t n_rows, const int32_t* q_positions, const uint16_t* cos_sin,
+                           int32_t max_pos, uint8_t* q_payload, uint8_t* q_scale, int32_t* status,
+                           cudaStream_t stream);
+
+cudaError_t launch_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int32_t n_rows,
+                                  int32_t num_ctas, void* ws, cudaStream_t stream);
+cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int32_t n_rows,
+                               const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                               const int32_t* page_table, int64_t num_seqs, int32_t max_pages,
+                               const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
+                               const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
+                               int32_t* status, cudaStream_t stream);
+cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
+                        int32_t max_context, int32_t k, int32_t* out, int32_t* status, cudaStream_t stream);
+
+}  // namespace fp4idx

@@ -1,0 +1,444 @@
+// Paged-MQA logits over the split FP4 index-K cache, on the block-scaled tensor cores.
+//
+// [AMD] Enable FP4 indexer for Deepseek V4 -- Modifications: decode and prefill "FP4
+// paged-MQA logits" read the 64-byte payload / 4-byte UE8M0 scale tensors through a
+// guarded page table; the logits are
+//   logits[t,s] = sum_h w[t,h] * ReLU(q_fp4[t,h] . k_fp4[s]),   s < context_lens[t].
+//
+// GB300 design (one persistent CTA per SM, 7 warps):
+//   warp 0  producer: per 128-token tile, two pages as 8 x 1 KB bulk copies into
+//           [block c][page][64 tokens][16 B] (a canonical no-swizzle K-major operand with
+//           M = 128 tokens) plus the two 256 B scale pages; per work item, the group's
+//           query rows (4 KB payload + 256 B scales each, one bulk copy each).  Page ids
+//           are read 32 at a time, one chunk ahead.
+//   warp 1  MMA issuer: copies the scale atoms to tensor memory (tcgen05.cp) and, per
+//           (tile, query row), issues two kind::mxf4 block-scaled MMAs (K = 64 each):
+//           D[128 tokens x 64 heads] in a 64-column TMEM slot (ring of 6 slots).
+//   warp 2  scale transposer: reorders the [c][token] scale bytes into the 32 x 16 B atom
+//           tcgen05.cp replicates over the four TMEM lane groups.
+//   warps 3-6 epilogue: thread = TMEM lane = token; ReLU, head-weighted sum, mask at the
+//           row's context length, coalesced fp32 store of the logits.
+// Work items come from the length-balanced schedule (schedule.cuh).  Every wait is
+// bounded: on expiry the CTA records FP4IDX_ERR_TIMEOUT, lets in-flight copies land,
+// frees its tensor memory and returns.
+#include "fp4idx_internal.cuh"
+#include "ptx.cuh"
+#include "schedule.cuh"
+
+namespace fp4idx {
+namespace {
+
+constexpr int kStages = 8;
+constexpr int kSlots = 6;
+constexpr int kWarps = 7;
+constexpr int kThreads = kWarps * 32;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSf = 2, kWarpEpi0 = 3;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+// tensor memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColAcc = 0;                       // kSlots x 64 fp32 accumulators
+constexpr uint32_t kColSfa = kSlots * 64;             // kStages x 4 (K scale atoms)
+constexpr uint32_t kColSfb = kColSfa + kStages * 4;   // 2 x kGroupMax x 4 (query scale atoms)
+static_assert(kColSfb + 2 * kGroupMax * 4 <= kTmemCols, "tensor memory budget");
+
+// shared memory layout (bytes from the 1 KB-aligned dynamic base)
+constexpr uint32_t kKPayBytes = 8192;  // [c][2 pages][64][16]
+constexpr uint32_t kKScBytes = 512;    // [2 pages][c][64]
+constexpr uint32_t kAtomBytes = 512;   // 32 x 16 B
+constexpr uint32_t kQPayBytes = kGroupMax * 4096;
+constexpr uint32_t kQScBytes = kGroupMax * 256;
+constexpr uint32_t OFF_KPAY = 0;
+constexpr uint32_t OFF_KSC = OFF_KPAY + kStages * kKPayBytes;
+constexpr uint32_t OFF_KATOM = OFF_KSC + kStages * kKScBytes;
+constexpr uint32_t OFF_QPAY = OFF_KATOM + kStages * kAtomBytes;
+constexpr uint32_t OFF_QSC = OFF_QPAY + 2 * kQPayBytes;
+constexpr uint32_t OFF_QATOM = OFF_QSC + 2 * kQScBytes;
+constexpr uint32_t OFF_W = OFF_QATOM + 2 * kGroupMax * kAtomBytes;      // per epilogue warp: [kGroupMax][64] fp32
+constexpr uint32_t OFF_LEN = OFF_W + 4 * kGroupMax * 64 * 4;            // per epilogue warp: [kGroupMax] int32
+constexpr uint32_t OFF_BAR = OFF_LEN + 4 * kGroupMax * 4;
+constexpr int kNumBars = 3 * kStages + 6 + 2 * kSlots;
+constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
+constexpr uint32_t kSmemBytes = OFF_MISC + 16;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 16 == 0, "alignment");
+
+// barrier slots
+__device__ __forceinline__ uint32_t bar_kfull(uint32_t b, int s) { return b + OFF_BAR + 8u * s; }
+__device__ __forceinline__ uint32_t bar_kempty(uint32_t b, int s) { return b + OFF_BAR + 8u * (kStages + s); }
+__device__ __forceinline__ uint32_t bar_sfready(uint32_t b, int s) { return b + OFF_BAR + 8u * (2 * kStages + s); }
+__device__ __forceinline__ uint32_t bar_qfull(uint32_t b, int q) { return b + OFF_BAR + 8u * (3 * kStages + q); }
+__device__ __forceinline__ uint32_t bar_qempty(uint32_t b, int q) { return b + OFF_BAR + 8u * (3 * kStages + 2 + q); }
+__device__ __forceinline__ uint32_t bar_qsf(uint32_t b, int q) { return b + OFF_BAR + 8u * (3 * kStages + 4 + q); }
+__device__ __forceinline__ uint32_t bar_accfull(uint32_t b, int s) { return b + OFF_BAR + 8u * (3 * kStages + 6 + s); }
+__device__ __forceinline__ uint32_t bar_accempty(uint32_t b, int s) {
+  return b + OFF_BAR + 8u * (3 * kStages + 6 + kSlots + s);
+}
+
+struct LogitsParams {
+  const uint8_t* q_payload;
+  const uint8_t* q_scale;
+  const float* w;
+  const uint8_t* payload;
+  const uint8_t* scale;
+  int64_t num_pages;
+  const int32_t* page_table;
+  int64_t num_seqs;
+  int32_t max_pages;
+  const int32_t* row_seq;
+  const int32_t* context_lens;
+  int32_t max_context;
+  int32_t n_rows;
+  const void* schedule;
+  float* out;
+  int64_t out_stride;
+  int32_t* status;
+};
+
+struct Ctl {
+  volatile int32_t* abort;
+  int32_t* status;
+};
+
+// Bounded wait on an mbarrier phase, polled by the whole warp.  False on timeout or when
+// another warp has aborted; the result is uniform across the warp.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort = true) {
+  bool ok = ptx::mbar_try_wait(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+      if (ptx::mbar_try_wait(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if ((it & 63u) == 0) {
+        if (honor_abort && *c.abort) break;
+        if (ptx::globaltimer() - t0 > kTimeoutNs) {
+          *c.abort = 1;
+          record_error(c.status, FP4IDX_ERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(kFull, ok);
+}
+
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return a | (b << 8) | (c << 16) | (d << 24);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sb = ptx::smem_addr(smem);
+
+  // The schedule must describe exactly these rows and this grid.
+  const SchedView sv = sched_view(const_cast<void*>(p.schedule), p.n_rows);
+  const SchedHeader hdr = *sv.hdr;
+  if (hdr.magic != kSchedMagic || hdr.n_rows != p.n_rows || hdr.num_ctas != (int32_t)gridDim.x ||
+      hdr.group_max != kGroupMax) {
+    if (threadIdx.x == 0) record_error(p.status, FP4IDX_ERR_SCHEDULE);
+    return;
+  }
+
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + OFF_MISC + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; s++) {
+      ptx::mbar_init(bar_kfull(sb, s), 1);
+      ptx::mbar_init(bar_kempty(sb, s), 1);
+      ptx::mbar_init(bar_sfready(sb, s), 1);
+    }
+    for (int q = 0; q < 2; q++) {
+      ptx::mbar_init(bar_qfull(sb, q), 1);
+      ptx::mbar_init(bar_qempty(sb, q), 1);
+      ptx::mbar_init(bar_qsf(sb, q), 1);
+    }
+    for (int s = 0; s < kSlots; s++) {
+      ptx::mbar_init(bar_accfull(sb, s), 1);
+      ptx::mbar_init(bar_accempty(sb, s), 4);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpMma) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{abort_flag, p.status};
+
+  ItemIter items;
+  items.init(sv, blockIdx.x, gridDim.x);
+  int32_t g, t0, t1;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    uint32_t kctr = 0, ictr = 0;
+    bool ok = true;
+    while (ok && items.next(g, t0, t1)) {
+      const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
+      const int32_t seq = __ldg(p.row_seq + r0);
+      const bool seq_ok = seq >= 0 && (int64_t)seq < p.num_seqs;
+      int32_t maxlen = sv.maxlen[g];
+      maxlen = min(maxlen, min(p.max_context, p.max_pages * kPage));
+      const int32_t npages = (maxlen + kPage - 1) / kPage;
+      const int qb = ictr & 1;
+      ok = wait_warp(bar_qempty(sb, qb), ((ictr >> 1) & 1) ^ 1, ctl);
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t qbar = bar_qfull(sb, qb);
+        ptx::mbar_arrive_expect_tx(qbar, (uint32_t)rows * (4096u + 256u));
+        ptx::bulk_g2s(sb + OFF_QPAY + qb * kQPayBytes, p.q_payload + (int64_t)r0 * 4096, rows * 4096u, qbar);
+        ptx::bulk_g2s(sb + OFF_QSC + qb * kQScBytes, p.q_scale + (int64_t)r0 * 256, rows * 256u, qbar);
+      }
+      if (lane == 0 && !seq_ok) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
+      const int32_t* pt = p.page_table + (int64_t)(seq_ok ? seq : 0) * p.max_pages;
+      // lane l holds the physical page of logical page 2*chunk + l (16 tiles per chunk)
+      int32_t chunk = t0;
+      int32_t lpa = 2 * chunk + lane;
+      int32_t pid_cur = (seq_ok && lpa < npages) ? __ldg(pt + lpa) : -1;
+      int32_t lpb = 2 * (chunk + 16) + lane;
+      int32_t pid_next = (seq_ok && lpb < npages) ? __ldg(pt + lpb) : -1;
+      for (int32_t i = t0; i < t1; i++) {
+        if (i - chunk == 16) {
+          chunk += 16;
+          pid_cur = pid_next;
+          lpb = 2 * (chunk + 16) + lane;
+          pid_next = (seq_ok && lpb < npages) ? __ldg(pt + lpb) : -1;
+        }
+        const int s = kctr % kStages;
+        ok = wait_warp(bar_kempty(sb, s), ((kctr / kStages) & 1) ^ 1, ctl);
+        if (!ok) break;
+        const int32_t pg0 = __shfl_sync(kFull, pid_cur, 2 * (i - chunk));
+        const int32_t pg1 = __shfl_sync(kFull, pid_cur, 2 * (i - chunk) + 1);
+        const bool need0 = 2 * i < npages, need1 = 2 * i + 1 < npages;
+        const bool v0 = need0 && pg0 >= 0 && (int64_t)pg0 < p.num_pages;
+        const bool v1 = need1 && pg1 >= 0 && (int64_t)pg1 < p.num_pages;
+        if (lane == 0 && seq_ok && ((need0 && !v0) || (need1 && !v1))) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
+        const uint32_t kbar = bar_kfull(sb, s);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(kbar, (v0 ? 4352u : 0u) + (v1 ? 4352u : 0u));
+        __syncwarp();
+        if (lane < 8) {
+          const int pp = lane >> 2, c = lane & 3;
+          const bool v = pp ? v1 : v0;
+          const int32_t pg = pp ? pg1 : pg0;
+          if (v)
+            ptx::bulk_g2s(sb + OFF_KPAY + s * kKPayBytes + c * 2048 + pp * 1024,
+                          p.payload + ((int64_t)pg * 4 + c) * 1024, 1024u, kbar);
+        } else if (lane < 10) {
+          const int pp = lane - 8;
+          const bool v = pp ? v1 : v0;
+          const int32_t pg = pp ? pg1 : pg0;
+          if (v) ptx::bulk_g2s(sb + OFF_KSC + s * kKScBytes + pp * 256, p.scale + (int64_t)pg * 256, 256u, kbar);
+        }
+        kctr++;
+      }
+      ictr++;
+    }
+    // Tail: every copy issued must land, and (when not aborting) every stage must be
+    // released by the MMAs that read it, before the CTA may exit.
+    for (uint32_t u = (kctr > (uint32_t)kStages ? kctr - kStages : 0); u < kctr; u++) {
+      wait_warp(bar_kfull(sb, u % kStages), (u / kStages) & 1, ctl, false);
+      if (!*abort_flag) wait_warp(bar_kempty(sb, u % kStages), (u / kStages) & 1, ctl);
+    }
+    for (uint32_t u = (ictr > 2u ? ictr - 2 : 0); u < ictr; u++) {
+      wait_warp(bar_qfull(sb, u & 1), (u >> 1) & 1, ctl, false);
+      if (!*abort_flag) wait_warp(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    uint32_t kctr = 0, ictr = 0, sctr = 0;
+    bool ok = true;
+    constexpr uint32_t kIdesc0 = ptx::idesc_mxf4(64, 0, 0);
+    constexpr uint32_t kIdesc1 = ptx::idesc_mxf4(64, 2, 2);
+    while (ok && items.next(g, t0, t1)) {
+      const int32_t rows = sv.row0[g + 1] - sv.row0[g];
+      const int qb = ictr & 1;
+      const uint32_t qph = (ictr >> 1) & 1;
+      ok = wait_warp(bar_qfull(sb, qb), qph, ctl) && wait_warp(bar_qsf(sb, qb), qph, ctl);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (lane == 0)
+        for (int r = 0; r < rows; r++)
+          ptx::tmem_cp_sf_atom(tmem + kColSfb + (qb * kGroupMax + r) * 4,
+                               sb + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes);
+      __syncwarp();
+      for (int32_t i = t0; i < t1 && ok; i++) {
+        const int s = kctr % kStages;
+        const uint32_t kph = (kctr / kStages) & 1;
+        ok = wait_warp(bar_kfull(sb, s), kph, ctl) && wait_warp(bar_sfready(sb, s), kph, ctl);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (lane == 0) ptx::tmem_cp_sf_atom(tmem + kColSfa + s * 4, sb + OFF_KATOM + s * kAtomBytes);
+        __syncwarp();
+        const uint32_t a0 = sb + OFF_KPAY + s * kKPayBytes;
+        for (int r = 0; r < rows; r++) {
+          const int slot = sctr % kSlots;
+          ok = wait_warp(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t b0 = sb + OFF_QPAY + qb * kQPayBytes + r * 4096;
+            const uint32_t d = tmem + kColAcc + slot * 64;
+            const uint32_t sfa = tmem + kColSfa + s * 4;
+            const uint32_t sfbt = tmem + kColSfb + (qb * kGroupMax + r) * 4;
+            ptx::mma_mxf4(d, ptx::smem_desc(a0, 2048, 128), ptx::smem_desc(b0, 1024, 128), kIdesc0, sfa, sfbt, 0);
+            ptx::mma_mxf4(d, ptx::smem_desc(a0 + 4096, 2048, 128), ptx::smem_desc(b0 + 2048, 1024, 128), kIdesc1,
+                          sfa, sfbt, 1);
+            ptx::mma_commit(bar_accfull(sb, slot));
+          }
+          __syncwarp();
+          sctr++;
+        }
+        if (!ok) break;
+        if (lane == 0) ptx::mma_commit(bar_kempty(sb, s));
+        __syncwarp();
+        kctr++;
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::mma_commit(bar_qempty(sb, qb));
+      __syncwarp();
+      ictr++;
+    }
+  } else if (warp == kWarpSf) {
+    // ------------------------------------------------------------ scale transposer
+    uint32_t kctr = 0, ictr = 0;
+    bool ok = true;
+    while (ok && items.next(g, t0, t1)) {
+      const int32_t rows = sv.row0[g + 1] - sv.row0[g];
+      const int qb = ictr & 1;
+      ok = wait_warp(bar_qfull(sb, qb), (ictr >> 1) & 1, ctl);
+      if (!ok) break;
+      for (int r = 0; r < rows; r++) {
+        // query rows: B operand of 64 heads; atom row r0 holds heads r0 and 32 + r0
+        const uint8_t* src = smem + OFF_QSC + qb * kQScBytes + r * 256;  // [c][64 heads]
+        uint4 v;
+        v.x = pack4(src[lane], src[64 + lane], src[128 + lane], src[192 + lane]);
+        v.y = pack4(src[32 + lane], src[96 + lane], src[160 + lane], src[224 + lane]);
+        v.z = 0u;
+        v.w = 0u;
+        *reinterpret_cast<uint4*>(smem + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes + lane * 16) = v;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_qsf(sb, qb));
+      for (int32_t i = t0; i < t1; i++) {
+        const int s = kctr % kStages;
+        ok = wait_warp(bar_kfull(sb, s), (kctr / kStages) & 1, ctl);
+        if (!ok) break;
+        // K tile: A operand of 128 tokens; token m = 64*page + j; atom row r0 holds tokens
+        // r0, 32 + r0 (page 0) and 64 + r0, 96 + r0 (page 1)
+        const uint8_t* src = smem + OFF_KSC + s * kKScBytes;  // [page][c][64]
+        uint4 v;
+        v.x = pack4(src[lane], src[64 + lane], src[128 + lane], src[192 + lane]);
+        v.y = pack4(src[32 + lane], src[96 + lane], src[160 + lane], src[224 + lane]);
+        v.z = pack4(src[256 + lane], src[320 + lane], src[384 + lane], src[448 + lane]);
+        v.w = pack4(src[288 + lane], src[352 + lane], src[416 + lane], src[480 + lane]);
+        *reinterpret_cast<uint4*>(smem + OFF_KATOM + s * kAtomBytes + lane * 16) = v;
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_sfready(sb, s));
+        kctr++;
+      }
+      ictr++;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - kWarpEpi0;  // 0..3: private copy of the group's weights
+    const int quad = warp & 3;        // TMEM lanes this warp may read
+    const int m = quad * 32 + lane;   // token row of the tile
+    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + ew * kGroupMax * 64;
+    int32_t* lsm = reinterpret_cast<int32_t*>(smem + OFF_LEN) + ew * kGroupMax;
+    uint32_t sctr = 0;
+    bool ok = true;
+    while (ok && items.next(g, t0, t1)) {
+      const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
+      __syncwarp();
+      for (int idx = lane; idx < rows * 64; idx += 32) wsm[idx] = __ldg(p.w + (int64_t)r0 * 64 + idx);
+      if (lane < rows) {
+        int32_t L = __ldg(p.context_lens + r0 + lane);
+        if (L < 0 || L > p.max_context) {
+          if (ew == 0) record_error(p.status, FP4IDX_ERR_BAD_LENGTH);
+          L = L < 0 ? 0 : p.max_context;
+        }
+        lsm[lane] = L;
+      }
+      __syncwarp();
+      for (int32_t i = t0; i < t1 && ok; i++) {
+        const int32_t tok = i * kTileTokens + m;
+        for (int r = 0; r < rows; r++) {
+          const int slot = sctr % kSlots;
+          ok = wait_warp(bar_accfull(sb, slot), (sctr / kSlots) & 1, ctl);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          float d[64];
+          ptx::tmem_ld64_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + slot * 64, d);
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar_accempty(sb, slot));
+          if (tok < lsm[r]) {
+            const float* wr = wsm + r * 64;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 64; h += 4) {
+              const float4 wv = *reinterpret_cast<const float4*>(wr + h);
+              a0 = fmaf(wv.x, fmaxf(d[h + 0], 0.f), a0);
+              a1 = fmaf(wv.y, fmaxf(d[h + 1], 0.f), a1);
+              a2 = fmaf(wv.z, fmaxf(d[h + 2], 0.f), a2);
+              a3 = fmaf(wv.w, fmaxf(d[h + 3], 0.f), a3);
+            }
+            p.out[(int64_t)(r0 + r) * p.out_stride + tok] = (a0 + a1) + (a2 + a3);
+          }
+          sctr++;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int32_t n_rows,
+                               const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                               const int32_t* page_table, int64_t num_seqs, int32_t max_pages,
+                               const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
+                               const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
+                               int32_t* status, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(logits_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  LogitsParams prm;
+  prm.q_payload = q_payload;
+  prm.q_scale = q_scale;
+  prm.w = w;
+  prm.payload = payload;
+  prm.scale = scale;
+  prm.num_pages = num_pages;
+  prm.page_table = page_table;
+  prm.num_seqs = num_seqs;
+  prm.max_pages = max_pages;
+  prm.row_seq = row_seq;
+  prm.context_lens = context_lens;
+  prm.max_context = max_context;
+  prm.n_rows = n_rows;
+  prm.schedule = schedule;
+  prm.out = out;
+  prm.out_stride = out_stride;
+  prm.status = status;
+  logits_mxf4_kernel<<<num_ctas, kThreads, kSmemBytes, stream>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4idx

@@ -1,0 +1,121 @@
+// Length-balanced split of the logits work over the grid.
+//
+// dsv4.1-amd: KV cache layouts, FP4 indexer, compressor and router kernels -- Summary:
+// the in-tree decode schedule writes its work list in dispatches whose registers do not
+// grow with the row count (the single-kernel schedule it replaced spilled past ~1K rows
+// and broke graph capture at 1,536 rows).  [AMD] Enable FP4 indexer for Deepseek V4 --
+// Attention runtime: decode schedules are built during graph capture and reused by all
+// C4 layers of a forward.
+//
+// Here: one CTA of 1024 threads walks the rows in chunks of 1024 with carried block
+// scans (registers fixed, any row count), entirely on the device: capturable, no host
+// synchronisation, a pure function of its inputs.
+#include "fp4idx_internal.cuh"
+#include "schedule.cuh"
+
+namespace fp4idx {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+// Inclusive block scan (sum or max) of a 64-bit value; every thread gets its prefix and
+// the block total.  `scratch` holds kWarps entries.
+template <bool kMax>
+__device__ int64_t block_scan(int64_t v, int64_t* scratch, int64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v = kMax ? (n > v ? n : v) : v + n;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < kWarps ? scratch[lane] : (kMax ? INT64_MIN : 0);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t n = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w = kMax ? (n > w ? n : w) : w + n;
+    }
+    if (lane < kWarps) scratch[lane] = w;
+  }
+  __syncthreads();
+  if (warp > 0) {
+    int64_t p = scratch[warp - 1];
+    v = kMax ? (p > v ? p : v) : v + p;
+  }
+  total = scratch[kWarps - 1];
+  __syncthreads();
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t* __restrict__ context_lens,
+                                                                  const int32_t* __restrict__ row_seq,
+                                                                  int32_t n_rows, int32_t num_ctas, void* ws) {
+  __shared__ int64_t scratch[kWarps];
+  SchedView s = sched_view(ws, n_rows);
+  const int tid = threadIdx.x;
+
+  // Phase A: group starts.  run_start(t) = last t' <= t where row_seq changes; a group
+  // starts where (t - run_start) is a multiple of kGroupMax.
+  int64_t carry_run = 0, carry_groups = 0;
+  for (int32_t base = 0; base < n_rows; base += kThreads) {
+    const int32_t t = base + tid;
+    const bool valid = t < n_rows;
+    int32_t rs = valid ? row_seq[t] : 0;
+    const bool seg = valid && (t == 0 || rs != row_seq[t - 1]);
+    int64_t run_tot, tot;
+    const int64_t run = block_scan<true>(seg ? (int64_t)t : carry_run, scratch, run_tot);
+    const bool gstart = valid && ((t - run) % kGroupMax == 0);
+    const int64_t cnt = block_scan<false>(gstart ? 1 : 0, scratch, tot);
+    if (gstart) s.row0[carry_groups + cnt - 1] = t;
+    carry_groups += tot;
+    carry_run = run_tot;
+  }
+  const int32_t n_groups = (int32_t)carry_groups;
+  if (tid == 0) s.row0[n_groups] = n_rows;
+  __syncthreads();
+
+  // Phase B: per-group longest (clamped) context and cost prefix.
+  int64_t carry_cost = 0;
+  if (tid == 0) s.prefix[0] = 0;
+  for (int32_t base = 0; base < n_groups; base += kThreads) {
+    const int32_t g = base + tid;
+    int64_t cost = 0;
+    if (g < n_groups) {
+      const int32_t r0 = s.row0[g], r1 = s.row0[g + 1];
+      int32_t mx = 0;
+      for (int32_t r = r0; r < r1; r++) {
+        int32_t L = context_lens[r];
+        L = L < 0 ? 0 : (L > FP4IDX_MAX_CONTEXT ? FP4IDX_MAX_CONTEXT : L);
+        mx = L > mx ? L : mx;
+      }
+      s.maxlen[g] = mx;
+      cost = ceil_div64(mx, kTileTokens) * (int64_t)(kTileCost + (r1 - r0));
+    }
+    int64_t tot;
+    int64_t inc = block_scan<false>(cost, scratch, tot);
+    if (g < n_groups) s.prefix[g + 1] = carry_cost + inc;
+    carry_cost += tot;
+  }
+  if (tid == 0) {
+    s.hdr->magic = kSchedMagic;
+    s.hdr->n_rows = n_rows;
+    s.hdr->num_ctas = num_ctas;
+    s.hdr->n_groups = n_groups;
+    s.hdr->total_cost = carry_cost;
+    s.hdr->group_max = kGroupMax;
+    s.hdr->reserved = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int32_t n_rows,
+                                  int32_t num_ctas, void* ws, cudaStream_t stream) {
+  build_schedule_kernel<<<1, kThreads, 0, stream>>>(context_lens, row_seq, n_rows, num_ctas, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4idx
