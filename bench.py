@@ -1,0 +1,519 @@
+#!/usr/bin/env python
+"""Throughput of the FP4 indexer decode step on GB300.
+
+One step = the whole hot path over one decode batch: K store of each sequence's
+newest compressed token, Q quant, schedule, paged-MQA logits, top-k.  Default
+workload: 64 sequences x 1 query row, context lengths ~U[8192, 32768] compressed
+tokens, pages from a permuted 40,960-page pool, 64 heads x 128, k = 2,048.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fp4idx|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on this
+host's cores on the same workload (rows sampled per step).  Under torchrun each
+rank runs its own replica of the batch (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP4 indexer decode: K-cache GB/s vs HBM peak; query rows/s (logits+top-k)"
+UNIT = "query rows/s"
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_decode_b64_traffic.json")
+LOGITS_SRC = os.path.join(ROOT, "sparse_attention_fp4_gb300", "csrc", "logits_mxf4.cu")
+KERNELS_PER_STEP = 5  # store_k, quant_q, build_schedule, logits, topk
+
+WORKLOADS = {
+    "decode_b64": ("decode_batch64", 1001),
+    "tiny": ("tiny_decode", 1000),
+    "draft_b256": ("draft_batch256", 1002),
+    "prefill": ("prefill_chunk", 1003),
+}
+
+
+# ------------------------------------------------------------------ distributed plumbing (timing only)
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def dist_reduce(value: float, op: str, device=None) -> float:
+    """max or sum of a host scalar over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(rows_this_rank: int, seconds_this_rank: float, device=None):
+    """Whole-job throughput: all ranks' rows over the slowest rank's time."""
+    total_rows = dist_reduce(rows_this_rank, "sum", device)
+    slowest = dist_reduce(seconds_this_rank, "max", device)
+    return total_rows / slowest, slowest
+
+
+# ------------------------------------------------------------------ workload
+def make_batch(name):
+    from sparse_attention_fp4_gb300 import workloads as wl
+    fn, seed = WORKLOADS[name]
+    return getattr(wl, fn)(seed)
+
+
+def newest_rows(b):
+    """Per sequence with stored tokens: (sequence id, index of its newest K row).  The
+    K rows are stored sequence by sequence in token order."""
+    toks = b.seq_tokens.astype(np.int64)
+    ends = np.cumsum(toks) - 1
+    seqs = np.nonzero(toks > 0)[0]
+    return seqs, ends[seqs]
+
+
+def algorithmic_bytes(b):
+    """Bytes the logits pass must move at minimum: the K cache of every visible token
+    (64 B payload + 4 B scale), the packed queries (4,352 B/row), head weights
+    (256 B/row), page ids and row metadata.  Logits kept on chip; top-k output 4 B/index."""
+    L = b.context_lens.astype(np.int64)
+    T = b.n_rows
+    pages = np.ceil(L / 64.0).sum()
+    kbytes = 68.0 * L.sum()
+    logits_pass = kbytes + 4352.0 * T + 256.0 * T + 4.0 * pages + 8.0 * T
+    return dict(k_cache=kbytes, logits_pass=logits_pass, topk_out=4.0 * T * b.topk)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.dirname(LOGITS_SRC))):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(os.path.dirname(LOGITS_SRC), f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", "fp4idx_clocks_%d.csv" % os.getpid())
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", self.gpu_id, "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                    power.append(float(p[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def gpu_id_for(device_index):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device_index)
+
+
+# ------------------------------------------------------------------ the GPU arm
+class DecodeStep:
+    """Device-resident inputs of one decode batch and the five launches of a step."""
+
+    def __init__(self, b, device):
+        import torch
+
+        from sparse_attention_fp4_gb300 import fp4idx
+        from sparse_attention_fp4_gb300 import workloads as wl
+        self.fp4idx = fp4idx
+        self.b = b
+        self.device = device
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+        def dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+        ks = b.kstore
+        self.cs = bf16(wl.rope_cos_sin_table())
+        self.payload, self.scale = fp4idx.alloc_cache(b.num_pages, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # fill the cache (setup, untimed)
+        chunk = 1 << 20
+        nw = bf16(ks.norm_w)
+        for r0 in range(0, ks.n_rows, chunk):
+            r1 = min(ks.n_rows, r0 + chunk)
+            fp4idx.store_k(bf16(ks.k_rows[r0:r1]), dev(ks.positions[r0:r1]), dev(ks.slots[r0:r1]), nw, ks.eps,
+                           self.cs, self.payload, self.scale, status=self.status)
+        _, idx = newest_rows(b)
+        self.h_new = dict(k=np.ascontiguousarray(ks.k_rows[idx]), pos=np.ascontiguousarray(ks.positions[idx]),
+                          slots=np.ascontiguousarray(ks.slots[idx]))
+        self.new_k = bf16(self.h_new["k"])
+        self.new_pos = dev(self.h_new["pos"])
+        self.new_slots = dev(self.h_new["slots"])
+        self.norm_w = nw
+        self.eps = ks.eps
+        self.q = bf16(b.q)
+        self.qpos = dev(b.q_positions)
+        self.w = dev(b.w)
+        self.pt = dev(b.page_table)
+        self.rs = dev(b.row_seq)
+        self.cl = dev(b.context_lens)
+        self.T = b.n_rows
+        self.k = b.topk
+        self.max_ctx = int(max(1, b.context_lens.max()))
+        self.qp, self.qs = fp4idx.alloc_query(self.T, device=device)
+        self.sched = torch.empty(fp4idx.schedule_workspace_bytes(self.T), dtype=torch.uint8, device=device)
+        self.logits = torch.empty((self.T, (self.max_ctx + 3) // 4 * 4), dtype=torch.float32, device=device)
+        self.topk = torch.empty((self.T, self.k), dtype=torch.int32, device=device)
+        torch.cuda.synchronize(device)
+
+    def launch(self, events=None):
+        f = self.fp4idx
+        ev = events or [None] * 6
+        if ev[0] is not None:
+            ev[0].record()
+        f.store_k(self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.cs, self.payload, self.scale,
+                  status=self.status)
+        if ev[1] is not None:
+            ev[1].record()
+        f.quant_q(self.q, self.qpos, self.cs, self.qp, self.qs, status=self.status)
+        if ev[2] is not None:
+            ev[2].record()
+        f.build_schedule(self.cl, self.rs, self.sched)
+        if ev[3] is not None:
+            ev[3].record()
+        f.logits(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl, self.max_ctx,
+                 self.sched, self.logits, status=self.status)
+        if ev[4] is not None:
+            ev[4].record()
+        f.topk(self.logits, self.cl, self.max_ctx, self.k, self.topk, status=self.status)
+        if ev[5] is not None:
+            ev[5].record()
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init("nccl")
+    b = make_batch(args.workload)
+    st = DecodeStep(b, device)
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush_l2():
+        flush_w.zero_()
+        _ = flush_r.sum()
+
+    # warm-up (also sets kernel attributes before capture)
+    for _ in range(max(3, args.warmup)):
+        st.launch()
+    torch.cuda.synchronize()
+    assert st.fp4idx.read_status(st.status) == 0, "device status after warm-up"
+
+    # the step as one CUDA graph (decode steps replay captured graphs)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        st.launch()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        st.launch()
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+
+    spin_cycles = int(2e5)  # ~0.1 ms at GB300 clocks: covers the host's enqueue of the next step
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_id_for(local)).start()
+    time.sleep(0.3)
+    dist_barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush_l2()
+        torch.cuda._sleep(spin_cycles)
+        starts[i].record()
+        g.replay()
+        ends[i].record()
+    torch.cuda.synchronize()
+    dist_barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
+    total_s = sum(step_ms) / 1e3
+    value, slowest = aggregate(st.T * K, total_s, device)
+    ms_per_step = slowest / K * 1e3
+
+    # per-kernel breakdown on the same stream (direct launches, L2 flushed)
+    Kb = min(K, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kb)]
+    for i in range(Kb):
+        flush_l2()
+        torch.cuda._sleep(spin_cycles * 4)
+        st.launch(evs[i])
+    torch.cuda.synchronize()
+    names = ["store_k", "quant_q", "build_schedule", "logits", "topk"]
+    per = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(Kb)]) * 1e3
+           for j, n in enumerate(names)}
+    logits_us = statistics.mean([evs[i][3].elapsed_time(evs[i][4]) for i in range(Kb)]) * 1e3
+    status = st.fp4idx.read_status(st.status)
+
+    ab = algorithmic_bytes(b)
+    peak, peak_kind = measured_peaks()
+    achieved = ab["logits_pass"] / (logits_us * 1e-6) / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == args.workload:
+            traffic = tr.get("dram_bytes_per_launch")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "logits_mxf4_kernel",
+                "algorithmic_bytes": ab["logits_pass"], "avg_launch_us": round(logits_us, 2),
+                "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
+
+    e2e = run_e2e(st, args, flush_l2) if not args.no_e2e else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(b, args)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1,ue8m0)->f32", "data": "synthetic",
+            "config": {"workload": b.name, "rows": b.n_rows, "heads": 64, "head_dim": 128, "topk": b.topk,
+                       "context_tokens": int(b.context_lens.sum()), "cache_pages": b.num_pages,
+                       "step": "K store (newest token per sequence) + Q quant + schedule + logits + top-k, "
+                               "one CUDA graph replay",
+                       "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "kcache_gbs": round(ab["k_cache"] / (logits_us * 1e-6) / 1e9, 1),
+            "kernel_us_median": {k: round(v, 2) for k, v in per.items()},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * K,
+            "clocks": clocks,
+            "wall_s_timed_region": round(t_wall, 3),
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(st, args, flush_l2):
+    """Same metric through the C ABI with host buffers: every step copies its inputs from
+    pinned host memory, runs the five calls and reads the selection back."""
+    import torch
+    b = st.b
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h = dict(k=pin(st.h_new["k"].view(np.int16)), pos=pin(st.h_new["pos"]), slots=pin(st.h_new["slots"]),
+             q=pin(b.q.view(np.int16)), qpos=pin(b.q_positions), w=pin(b.w), pt=pin(b.page_table),
+             rs=pin(b.row_seq), cl=pin(b.context_lens))
+    out = torch.empty((st.T, st.k), dtype=torch.int32).pin_memory()
+    dst = dict(k=st.new_k.view(torch.int16), pos=st.new_pos, slots=st.new_slots, q=st.q.view(torch.int16),
+               qpos=st.qpos, w=st.w, pt=st.pt, rs=st.rs, cl=st.cl)
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out.numel() * out.element_size()
+    K = min(args.steps, 200)
+    times = []
+    for i in range(K + 3):
+        flush_l2()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for key, t in h.items():
+            dst[key].copy_(t, non_blocking=True)
+        st.launch()
+        out.copy_(st.topk, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    value, _ = aggregate(st.T * K, sum(times), st.device)
+    return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": K, "ms_per_step": round(sum(times) / K * 1e3, 4)}
+
+
+# ------------------------------------------------------------------ the CPU oracle (baseline / reference arm)
+class OracleStep:
+    def __init__(self, b):
+        import oracle
+        from sparse_attention_fp4_gb300 import workloads as wl
+        self.oracle = oracle
+        self.b = b
+        self.cs = wl.rope_cos_sin_table()
+        self.payload, self.scale, st = oracle.store_k(b.kstore, self.cs)  # cache fill: setup, untimed
+        assert st == 0
+        self.new_seqs, idx = newest_rows(b)
+        ks = b.kstore
+        from sparse_attention_fp4_gb300.workloads import KStoreInputs
+        self.new = KStoreInputs(ks.k_rows[idx], ks.positions[idx], ks.slots[idx], ks.norm_w, ks.eps, ks.num_pages)
+
+    def run(self, rows):
+        """The step for a sample of query rows: K store of the newest rows of their
+        sequences, Q quant, logits and top-k of those rows.  Returns seconds."""
+        o = self.oracle
+        b = self.b
+        t0 = time.perf_counter()
+        seqs = set(int(s) for s in b.row_seq[rows])
+        sel = [i for i, s in enumerate(self.new_seqs) if int(s) in seqs]
+        from sparse_attention_fp4_gb300.workloads import KStoreInputs
+        new = KStoreInputs(self.new.k_rows[sel], self.new.positions[sel], self.new.slots[sel], self.new.norm_w,
+                           self.new.eps, self.new.num_pages)
+        o.store_k(new, self.cs, self.payload, self.scale)
+        qp, qs, _ = o.quant_q(b.q[rows], b.q_positions[rows], self.cs)
+        lg, _, _ = o.logits(qp, qs, b.w[rows], self.payload, self.scale, b.page_table, b.row_seq[rows],
+                            b.context_lens[rows], with_bound=False)
+        for i, t in enumerate(rows):
+            o.topk(lg[i], int(b.context_lens[t]), b.topk)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(b, args):
+    import oracle
+    cores = oracle.max_threads()
+    step = OracleStep(b)
+    rows_per = 8
+    done, secs, i = 0, 0.0, 0
+    while secs < args.cpu_seconds and done < b.n_rows * 4:
+        rows = np.arange(i, i + rows_per) % b.n_rows
+        secs += step.run(rows)
+        done += rows_per
+        i += rows_per
+    return {"value": round(done / secs, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d query rows (%d per call, full contexts) of the same workload incl. K store of their "
+                      "newest tokens, Q quant, binary64 logits and top-k; %.1f s" % (done, rows_per, secs)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    b = make_batch(args.workload)
+    step = OracleStep(b)
+    cores = oracle.max_threads()
+    rows_per = 8
+    for i in range(3):  # warm-up: page in the oracle and its inputs
+        step.run(np.arange(i * rows_per, (i + 1) * rows_per) % b.n_rows)
+    secs = 0.0
+    for i in range(args.steps):
+        secs += step.run(np.arange(i * rows_per, (i + 1) * rows_per) % b.n_rows)
+    value = rows_per * args.steps / secs
+    sample = "%d query rows per step (full contexts), %d steps" % (rows_per, args.steps)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": b.name, "rows_sampled_per_step": rows_per, "topk": b.topk},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["fp4idx", "reference"], default="fp4idx")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_b64")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

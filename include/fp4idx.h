@@ -165,6 +165,21 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
                        size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                        float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream);
 
+/*
+ * The two halves of fp4idx_logits_topk, for callers that want the logits themselves or
+ * select elsewhere.  fp4idx_logits writes logits_out[t][s] for s < context_lens[t]
+ * (logits_stride >= max_context; the rest of each row is not written).  fp4idx_topk
+ * selects from such a buffer: topk_idx[t] = the k largest of logits[t][0..L_t), ascending
+ * positions, -1 padding; ties at the k-th value go to the lower positions.
+ */
+int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows, int32_t n_heads,
+                  const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
+                  int64_t num_seqs, int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
+                  int32_t max_context, const void* schedule, size_t schedule_bytes, float* logits_out,
+                  int64_t logits_stride, int32_t* status_dev, void* stream);
+int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
+                int32_t max_context, int32_t k, int32_t* topk_idx, int32_t* status_dev, void* stream);
+
 /* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
  * a test/diagnostic helper, not for the hot path. */
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream);

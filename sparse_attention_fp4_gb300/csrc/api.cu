@@ -119,27 +119,83 @@ size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int3
   return (size_t)max_rows * (size_t)logits_row_stride(max_context) * sizeof(float);
 }
 
+namespace {
+
+int check_logits_args(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                      int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                      const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                      const int32_t* context_lens, int32_t max_context, const void* schedule, size_t schedule_bytes,
+                      int32_t* status_dev) {
+  if (n_rows < 0 || n_rows > INT32_MAX - 1 || num_pages < 0 || num_seqs < 0 || max_pages < 0 || max_context < 0)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
+  if (max_context > FP4IDX_MAX_CONTEXT) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!q_payload || !q_scale || !w || !payload || !scale || !page_table || !row_seq || !context_lens || !schedule)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(q_payload) || !aligned16(q_scale) || !aligned16(w) || !aligned16(payload) || !aligned16(scale) ||
+      !aligned4(page_table) || !aligned4(row_seq) || !aligned4(context_lens) || !aligned16(schedule))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  if (schedule_bytes < fp4idx::sched_bytes(n_rows)) return FP4IDX_ERR_WORKSPACE;
+  return FP4IDX_OK;
+}
+
+int launch_logits_checked(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                          const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
+                          int64_t num_seqs, int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
+                          int32_t max_context, const void* schedule, float* buf, int64_t stride, int32_t* status_dev,
+                          cudaStream_t s) {
+  int32_t grid = 0;
+  int st = device_sms(&grid);
+  if (st != FP4IDX_OK) return st;
+  return from_cuda(fp4idx::launch_logits_mxf4(q_payload, q_scale, w, (int32_t)n_rows, payload, scale, num_pages,
+                                              page_table, num_seqs, max_pages, row_seq, context_lens, max_context,
+                                              schedule, grid, buf, stride, status_dev, s));
+}
+
+}  // namespace
+
+int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows, int32_t n_heads,
+                  const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
+                  int64_t num_seqs, int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
+                  int32_t max_context, const void* schedule, size_t schedule_bytes, float* logits_out,
+                  int64_t logits_stride, int32_t* status_dev, void* stream) {
+  int st = check_logits_args(q_payload, q_scale, w, n_rows, n_heads, payload, scale, num_pages, page_table, num_seqs,
+                             max_pages, row_seq, context_lens, max_context, schedule, schedule_bytes, status_dev);
+  if (st != FP4IDX_OK || n_rows == 0) return st;
+  if (!logits_out || !aligned4(logits_out) || logits_stride < max_context) return FP4IDX_ERR_INVALID_ARG;
+  return launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs,
+                               max_pages, row_seq, context_lens, max_context, schedule, logits_out, logits_stride,
+                               status_dev, as_stream(stream));
+}
+
+int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
+                int32_t max_context, int32_t k, int32_t* topk_idx, int32_t* status_dev, void* stream) {
+  if (n_rows < 0 || n_rows > INT32_MAX - 1 || max_context < 0 || k < 1 || k > FP4IDX_MAX_TOPK)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (max_context > FP4IDX_MAX_CONTEXT) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!logits || !context_lens || !topk_idx || !aligned4(logits) || !aligned4(context_lens) || !aligned4(topk_idx) ||
+      logits_stride < max_context)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_topk(logits, logits_stride, context_lens, (int32_t)n_rows, max_context, k, topk_idx,
+                                       status_dev, as_stream(stream)));
+}
+
 int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
                        int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
                        const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
                        const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
                        size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                        float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream) {
-  if (n_rows < 0 || n_rows > INT32_MAX - 1 || num_pages < 0 || num_seqs < 0 || max_pages < 0)
-    return FP4IDX_ERR_INVALID_ARG;
-  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
-  if (k < 1 || k > FP4IDX_MAX_TOPK || max_context < 0) return FP4IDX_ERR_INVALID_ARG;
-  if (max_context > FP4IDX_MAX_CONTEXT) return FP4IDX_ERR_UNSUPPORTED;
+  int st = check_logits_args(q_payload, q_scale, w, n_rows, n_heads, payload, scale, num_pages, page_table, num_seqs,
+                             max_pages, row_seq, context_lens, max_context, schedule, schedule_bytes, status_dev);
+  if (st != FP4IDX_OK) return st;
+  if (k < 1 || k > FP4IDX_MAX_TOPK) return FP4IDX_ERR_INVALID_ARG;
   if (n_rows == 0) return FP4IDX_OK;
-  if (!q_payload || !q_scale || !w || !payload || !scale || !page_table || !row_seq || !context_lens || !schedule ||
-      !topk_idx)
-    return FP4IDX_ERR_INVALID_ARG;
-  if (!aligned16(q_payload) || !aligned16(q_scale) || !aligned16(w) || !aligned16(payload) || !aligned16(scale) ||
-      !aligned4(page_table) || !aligned4(row_seq) || !aligned4(context_lens) || !aligned16(schedule) ||
-      !aligned4(topk_idx))
-    return FP4IDX_ERR_INVALID_ARG;
-  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
-  if (schedule_bytes < fp4idx::sched_bytes(n_rows)) return FP4IDX_ERR_WORKSPACE;
+  if (!topk_idx || !aligned4(topk_idx)) return FP4IDX_ERR_INVALID_ARG;
   float* buf;
   int64_t stride;
   if (logits_out) {
@@ -152,14 +208,10 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
     if (workspace_bytes < fp4idx_logits_workspace_bytes(n_rows, max_context, k)) return FP4IDX_ERR_WORKSPACE;
     buf = reinterpret_cast<float*>(workspace);
   }
-  int32_t grid = 0;
-  int st = device_sms(&grid);
-  if (st != FP4IDX_OK) return st;
   cudaStream_t s = as_stream(stream);
-  cudaError_t e = fp4idx::launch_logits_mxf4(q_payload, q_scale, w, (int32_t)n_rows, payload, scale, num_pages,
-                                             page_table, num_seqs, max_pages, row_seq, context_lens, max_context,
-                                             schedule, grid, buf, stride, status_dev, s);
-  if (e != cudaSuccess) return FP4IDX_ERR_CUDA;
+  st = launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs, max_pages,
+                             row_seq, context_lens, max_context, schedule, buf, stride, status_dev, s);
+  if (st != FP4IDX_OK) return st;
   return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_idx,
                                        status_dev, s));
 }

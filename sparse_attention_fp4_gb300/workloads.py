@@ -102,6 +102,7 @@ class IndexerInputs:
     row_seq: np.ndarray       # [T] int32 sequence of each query row
     context_lens: np.ndarray  # [T] int32 compressed tokens visible to each row
     topk: int
+    seq_tokens: np.ndarray = None  # [S] int64 tokens stored per sequence (rows stored sequence by sequence)
 
     @property
     def n_rows(self) -> int:
@@ -175,7 +176,8 @@ def build_decode_batch(name, seed, seq_tokens, rows_per_seq_lens, pool_pages, to
         name=name,
         kstore=KStoreInputs(rows, pos, slots, norm_w, RMS_EPS, int(pool_pages)),
         q=q, q_positions=_decode_q_positions(lens), w=w, page_table=pt,
-        row_seq=row_seq, context_lens=lens, topk=int(topk))
+        row_seq=row_seq, context_lens=lens, topk=int(topk),
+        seq_tokens=np.asarray([int(x) for x in seq_tokens], dtype=np.int64))
 
 
 # --------------------------------------------------------------------------- the five workloads
