@@ -5,22 +5,28 @@
 // guarded page table; the logits are
 //   logits[t,s] = sum_h w[t,h] * ReLU(q_fp4[t,h] . k_fp4[s]),   s < context_lens[t].
 //
-// GB300 design (one persistent CTA per SM, 7 warps):
-//   warp 0  producer: per 128-token tile, two pages as 8 x 1 KB bulk copies into
-//           [block c][page][64 tokens][16 B] (a canonical no-swizzle K-major operand with
-//           M = 128 tokens) plus the two 256 B scale pages; per work item, the group's
-//           query rows (4 KB payload + 256 B scales each, one bulk copy each).  Page ids
-//           are read 32 at a time, one chunk ahead.
-//   warp 1  MMA issuer: copies the scale atoms to tensor memory (tcgen05.cp) and, per
-//           (tile, query row), issues two kind::mxf4 block-scaled MMAs (K = 64 each):
-//           D[128 tokens x 64 heads] in a 64-column TMEM slot (ring of 6 slots).
-//   warp 2  scale transposer: reorders the [c][token] scale bytes into the 32 x 16 B atom
-//           tcgen05.cp replicates over the four TMEM lane groups.
-//   warps 3-6 epilogue: thread = TMEM lane = token; ReLU, head-weighted sum, mask at the
-//           row's context length, coalesced fp32 store of the logits.
+// GB300 design (one persistent CTA per SM, 11 warps):
+//   A tile is 128 tokens = two cache pages, the A operand of an M = 128 MMA laid out as
+//   [block c][page][64 tokens][16 B] (canonical no-swizzle K-major).  A pipeline stage
+//   holds two tiles (four pages).
+//   warp 0  producer: per stage, four TMA tile::gather4 loads of the payload (each
+//           fetches the 1 KB rows (page, c) of two pages for two blocks, landing
+//           directly in the interleaved operand layout) and one gather4 of the four
+//           256 B scale pages; per work item, the group's query rows (one bulk copy
+//           for the payloads, one for the scales).  Page ids are read 32 at a time.
+//   warp 1  MMA issuer: copies scale atoms to tensor memory (tcgen05.cp) and, per
+//           (stage, query row), issues two kind::mxf4 MMAs (K = 64 each) per tile into
+//           a 128-column TMEM slot (2 slots): D[128 tokens x 64 heads] per tile.
+//   warp 2  scale transposer: reorders the [page][c][token] scale bytes into the
+//           32 x 16 B atom that tcgen05.cp replicates over the four TMEM lane groups.
+//   warps 3-10 epilogue, two per TMEM lane group taking alternate slots: thread =
+//           TMEM lane = token; ReLU, head-weighted sum, mask at the row's context
+//           length, coalesced fp32 store.
 // Work items come from the length-balanced schedule (schedule.cuh).  Every wait is
 // bounded: on expiry the CTA records FP4IDX_ERR_TIMEOUT, lets in-flight copies land,
 // frees its tensor memory and returns.
+#include <cuda.h>
+
 #include "fp4idx_internal.cuh"
 #include "ptx.cuh"
 #include "schedule.cuh"
@@ -28,9 +34,11 @@
 namespace fp4idx {
 namespace {
 
-constexpr int kStages = 8;
-constexpr int kSlots = 6;
-constexpr int kWarps = 7;
+constexpr int kStages = 6;          // pipeline stages, two tiles each
+constexpr int kTilesPerStage = 2;
+constexpr int kSlots = 2;           // TMEM accumulator slots, 128 columns (two tiles) each
+constexpr int kEpiWarps = 8;
+constexpr int kWarps = 3 + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSf = 2, kWarpEpi0 = 3;
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -38,31 +46,36 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc = 0;                       // kSlots x 64 fp32 accumulators
-constexpr uint32_t kColSfa = kSlots * 64;             // kStages x 4 (K scale atoms)
-constexpr uint32_t kColSfb = kColSfa + kStages * 4;   // 2 x kGroupMax x 4 (query scale atoms)
+constexpr uint32_t kColAcc = 0;                                     // kSlots x 128 fp32
+constexpr uint32_t kColSfa = kSlots * 128;                          // kStages x 2 atoms x 4
+constexpr uint32_t kColSfb = kColSfa + kStages * kTilesPerStage * 4;  // 2 x kGroupMax x 4
 static_assert(kColSfb + 2 * kGroupMax * 4 <= kTmemCols, "tensor memory budget");
+// Slot use u goes to epilogue half u % 2; with an even slot count every slot always
+// belongs to one half, which consumes its uses in order, so a parity wait is never
+// more than one phase ahead of the barrier.
+static_assert(kSlots % 2 == 0, "slots per epilogue half");
 
 // shared memory layout (bytes from the 1 KB-aligned dynamic base)
-constexpr uint32_t kKPayBytes = 8192;  // [c][2 pages][64][16]
-constexpr uint32_t kKScBytes = 512;    // [2 pages][c][64]
-constexpr uint32_t kAtomBytes = 512;   // 32 x 16 B
+constexpr uint32_t kTileBytes = 8192;   // [c][2 pages][64][16]
+constexpr uint32_t kKPayBytes = kTilesPerStage * kTileBytes;
+constexpr uint32_t kKScBytes = 4 * 256;  // [4 pages][c][64]
+constexpr uint32_t kAtomBytes = 512;     // 32 x 16 B
 constexpr uint32_t kQPayBytes = kGroupMax * 4096;
 constexpr uint32_t kQScBytes = kGroupMax * 256;
 constexpr uint32_t OFF_KPAY = 0;
 constexpr uint32_t OFF_KSC = OFF_KPAY + kStages * kKPayBytes;
 constexpr uint32_t OFF_KATOM = OFF_KSC + kStages * kKScBytes;
-constexpr uint32_t OFF_QPAY = OFF_KATOM + kStages * kAtomBytes;
+constexpr uint32_t OFF_QPAY = OFF_KATOM + kStages * kTilesPerStage * kAtomBytes;
 constexpr uint32_t OFF_QSC = OFF_QPAY + 2 * kQPayBytes;
 constexpr uint32_t OFF_QATOM = OFF_QSC + 2 * kQScBytes;
-constexpr uint32_t OFF_W = OFF_QATOM + 2 * kGroupMax * kAtomBytes;      // per epilogue warp: [kGroupMax][64] fp32
-constexpr uint32_t OFF_LEN = OFF_W + 4 * kGroupMax * 64 * 4;            // per epilogue warp: [kGroupMax] int32
-constexpr uint32_t OFF_BAR = OFF_LEN + 4 * kGroupMax * 4;
+constexpr uint32_t OFF_W = OFF_QATOM + 2 * kGroupMax * kAtomBytes;  // per epilogue warp: [kGroupMax][64] fp32
+constexpr uint32_t OFF_LEN = OFF_W + kEpiWarps * kGroupMax * 64 * 4;  // per epilogue warp: [kGroupMax] int32
+constexpr uint32_t OFF_BAR = OFF_LEN + kEpiWarps * kGroupMax * 4;
 constexpr int kNumBars = 3 * kStages + 6 + 2 * kSlots;
 constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 16 == 0, "alignment");
+static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0 && OFF_KATOM % 16 == 0, "alignment");
 
 // barrier slots
 __device__ __forceinline__ uint32_t bar_kfull(uint32_t b, int s) { return b + OFF_BAR + 8u * s; }
@@ -80,8 +93,6 @@ struct LogitsParams {
   const uint8_t* q_payload;
   const uint8_t* q_scale;
   const float* w;
-  const uint8_t* payload;
-  const uint8_t* scale;
   int64_t num_pages;
   const int32_t* page_table;
   int64_t num_seqs;
@@ -101,35 +112,57 @@ struct Ctl {
   int32_t* status;
 };
 
-// Bounded wait on an mbarrier phase, polled by the whole warp.  False on timeout or when
-// another warp has aborted; the result is uniform across the warp.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort = true) {
-  bool ok = ptx::mbar_try_wait(bar, parity);
-  if (!ok) {
-    const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t it = 1;; ++it) {
-      if (ptx::mbar_try_wait(bar, parity)) {
-        ok = true;
-        break;
-      }
-      if ((it & 63u) == 0) {
-        if (honor_abort && *c.abort) break;
-        if (ptx::globaltimer() - t0 > kTimeoutNs) {
-          *c.abort = 1;
-          record_error(c.status, FP4IDX_ERR_TIMEOUT);
-          break;
-        }
+// Bounded poll of an mbarrier phase by the calling thread.  False on timeout (which
+// raises the abort flag) or, when honor_abort, once another warp has aborted.
+__device__ __forceinline__ bool poll(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (honor_abort && *c.abort) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        *c.abort = 1;
+        record_error(c.status, FP4IDX_ERR_TIMEOUT);
+        return false;
       }
     }
   }
+}
+
+// Every lane polls (the lanes then read what the barrier guards); uniform result.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort = true) {
+  const bool ok = poll(bar, parity, c, honor_abort);
   return __all_sync(kFull, ok);
+}
+
+// Lane 0 polls for a warp whose work after the wait is issued by lane 0 alone.
+__device__ __forceinline__ bool wait_lane0(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort = true) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = poll(bar, parity, c, honor_abort) ? 1 : 0;
+  return __shfl_sync(kFull, ok, 0) != 0;
 }
 
 __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   return a | (b << 8) | (c << 16) | (d << 24);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsParams p) {
+// TMA tile::gather4: rows r0..r3 (each one box of the 2D map) -> 4 consecutive rows in smem.
+__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int32_t r0, int32_t r1, int32_t r2,
+                                        int32_t r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+// Stage bookkeeping shared by all roles: tile pairs [i, i+1] of an item, in order.
+__device__ __forceinline__ int stage_tiles(int32_t i, int32_t t1) { return min(kTilesPerStage, t1 - i); }
+
+__global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_constant__ CUtensorMap pay_map,
+                                                                 const __grid_constant__ CUtensorMap sc_map,
+                                                                 const LogitsParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = ptx::smem_addr(smem);
@@ -163,6 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
+  if (warp == kWarpProducer && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&pay_map) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&sc_map) : "memory");
+  }
   if (warp == kWarpMma) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
   ptx::tc_fence_before();
   __syncthreads();
@@ -186,54 +223,57 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
       maxlen = min(maxlen, min(p.max_context, p.max_pages * kPage));
       const int32_t npages = (maxlen + kPage - 1) / kPage;
       const int qb = ictr & 1;
-      ok = wait_warp(bar_qempty(sb, qb), ((ictr >> 1) & 1) ^ 1, ctl);
+      ok = wait_lane0(bar_qempty(sb, qb), ((ictr >> 1) & 1) ^ 1, ctl);
       if (!ok) break;
       if (lane == 0) {
         const uint32_t qbar = bar_qfull(sb, qb);
         ptx::mbar_arrive_expect_tx(qbar, (uint32_t)rows * (4096u + 256u));
         ptx::bulk_g2s(sb + OFF_QPAY + qb * kQPayBytes, p.q_payload + (int64_t)r0 * 4096, rows * 4096u, qbar);
         ptx::bulk_g2s(sb + OFF_QSC + qb * kQScBytes, p.q_scale + (int64_t)r0 * 256, rows * 256u, qbar);
+        if (!seq_ok) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
       }
-      if (lane == 0 && !seq_ok) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
       const int32_t* pt = p.page_table + (int64_t)(seq_ok ? seq : 0) * p.max_pages;
-      // lane l holds the physical page of logical page 2*chunk + l (16 tiles per chunk)
+      // lane l holds the physical page of logical page 2*chunk + l (16 tiles per chunk);
+      // a page that is not needed or not valid reads page 0 (status recorded if needed).
+      auto fetch = [&](int32_t tile0) -> int32_t {
+        const int32_t lp = 2 * tile0 + lane;
+        if (!seq_ok || lp >= npages) return -2;
+        return __ldg(pt + lp);
+      };
       int32_t chunk = t0;
-      int32_t lpa = 2 * chunk + lane;
-      int32_t pid_cur = (seq_ok && lpa < npages) ? __ldg(pt + lpa) : -1;
-      int32_t lpb = 2 * (chunk + 16) + lane;
-      int32_t pid_next = (seq_ok && lpb < npages) ? __ldg(pt + lpb) : -1;
-      for (int32_t i = t0; i < t1; i++) {
-        if (i - chunk == 16) {
+      int32_t pid_cur = fetch(chunk);
+      int32_t pid_next = fetch(chunk + 16);
+      for (int32_t i = t0; i < t1; i += kTilesPerStage) {
+        if (i - chunk >= 16) {
           chunk += 16;
           pid_cur = pid_next;
-          lpb = 2 * (chunk + 16) + lane;
-          pid_next = (seq_ok && lpb < npages) ? __ldg(pt + lpb) : -1;
+          pid_next = fetch(chunk + 16);
         }
         const int s = kctr % kStages;
-        ok = wait_warp(bar_kempty(sb, s), ((kctr / kStages) & 1) ^ 1, ctl);
+        ok = wait_lane0(bar_kempty(sb, s), ((kctr / kStages) & 1) ^ 1, ctl);
         if (!ok) break;
-        const int32_t pg0 = __shfl_sync(kFull, pid_cur, 2 * (i - chunk));
-        const int32_t pg1 = __shfl_sync(kFull, pid_cur, 2 * (i - chunk) + 1);
-        const bool need0 = 2 * i < npages, need1 = 2 * i + 1 < npages;
-        const bool v0 = need0 && pg0 >= 0 && (int64_t)pg0 < p.num_pages;
-        const bool v1 = need1 && pg1 >= 0 && (int64_t)pg1 < p.num_pages;
-        if (lane == 0 && seq_ok && ((need0 && !v0) || (need1 && !v1))) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
-        const uint32_t kbar = bar_kfull(sb, s);
-        if (lane == 0) ptx::mbar_arrive_expect_tx(kbar, (v0 ? 4352u : 0u) + (v1 ? 4352u : 0u));
-        __syncwarp();
-        if (lane < 8) {
-          const int pp = lane >> 2, c = lane & 3;
-          const bool v = pp ? v1 : v0;
-          const int32_t pg = pp ? pg1 : pg0;
-          if (v)
-            ptx::bulk_g2s(sb + OFF_KPAY + s * kKPayBytes + c * 2048 + pp * 1024,
-                          p.payload + ((int64_t)pg * 4 + c) * 1024, 1024u, kbar);
-        } else if (lane < 10) {
-          const int pp = lane - 8;
-          const bool v = pp ? v1 : v0;
-          const int32_t pg = pp ? pg1 : pg0;
-          if (v) ptx::bulk_g2s(sb + OFF_KSC + s * kKScBytes + pp * 256, p.scale + (int64_t)pg * 256, 256u, kbar);
+        const int tiles = stage_tiles(i, t1);
+        // pages of this stage in lanes 0..3 (tile a: pages 2a, 2a+1)
+        int32_t pg = __shfl_sync(kFull, pid_cur, (2 * (i - chunk) + (lane & 3)) & 31);
+        const bool needed = (lane & 3) < 2 * tiles && pg != -2;
+        const bool valid = pg >= 0 && (int64_t)pg < p.num_pages;
+        if (lane < 4 && needed && !valid) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
+        if (!valid) pg = 0;
+        const int32_t q0 = __shfl_sync(kFull, pg, 0), q1 = __shfl_sync(kFull, pg, 1);
+        const int32_t q2 = __shfl_sync(kFull, pg, 2), q3 = __shfl_sync(kFull, pg, 3);
+        if (lane == 0) {
+          const uint32_t kbar = bar_kfull(sb, s);
+          ptx::mbar_arrive_expect_tx(kbar, (uint32_t)tiles * kTileBytes + kKScBytes);
+          const uint32_t dst = sb + OFF_KPAY + s * kKPayBytes;
+          gather4(dst, &pay_map, 4 * q0 + 0, 4 * q1 + 0, 4 * q0 + 1, 4 * q1 + 1, kbar);
+          gather4(dst + 4096, &pay_map, 4 * q0 + 2, 4 * q1 + 2, 4 * q0 + 3, 4 * q1 + 3, kbar);
+          if (tiles > 1) {
+            gather4(dst + kTileBytes, &pay_map, 4 * q2 + 0, 4 * q3 + 0, 4 * q2 + 1, 4 * q3 + 1, kbar);
+            gather4(dst + kTileBytes + 4096, &pay_map, 4 * q2 + 2, 4 * q3 + 2, 4 * q2 + 3, 4 * q3 + 3, kbar);
+          }
+          gather4(sb + OFF_KSC + s * kKScBytes, &sc_map, q0, q1, q2, q3, kbar);
         }
+        __syncwarp();
         kctr++;
       }
       ictr++;
@@ -241,12 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
     // Tail: every copy issued must land, and (when not aborting) every stage must be
     // released by the MMAs that read it, before the CTA may exit.
     for (uint32_t u = (kctr > (uint32_t)kStages ? kctr - kStages : 0); u < kctr; u++) {
-      wait_warp(bar_kfull(sb, u % kStages), (u / kStages) & 1, ctl, false);
-      if (!*abort_flag) wait_warp(bar_kempty(sb, u % kStages), (u / kStages) & 1, ctl);
+      wait_lane0(bar_kfull(sb, u % kStages), (u / kStages) & 1, ctl, false);
+      if (!*abort_flag) wait_lane0(bar_kempty(sb, u % kStages), (u / kStages) & 1, ctl);
     }
     for (uint32_t u = (ictr > 2u ? ictr - 2 : 0); u < ictr; u++) {
-      wait_warp(bar_qfull(sb, u & 1), (u >> 1) & 1, ctl, false);
-      if (!*abort_flag) wait_warp(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
+      wait_lane0(bar_qfull(sb, u & 1), (u >> 1) & 1, ctl, false);
+      if (!*abort_flag) wait_lane0(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -257,37 +297,39 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
     while (ok && items.next(g, t0, t1)) {
       const int32_t rows = sv.row0[g + 1] - sv.row0[g];
       const int qb = ictr & 1;
-      const uint32_t qph = (ictr >> 1) & 1;
-      ok = wait_warp(bar_qfull(sb, qb), qph, ctl) && wait_warp(bar_qsf(sb, qb), qph, ctl);
+      ok = wait_lane0(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl);  // implies the query rows landed
       if (!ok) break;
       ptx::tc_fence_after();
       if (lane == 0)
         for (int r = 0; r < rows; r++)
           ptx::tmem_cp_sf_atom(tmem + kColSfb + (qb * kGroupMax + r) * 4,
                                sb + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes);
-      __syncwarp();
-      for (int32_t i = t0; i < t1 && ok; i++) {
+      for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
         const int s = kctr % kStages;
-        const uint32_t kph = (kctr / kStages) & 1;
-        ok = wait_warp(bar_kfull(sb, s), kph, ctl) && wait_warp(bar_sfready(sb, s), kph, ctl);
+        const int tiles = stage_tiles(i, t1);
+        ok = wait_lane0(bar_sfready(sb, s), (kctr / kStages) & 1, ctl);  // implies the tiles landed
         if (!ok) break;
         ptx::tc_fence_after();
-        if (lane == 0) ptx::tmem_cp_sf_atom(tmem + kColSfa + s * 4, sb + OFF_KATOM + s * kAtomBytes);
-        __syncwarp();
-        const uint32_t a0 = sb + OFF_KPAY + s * kKPayBytes;
+        if (lane == 0)
+          for (int a = 0; a < tiles; a++)
+            ptx::tmem_cp_sf_atom(tmem + kColSfa + (s * kTilesPerStage + a) * 4,
+                                 sb + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes);
         for (int r = 0; r < rows; r++) {
           const int slot = sctr % kSlots;
-          ok = wait_warp(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl);
+          ok = wait_lane0(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl);
           if (!ok) break;
           ptx::tc_fence_after();
           if (lane == 0) {
             const uint32_t b0 = sb + OFF_QPAY + qb * kQPayBytes + r * 4096;
-            const uint32_t d = tmem + kColAcc + slot * 64;
-            const uint32_t sfa = tmem + kColSfa + s * 4;
             const uint32_t sfbt = tmem + kColSfb + (qb * kGroupMax + r) * 4;
-            ptx::mma_mxf4(d, ptx::smem_desc(a0, 2048, 128), ptx::smem_desc(b0, 1024, 128), kIdesc0, sfa, sfbt, 0);
-            ptx::mma_mxf4(d, ptx::smem_desc(a0 + 4096, 2048, 128), ptx::smem_desc(b0 + 2048, 1024, 128), kIdesc1,
-                          sfa, sfbt, 1);
+            for (int a = 0; a < tiles; a++) {
+              const uint32_t a0 = sb + OFF_KPAY + s * kKPayBytes + a * kTileBytes;
+              const uint32_t d = tmem + kColAcc + slot * 128 + a * 64;
+              const uint32_t sfa = tmem + kColSfa + (s * kTilesPerStage + a) * 4;
+              ptx::mma_mxf4(d, ptx::smem_desc(a0, 2048, 128), ptx::smem_desc(b0, 1024, 128), kIdesc0, sfa, sfbt, 0);
+              ptx::mma_mxf4(d, ptx::smem_desc(a0 + 4096, 2048, 128), ptx::smem_desc(b0 + 2048, 1024, 128), kIdesc1,
+                            sfa, sfbt, 1);
+            }
             ptx::mma_commit(bar_accfull(sb, slot));
           }
           __syncwarp();
@@ -325,19 +367,22 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_qsf(sb, qb));
-      for (int32_t i = t0; i < t1; i++) {
+      for (int32_t i = t0; i < t1; i += kTilesPerStage) {
         const int s = kctr % kStages;
+        const int tiles = stage_tiles(i, t1);
         ok = wait_warp(bar_kfull(sb, s), (kctr / kStages) & 1, ctl);
         if (!ok) break;
-        // K tile: A operand of 128 tokens; token m = 64*page + j; atom row r0 holds tokens
-        // r0, 32 + r0 (page 0) and 64 + r0, 96 + r0 (page 1)
-        const uint8_t* src = smem + OFF_KSC + s * kKScBytes;  // [page][c][64]
-        uint4 v;
-        v.x = pack4(src[lane], src[64 + lane], src[128 + lane], src[192 + lane]);
-        v.y = pack4(src[32 + lane], src[96 + lane], src[160 + lane], src[224 + lane]);
-        v.z = pack4(src[256 + lane], src[320 + lane], src[384 + lane], src[448 + lane]);
-        v.w = pack4(src[288 + lane], src[352 + lane], src[416 + lane], src[480 + lane]);
-        *reinterpret_cast<uint4*>(smem + OFF_KATOM + s * kAtomBytes + lane * 16) = v;
+        for (int a = 0; a < tiles; a++) {
+          // tile a: A operand of 128 tokens, token m = 64*page + j; atom row r0 holds tokens
+          // r0, 32 + r0 (first page) and 64 + r0, 96 + r0 (second page)
+          const uint8_t* src = smem + OFF_KSC + s * kKScBytes + a * 512;  // [page][c][64]
+          uint4 v;
+          v.x = pack4(src[lane], src[64 + lane], src[128 + lane], src[192 + lane]);
+          v.y = pack4(src[32 + lane], src[96 + lane], src[160 + lane], src[224 + lane]);
+          v.z = pack4(src[256 + lane], src[320 + lane], src[384 + lane], src[448 + lane]);
+          v.w = pack4(src[288 + lane], src[352 + lane], src[416 + lane], src[480 + lane]);
+          *reinterpret_cast<uint4*>(smem + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes + lane * 16) = v;
+        }
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar_sfready(sb, s));
@@ -347,9 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kWarpEpi0;  // 0..3: private copy of the group's weights
+    const int ew = warp - kWarpEpi0;  // 0..7: private copy of the group's weights
+    const int half = ew >> 2;         // takes slots with sctr % 2 == half
     const int quad = warp & 3;        // TMEM lanes this warp may read
-    const int m = quad * 32 + lane;   // token row of the tile
+    const int m = quad * 32 + lane;   // token row of a tile
     float* wsm = reinterpret_cast<float*>(smem + OFF_W) + ew * kGroupMax * 64;
     int32_t* lsm = reinterpret_cast<int32_t*>(smem + OFF_LEN) + ew * kGroupMax;
     uint32_t sctr = 0;
@@ -367,32 +413,39 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
         lsm[lane] = L;
       }
       __syncwarp();
-      for (int32_t i = t0; i < t1 && ok; i++) {
-        const int32_t tok = i * kTileTokens + m;
-        for (int r = 0; r < rows; r++) {
+      for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
+        const int tiles = stage_tiles(i, t1);
+        for (int r = 0; r < rows; r++, sctr++) {
+          if ((int)(sctr & 1) != half) continue;
           const int slot = sctr % kSlots;
           ok = wait_warp(bar_accfull(sb, slot), (sctr / kSlots) & 1, ctl);
           if (!ok) break;
           ptx::tc_fence_after();
-          float d[64];
-          ptx::tmem_ld64_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + slot * 64, d);
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar_accempty(sb, slot));
-          if (tok < lsm[r]) {
-            const float* wr = wsm + r * 64;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int h = 0; h < 64; h += 4) {
-              const float4 wv = *reinterpret_cast<const float4*>(wr + h);
-              a0 = fmaf(wv.x, fmaxf(d[h + 0], 0.f), a0);
-              a1 = fmaf(wv.y, fmaxf(d[h + 1], 0.f), a1);
-              a2 = fmaf(wv.z, fmaxf(d[h + 2], 0.f), a2);
-              a3 = fmaf(wv.w, fmaxf(d[h + 3], 0.f), a3);
+          const float* wr = wsm + r * 64;
+          const int32_t L = lsm[r];
+          float* orow = p.out + (int64_t)(r0 + r) * p.out_stride;
+          for (int a = 0; a < tiles; a++) {
+            float d[64];
+            ptx::tmem_ld64_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + slot * 128 + a * 64, d);
+            if (a == tiles - 1) {
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(bar_accempty(sb, slot));
             }
-            p.out[(int64_t)(r0 + r) * p.out_stride + tok] = (a0 + a1) + (a2 + a3);
+            const int32_t tok = (i + a) * kTileTokens + m;
+            if (tok < L) {
+              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+              for (int h = 0; h < 64; h += 4) {
+                const float4 wv = *reinterpret_cast<const float4*>(wr + h);
+                a0 = fmaf(wv.x, fmaxf(d[h + 0], 0.f), a0);
+                a1 = fmaf(wv.y, fmaxf(d[h + 1], 0.f), a1);
+                a2 = fmaf(wv.z, fmaxf(d[h + 2], 0.f), a2);
+                a3 = fmaf(wv.w, fmaxf(d[h + 3], 0.f), a3);
+              }
+              orow[tok] = (a0 + a1) + (a2 + a3);
+            }
           }
-          sctr++;
         }
       }
     }
@@ -402,6 +455,37 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const LogitsPa
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D view of `rows` rows of `row_bytes` bytes as uint64 elements; box = one row.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, uint32_t row_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {row_bytes / 8, 1};
+  cuuint32_t es[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -419,12 +503,14 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (num_pages < 1) return cudaErrorInvalidValue;
+  CUtensorMap pay_map, sc_map;
+  if (!encode_rows(&pay_map, payload, num_pages * 4, 1024) || !encode_rows(&sc_map, scale, num_pages, 256))
+    return cudaErrorInvalidValue;
   LogitsParams prm;
   prm.q_payload = q_payload;
   prm.q_scale = q_scale;
   prm.w = w;
-  prm.payload = payload;
-  prm.scale = scale;
   prm.num_pages = num_pages;
   prm.page_table = page_table;
   prm.num_seqs = num_seqs;
@@ -437,7 +523,7 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
   prm.out = out;
   prm.out_stride = out_stride;
   prm.status = status;
-  logits_mxf4_kernel<<<num_ctas, kThreads, kSmemBytes, stream>>>(prm);
+  logits_mxf4_kernel<<<num_ctas, kThreads, kSmemBytes, stream>>>(pay_map, sc_map, prm);
   return cudaGetLastError();
 }
 
