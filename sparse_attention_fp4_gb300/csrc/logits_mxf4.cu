@@ -14,11 +14,12 @@
 //           directly in the interleaved operand layout) and one gather4 of the four
 //           256 B scale pages; per work item, the group's query rows (one bulk copy
 //           for the payloads, one for the scales).  Page ids are read 32 at a time.
-//   warp 1  MMA issuer: copies scale atoms to tensor memory (tcgen05.cp) and, per
-//           (stage, query row), issues two kind::mxf4 MMAs (K = 64 each) per tile into
-//           a 128-column TMEM slot (2 slots): D[128 tokens x 64 heads] per tile.
+//   warp 1  MMA issuer: per (stage, query row), two kind::mxf4 MMAs (K = 64 each) per
+//           tile into a 128-column TMEM slot (2 slots): D[128 tokens x 64 heads] per tile.
 //   warp 2  scale transposer: reorders the [page][c][token] scale bytes into the
-//           32 x 16 B atom that tcgen05.cp replicates over the four TMEM lane groups.
+//           32 x 16 B atom that tcgen05.cp replicates over the four TMEM lane groups,
+//           issues those copies and signals the MMA issuer with tcgen05.commit, which
+//           keeps every operation but the MMAs off the issuer's serial path.
 //   warps 3-10 epilogue, two per TMEM lane group taking alternate slots: thread =
 //           TMEM lane = token; ReLU, head-weighted sum, mask at the row's context
 //           length, coalesced fp32 store.
@@ -297,23 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     while (ok && items.next(g, t0, t1)) {
       const int32_t rows = sv.row0[g + 1] - sv.row0[g];
       const int qb = ictr & 1;
-      ok = wait_lane0(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl);  // implies the query rows landed
+      // query rows landed and their scale atoms are in tensor memory
+      ok = wait_lane0(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl);
       if (!ok) break;
       ptx::tc_fence_after();
-      if (lane == 0)
-        for (int r = 0; r < rows; r++)
-          ptx::tmem_cp_sf_atom(tmem + kColSfb + (qb * kGroupMax + r) * 4,
-                               sb + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes);
       for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
         const int s = kctr % kStages;
         const int tiles = stage_tiles(i, t1);
-        ok = wait_lane0(bar_sfready(sb, s), (kctr / kStages) & 1, ctl);  // implies the tiles landed
+        // the stage's tiles landed and their scale atoms are in tensor memory
+        ok = wait_lane0(bar_sfready(sb, s), (kctr / kStages) & 1, ctl);
         if (!ok) break;
         ptx::tc_fence_after();
-        if (lane == 0)
-          for (int a = 0; a < tiles; a++)
-            ptx::tmem_cp_sf_atom(tmem + kColSfa + (s * kTilesPerStage + a) * 4,
-                                 sb + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes);
         for (int r = 0; r < rows; r++) {
           const int slot = sctr % kSlots;
           ok = wait_lane0(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl);
@@ -366,7 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar_qsf(sb, qb));
+      if (lane == 0) {
+        for (int r = 0; r < rows; r++)
+          ptx::tmem_cp_sf_atom(tmem + kColSfb + (qb * kGroupMax + r) * 4,
+                               sb + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes);
+        ptx::mma_commit(bar_qsf(sb, qb));  // arrives once the copies have completed
+      }
       for (int32_t i = t0; i < t1; i += kTilesPerStage) {
         const int s = kctr % kStages;
         const int tiles = stage_tiles(i, t1);
@@ -385,7 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_sfready(sb, s));
+        if (lane == 0) {
+          for (int a = 0; a < tiles; a++)
+            ptx::tmem_cp_sf_atom(tmem + kColSfa + (s * kTilesPerStage + a) * 4,
+                                 sb + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes);
+          ptx::mma_commit(bar_sfready(sb, s));
+        }
         kctr++;
       }
       ictr++;
