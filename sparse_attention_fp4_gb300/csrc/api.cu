@@ -93,9 +93,9 @@ int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int
 }
 
 size_t fp4idx_schedule_workspace_bytes(int64_t max_rows, int32_t num_ctas) {
-  (void)num_ctas;
-  if (max_rows < 0 || max_rows > INT32_MAX - 1) return 0;
-  return fp4idx::sched_bytes(max_rows);
+  if (max_rows < 0 || max_rows > INT32_MAX - 1 || num_ctas < 0) return 0;
+  if (num_ctas == 0 && device_sms(&num_ctas) != FP4IDX_OK) return 0;
+  return fp4idx::sched_bytes(max_rows, num_ctas);
 }
 
 int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int64_t n_rows, int32_t num_ctas,
@@ -104,11 +104,11 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
   if (!schedule || !aligned16(schedule)) return FP4IDX_ERR_INVALID_ARG;
   if (n_rows > 0 && (!context_lens || !row_seq || !aligned4(context_lens) || !aligned4(row_seq)))
     return FP4IDX_ERR_INVALID_ARG;
-  if (schedule_bytes < fp4idx::sched_bytes(n_rows)) return FP4IDX_ERR_WORKSPACE;
   if (num_ctas == 0) {
     int st = device_sms(&num_ctas);
     if (st != FP4IDX_OK) return st;
   }
+  if (schedule_bytes < fp4idx::sched_bytes(n_rows, num_ctas)) return FP4IDX_ERR_WORKSPACE;
   return from_cuda(fp4idx::launch_build_schedule(context_lens, row_seq, (int32_t)n_rows, num_ctas, schedule,
                                                  as_stream(stream)));
 }
@@ -137,7 +137,9 @@ int check_logits_args(const uint8_t* q_payload, const uint8_t* q_scale, const fl
       !aligned4(page_table) || !aligned4(row_seq) || !aligned4(context_lens) || !aligned16(schedule))
     return FP4IDX_ERR_INVALID_ARG;
   if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
-  if (schedule_bytes < fp4idx::sched_bytes(n_rows)) return FP4IDX_ERR_WORKSPACE;
+  int32_t sms = 0;
+  if (device_sms(&sms) != FP4IDX_OK) return FP4IDX_ERR_CUDA;
+  if (schedule_bytes < fp4idx::sched_bytes(n_rows, sms)) return FP4IDX_ERR_WORKSPACE;
   return FP4IDX_OK;
 }
 

@@ -9,14 +9,14 @@
 //   A tile is 128 tokens = two cache pages, the A operand of an M = 128 MMA laid out as
 //   [block c][page][64 tokens][16 B] (canonical no-swizzle K-major).  A pipeline stage
 //   holds two tiles (four pages).
-//   warp 0  producer: per stage, four TMA tile::gather4 loads of the payload (each
+//   warp 2  producer: per stage, four TMA tile::gather4 loads of the payload (each
 //           fetches the 1 KB rows (page, c) of two pages for two blocks, landing
 //           directly in the interleaved operand layout) and one gather4 of the four
 //           256 B scale pages; per work item, the group's query rows (one bulk copy
 //           for the payloads, one for the scales).  Page ids are read 32 at a time.
 //   warp 1  MMA issuer: per (stage, query row), two kind::mxf4 MMAs (K = 64 each) per
 //           tile into a 128-column TMEM slot (2 slots): D[128 tokens x 64 heads] per tile.
-//   warp 2  scale transposer: reorders the [page][c][token] scale bytes into the
+//   warp 0  scale transposer: reorders the [page][c][token] scale bytes into the
 //           32 x 16 B atom that tcgen05.cp replicates over the four TMEM lane groups,
 //           issues those copies and signals the MMA issuer with tcgen05.commit, which
 //           keeps every operation but the MMAs off the issuer's serial path.
@@ -35,13 +35,13 @@
 namespace fp4idx {
 namespace {
 
-constexpr int kStages = 6;          // pipeline stages, two tiles each
+constexpr int kStages = 8;          // pipeline stages, two tiles each
 constexpr int kTilesPerStage = 2;
 constexpr int kSlots = 2;           // TMEM accumulator slots, 128 columns (two tiles) each
 constexpr int kEpiWarps = 8;
 constexpr int kWarps = 3 + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSf = 2, kWarpEpi0 = 3;
+constexpr int kWarpSf = 0, kWarpMma = 1, kWarpProducer = 2, kWarpEpi0 = 3;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
@@ -69,14 +69,13 @@ constexpr uint32_t OFF_KATOM = OFF_KSC + kStages * kKScBytes;
 constexpr uint32_t OFF_QPAY = OFF_KATOM + kStages * kTilesPerStage * kAtomBytes;
 constexpr uint32_t OFF_QSC = OFF_QPAY + 2 * kQPayBytes;
 constexpr uint32_t OFF_QATOM = OFF_QSC + 2 * kQScBytes;
-constexpr uint32_t OFF_W = OFF_QATOM + 2 * kGroupMax * kAtomBytes;  // per epilogue warp: [kGroupMax][64] fp32
-constexpr uint32_t OFF_LEN = OFF_W + kEpiWarps * kGroupMax * 64 * 4;  // per epilogue warp: [kGroupMax] int32
+constexpr uint32_t OFF_LEN = OFF_QATOM + 2 * kGroupMax * kAtomBytes;  // per epilogue warp: [kGroupMax] int32
 constexpr uint32_t OFF_BAR = OFF_LEN + kEpiWarps * kGroupMax * 4;
 constexpr int kNumBars = 3 * kStages + 6 + 2 * kSlots;
 constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr uint32_t kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0 && OFF_KATOM % 16 == 0, "alignment");
+static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0, "alignment");
 
 // barrier slots
 __device__ __forceinline__ uint32_t bar_kfull(uint32_t b, int s) { return b + OFF_BAR + 8u * s; }
@@ -262,16 +261,18 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
         if (!valid) pg = 0;
         const int32_t q0 = __shfl_sync(kFull, pg, 0), q1 = __shfl_sync(kFull, pg, 1);
         const int32_t q2 = __shfl_sync(kFull, pg, 2), q3 = __shfl_sync(kFull, pg, 3);
-        if (lane == 0) {
-          const uint32_t kbar = bar_kfull(sb, s);
-          ptx::mbar_arrive_expect_tx(kbar, (uint32_t)tiles * kTileBytes + kKScBytes);
-          const uint32_t dst = sb + OFF_KPAY + s * kKPayBytes;
-          gather4(dst, &pay_map, 4 * q0 + 0, 4 * q1 + 0, 4 * q0 + 1, 4 * q1 + 1, kbar);
-          gather4(dst + 4096, &pay_map, 4 * q0 + 2, 4 * q1 + 2, 4 * q0 + 3, 4 * q1 + 3, kbar);
-          if (tiles > 1) {
-            gather4(dst + kTileBytes, &pay_map, 4 * q2 + 0, 4 * q3 + 0, 4 * q2 + 1, 4 * q3 + 1, kbar);
-            gather4(dst + kTileBytes + 4096, &pay_map, 4 * q2 + 2, 4 * q3 + 2, 4 * q2 + 3, 4 * q3 + 3, kbar);
-          }
+        const uint32_t kbar = bar_kfull(sb, s);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(kbar, (uint32_t)tiles * kTileBytes + kKScBytes);
+        __syncwarp();
+        // lanes 0-3: tile lane/2, blocks (2h, 2h+1) with h = lane%2, each row (page, block)
+        // 1 KB; lane 4: the four scale pages
+        if (lane < 4) {
+          const int a = lane >> 1, h = lane & 1;
+          const int32_t pa = a ? q2 : q0, pb = a ? q3 : q1;
+          if (a < tiles)
+            gather4(sb + OFF_KPAY + s * kKPayBytes + a * kTileBytes + h * 4096, &pay_map, 4 * pa + 2 * h,
+                    4 * pb + 2 * h, 4 * pa + 2 * h + 1, 4 * pb + 2 * h + 1, kbar);
+        } else if (lane == 4) {
           gather4(sb + OFF_KSC + s * kKScBytes, &sc_map, q0, q1, q2, q3, kbar);
         }
         __syncwarp();
@@ -290,31 +291,31 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       if (!*abort_flag) wait_lane0(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    uint32_t kctr = 0, ictr = 0, sctr = 0;
-    bool ok = true;
-    constexpr uint32_t kIdesc0 = ptx::idesc_mxf4(64, 0, 0);
-    constexpr uint32_t kIdesc1 = ptx::idesc_mxf4(64, 2, 2);
-    while (ok && items.next(g, t0, t1)) {
-      const int32_t rows = sv.row0[g + 1] - sv.row0[g];
-      const int qb = ictr & 1;
-      // query rows landed and their scale atoms are in tensor memory
-      ok = wait_lane0(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
-        const int s = kctr % kStages;
-        const int tiles = stage_tiles(i, t1);
-        // the stage's tiles landed and their scale atoms are in tensor memory
-        ok = wait_lane0(bar_sfready(sb, s), (kctr / kStages) & 1, ctl);
+    // ------------------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      uint32_t kctr = 0, ictr = 0, sctr = 0;
+      bool ok = true;
+      constexpr uint32_t kIdesc0 = ptx::idesc_mxf4(64, 0, 0);
+      constexpr uint32_t kIdesc1 = ptx::idesc_mxf4(64, 2, 2);
+      while (ok && items.next(g, t0, t1)) {
+        const int32_t rows = sv.row0[g + 1] - sv.row0[g];
+        const int qb = ictr & 1;
+        // query rows landed and their scale atoms are in tensor memory
+        ok = poll(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl, true);
         if (!ok) break;
         ptx::tc_fence_after();
-        for (int r = 0; r < rows; r++) {
-          const int slot = sctr % kSlots;
-          ok = wait_lane0(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl);
+        for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
+          const int s = kctr % kStages;
+          const int tiles = stage_tiles(i, t1);
+          // the stage's tiles landed and their scale atoms are in tensor memory
+          ok = poll(bar_sfready(sb, s), (kctr / kStages) & 1, ctl, true);
           if (!ok) break;
           ptx::tc_fence_after();
-          if (lane == 0) {
+          for (int r = 0; r < rows; r++) {
+            const int slot = sctr % kSlots;
+            ok = poll(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl, true);
+            if (!ok) break;
+            ptx::tc_fence_after();
             const uint32_t b0 = sb + OFF_QPAY + qb * kQPayBytes + r * 4096;
             const uint32_t sfbt = tmem + kColSfb + (qb * kGroupMax + r) * 4;
             for (int a = 0; a < tiles; a++) {
@@ -326,19 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
                             sfa, sfbt, 1);
             }
             ptx::mma_commit(bar_accfull(sb, slot));
+            sctr++;
           }
-          __syncwarp();
-          sctr++;
+          if (!ok) break;
+          ptx::mma_commit(bar_kempty(sb, s));
+          kctr++;
         }
         if (!ok) break;
-        if (lane == 0) ptx::mma_commit(bar_kempty(sb, s));
-        __syncwarp();
-        kctr++;
+        ptx::mma_commit(bar_qempty(sb, qb));
+        ictr++;
       }
-      if (!ok) break;
-      if (lane == 0) ptx::mma_commit(bar_qempty(sb, qb));
-      __syncwarp();
-      ictr++;
     }
   } else if (warp == kWarpSf) {
     // ------------------------------------------------------------ scale transposer
@@ -389,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           for (int a = 0; a < tiles; a++)
             ptx::tmem_cp_sf_atom(tmem + kColSfa + (s * kTilesPerStage + a) * 4,
                                  sb + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes);
-          ptx::mma_commit(bar_sfready(sb, s));
+          ptx::mma_commit(bar_sfready(sb, s));  // arrives once the copies have completed
         }
         kctr++;
       }
@@ -397,18 +395,16 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - kWarpEpi0;  // 0..7: private copy of the group's weights
+    const int ew = warp - kWarpEpi0;  // 0..7: private copy of the group's lengths
     const int half = ew >> 2;         // takes slots with sctr % 2 == half
     const int quad = warp & 3;        // TMEM lanes this warp may read
     const int m = quad * 32 + lane;   // token row of a tile
-    float* wsm = reinterpret_cast<float*>(smem + OFF_W) + ew * kGroupMax * 64;
     int32_t* lsm = reinterpret_cast<int32_t*>(smem + OFF_LEN) + ew * kGroupMax;
     uint32_t sctr = 0;
     bool ok = true;
     while (ok && items.next(g, t0, t1)) {
       const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
       __syncwarp();
-      for (int idx = lane; idx < rows * 64; idx += 32) wsm[idx] = __ldg(p.w + (int64_t)r0 * 64 + idx);
       if (lane < rows) {
         int32_t L = __ldg(p.context_lens + r0 + lane);
         if (L < 0 || L > p.max_context) {
@@ -426,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           ok = wait_warp(bar_accfull(sb, slot), (sctr / kSlots) & 1, ctl);
           if (!ok) break;
           ptx::tc_fence_after();
-          const float* wr = wsm + r * 64;
+          const float* wr = p.w + (int64_t)(r0 + r) * 64;  // same address in every lane: L1 broadcast
           const int32_t L = lsm[r];
           float* orow = p.out + (int64_t)(r0 + r) * p.out_stride;
           for (int a = 0; a < tiles; a++) {
@@ -442,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
               float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
               for (int h = 0; h < 64; h += 4) {
-                const float4 wv = *reinterpret_cast<const float4*>(wr + h);
+                const float4 wv = __ldg(reinterpret_cast<const float4*>(wr + h));
                 a0 = fmaf(wv.x, fmaxf(d[h + 0], 0.f), a0);
                 a1 = fmaf(wv.y, fmaxf(d[h + 1], 0.f), a1);
                 a2 = fmaf(wv.z, fmaxf(d[h + 2], 0.f), a2);

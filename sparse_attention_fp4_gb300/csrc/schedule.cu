@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
     if (g < n_groups) s.prefix[g + 1] = carry_cost + inc;
     carry_cost += tot;
   }
+  __syncthreads();
+  // Phase C: each logits CTA's first group, so the kernel starts without a search.
+  for (int32_t c = tid; c < num_ctas; c += kThreads)
+    s.cta_g0[c] = first_group_after(s.prefix, n_groups, carry_cost * c / num_ctas);
   if (tid == 0) {
     s.hdr->magic = kSchedMagic;
     s.hdr->n_rows = n_rows;

@@ -14,7 +14,7 @@
 
 namespace fp4idx {
 
-constexpr int kGroupMax = 8;
+constexpr int kGroupMax = 6;  // six draft rows of a sequence share one group
 constexpr int kTileTokens = 128;
 constexpr int kTileCost = 2;
 constexpr int32_t kSchedMagic = 0x46344944;  // "F4ID"
@@ -34,15 +34,17 @@ struct SchedView {
   int32_t* row0;     // [n_rows + 1] first row of each group (entry n_groups = n_rows)
   int32_t* maxlen;   // [n_rows] largest clamped context length in the group
   int64_t* prefix;   // [n_rows + 1] exclusive prefix of group costs
+  int32_t* cta_g0;   // [num_ctas] first group whose cost interval ends after the CTA's range start
 };
 
 __host__ __device__ inline size_t sched_align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
-__host__ __device__ inline size_t sched_bytes(int64_t n_rows) {
+__host__ __device__ inline size_t sched_bytes(int64_t n_rows, int64_t num_ctas) {
   size_t b = sched_align16(sizeof(SchedHeader));
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
+  b += sched_align16(sizeof(int32_t) * (size_t)num_ctas);
   return b;
 }
 
@@ -56,10 +58,23 @@ __host__ __device__ inline SchedView sched_view(void* base, int64_t n_rows) {
   v.maxlen = reinterpret_cast<int32_t*>(p);
   p += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   v.prefix = reinterpret_cast<int64_t*>(p);
+  p += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
+  v.cta_g0 = reinterpret_cast<int32_t*>(p);
   return v;
 }
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// First group whose cost interval [prefix[g], prefix[g+1]) ends after `lo`.
+__host__ __device__ inline int32_t first_group_after(const int64_t* prefix, int32_t n_groups, int64_t lo) {
+  int32_t a = 0, b = n_groups;
+  while (a < b) {
+    const int32_t m = (a + b) >> 1;
+    if (prefix[m + 1] <= lo) a = m + 1;
+    else b = m;
+  }
+  return a;
+}
 
 // Iterates the (group, tile range) items of one CTA in a fixed order.
 struct ItemIter {
@@ -78,14 +93,7 @@ struct ItemIter {
     const int64_t W = s.hdr->total_cost;
     lo = W * cta / num_ctas;
     hi = W * (cta + 1) / num_ctas;
-    // first group whose cost interval ends after lo
-    int32_t a = 0, b = n_groups;
-    while (a < b) {
-      int32_t m = (a + b) >> 1;
-      if (prefix[m + 1] <= lo) a = m + 1;
-      else b = m;
-    }
-    g = a;
+    g = s.cta_g0[cta];  // precomputed by the schedule kernel
   }
 
   // Next non-empty item; false when this CTA's range is exhausted.
