@@ -11,11 +11,12 @@
 //   1. bucket histogram: 2048 buckets linear in value between the row's min and max.
 //      floor((x - min) * 2047/(max - min)) is non-decreasing in x, so every logit in a
 //      higher bucket is larger than every logit in a lower one; values spread over the
-//      buckets, so the shared-memory atomics rarely collide.
-//   2. the bucket holding the k-th largest is resolved exactly: its few candidates are
-//      gathered and ranked by (key desc, index asc).  When it holds more than kGather
-//      candidates (a degenerate row: many equal values), a radix select over the exact
-//      keys with warp-aggregated atomics takes over.
+//      buckets, so the shared-memory atomics rarely collide.  When the bucket holding the
+//      k-th largest is crowded (heavy tails), a second linear histogram over that
+//      bucket's own value range narrows it.
+//   2. the candidates of the final bucket are gathered and ranked by (key desc, index
+//      asc).  When more than kGather remain (many equal values), a radix select over the
+//      exact keys with warp-aggregated atomics takes over.
 //   3. one ordered pass keeps every key above the threshold key and the lowest-indexed
 //      keys equal to it: each thread owns a contiguous run of positions, two block scans
 //      give the output offsets, so the selection comes out sorted by position.
@@ -40,10 +41,16 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__device__ __forceinline__ int bucket_of(float x, float lo, float scale) {
+// Linear bucket of value x over [lo, lo + 2047/scale]; scale = 0 puts everything in bucket 0.
+__device__ __forceinline__ int lin_bucket(float x, float lo, float scale) {
   const float v = (x - lo) * scale;
   if (!(v >= 0.0f)) return 0;  // also NaN
   return v >= (float)(kBins - 1) ? kBins - 1 : (int)v;
+}
+
+__device__ __forceinline__ float lin_scale(float lo, float hi) {
+  const float range = hi - lo;
+  return (range > 0.0f && range < INFINITY) ? (float)(kBins - 1) / range : 0.0f;
 }
 
 // Exclusive block scan of an int; `total` gets the block sum.
@@ -74,17 +81,17 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int& total) 
 }
 
 template <bool kMax>
-__device__ __forceinline__ float block_reduce(float v, float* scratch) {
+__device__ __forceinline__ uint32_t block_reduce(uint32_t v, uint32_t* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float n = __shfl_xor_sync(kFull, v, o);
-    v = kMax ? fmaxf(v, n) : fminf(v, n);
+    const uint32_t n = __shfl_xor_sync(kFull, v, o);
+    v = kMax ? max(v, n) : min(v, n);
   }
   if (lane == 0) scratch[warp] = v;
   __syncthreads();
-  float r = scratch[0];
-  for (int i = 1; i < kWarps; i++) r = kMax ? fmaxf(r, scratch[i]) : fminf(r, scratch[i]);
+  uint32_t r = scratch[0];
+  for (int i = 1; i < kWarps; i++) r = kMax ? max(r, scratch[i]) : min(r, scratch[i]);
   __syncthreads();
   return r;
 }
@@ -123,8 +130,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
   __shared__ uint32_t gkey[kGather];
   __shared__ int gidx[kGather];
   __shared__ int scratch[kWarps];
-  __shared__ float fscratch[kWarps];
+  __shared__ uint32_t uscratch[kWarps];
   __shared__ int sh_bin, sh_rem, sh_gcount;
+  __shared__ uint32_t sh_kmin, sh_kmax;
   __shared__ uint32_t sh_key;
   __shared__ int sh_take;
 
@@ -142,34 +150,107 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
   }
   const float* lg = logits + row * stride;
   const bool cached = L <= smem_cap;
-  float mn = INFINITY, mx = -INFINITY;
-  for (int s = tid; s < L; s += kThreads) {
-    const float x = __ldg(lg + s);
-    mn = fminf(mn, x);
-    mx = fmaxf(mx, x);
-    if (cached) keys[s] = order_key(x);
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  auto take = [&](int s, float x) {
+    const uint32_t u = order_key(x);
+    kmin = min(kmin, u);
+    kmax = max(kmax, u);
+    if (cached) keys[s] = u;
+  };
+  // The row comes from L2 or HBM: keep four 16-byte loads in flight per thread.
+  int s_done = 0;
+  if ((stride & 3) == 0 && (reinterpret_cast<uintptr_t>(lg) & 15) == 0) {
+    const float4* lg4 = reinterpret_cast<const float4*>(lg);
+    const int L4 = L >> 2;
+    for (int v0 = 0; v0 < L4; v0 += 4 * kThreads) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int v = v0 + u * kThreads + tid;
+        x[u] = v < L4 ? __ldg(lg4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int v = v0 + u * kThreads + tid;
+        if (v < L4) {
+          take(4 * v, x[u].x);
+          take(4 * v + 1, x[u].y);
+          take(4 * v + 2, x[u].z);
+          take(4 * v + 3, x[u].w);
+        }
+      }
+    }
+    s_done = L4 << 2;
+  }
+  for (int s0 = s_done; s0 < L; s0 += 4 * kThreads) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int s = s0 + u * kThreads + tid;
+      x[u] = s < L ? __ldg(lg + s) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int s = s0 + u * kThreads + tid;
+      if (s < L) take(s, x[u]);
+    }
   }
   for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-  mn = block_reduce<false>(mn, fscratch);
-  mx = block_reduce<true>(mx, fscratch);
-  const float range = mx - mn;
-  const float scale = (range > 0.0f && range < INFINITY) ? (float)(kBins - 1) / range : 0.0f;
+  kmin = block_reduce<false>(kmin, uscratch);
+  kmax = block_reduce<true>(kmax, uscratch);
   auto key_at = [&](int s) -> uint32_t { return cached ? keys[s] : order_key(__ldg(lg + s)); };
 
-  // 1. bucket histogram
-  for (int s = tid; s < L; s += kThreads) atomicAdd(&hist[bucket_of(key_value(key_at(s)), mn, scale)], 1);
-  if (tid == 0) sh_gcount = 0;
+  // 1. bucket histogram over [min, max]
+  const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
+  for (int s = tid; s < L; s += kThreads) atomicAdd(&hist[lin_bucket(key_value(key_at(s)), lo1, sc1)], 1);
+  if (tid == 0) {
+    sh_gcount = 0;
+    sh_kmin = 0xFFFFFFFFu;
+    sh_kmax = 0u;
+  }
   __syncthreads();
   find_bin_from_top(hist, k, scratch, &sh_bin, &sh_rem);
-  const int bstar = sh_bin;
-  const int rem = sh_rem;
-  const int nb = hist[bstar];
+  const int b1 = sh_bin;
+  int rem = sh_rem;
+  int nb = hist[b1];
+  __syncthreads();  // every thread has read nb before any path clears the histogram
+  // optional refinement of a crowded bucket over its own value range
+  float lo2 = 0.0f, sc2 = 0.0f;
+  int b2 = -1;
+  if (nb > kGather) {
+    for (int s = tid; s < L; s += kThreads) {
+      const uint32_t u = key_at(s);
+      if (lin_bucket(key_value(u), lo1, sc1) == b1) {
+        atomicMin(&sh_kmin, u);
+        atomicMax(&sh_kmax, u);
+      }
+    }
+    for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    lo2 = key_value(sh_kmin);
+    sc2 = lin_scale(lo2, key_value(sh_kmax));
+    for (int s = tid; s < L; s += kThreads) {
+      const float x = key_value(key_at(s));
+      if (lin_bucket(x, lo1, sc1) == b1) atomicAdd(&hist[lin_bucket(x, lo2, sc2)], 1);
+    }
+    __syncthreads();
+    find_bin_from_top(hist, rem, scratch, &sh_bin, &sh_rem);
+    b2 = sh_bin;
+    rem = sh_rem;
+    nb = hist[b2];
+    __syncthreads();
+  }
+  // membership of the final candidate bucket
+  auto in_bucket = [&](uint32_t u) -> bool {
+    const float x = key_value(u);
+    return lin_bucket(x, lo1, sc1) == b1 && (b2 < 0 || lin_bucket(x, lo2, sc2) == b2);
+  };
 
   // 2. resolve the threshold bucket: threshold key tau and how many keys equal to tau to keep
   if (nb <= kGather) {
     for (int s = tid; s < L; s += kThreads) {
       const uint32_t u = key_at(s);
-      if (bucket_of(key_value(u), mn, scale) == bstar) {
+      if (in_bucket(u)) {
         const int slot = atomicAdd(&sh_gcount, 1);
         gkey[slot] = u;
         gidx[slot] = s;
@@ -198,18 +279,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
     int r = rem;
 #pragma unroll 1
     for (int pass = 0; pass < 3; pass++) {
-      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int dshift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
       for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
       __syncthreads();
-      for (int base = 0; base < L; base += kThreads) {
-        const int s = base + tid;
+      for (int s_base = 0; s_base < L; s_base += kThreads) {
+        const int s = s_base + tid;
         bool take = false;
         uint32_t digit = 0;
         if (s < L) {
           const uint32_t u = key_at(s);
-          take = bucket_of(key_value(u), mn, scale) == bstar && (u & pmask) == prefix;
-          digit = (u >> shift) & dmask;
+          take = in_bucket(u) && (u & pmask) == prefix;
+          digit = (u >> dshift) & dmask;
         }
         const unsigned active = __ballot_sync(kFull, take);
         if (take) {
@@ -219,8 +300,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
       }
       __syncthreads();
       find_bin_from_top(hist, r, scratch, &sh_bin, &sh_rem);
-      prefix |= (uint32_t)sh_bin << shift;
-      pmask |= dmask << shift;
+      prefix |= (uint32_t)sh_bin << dshift;
+      pmask |= dmask << dshift;
       r = sh_rem;
       __syncthreads();
     }

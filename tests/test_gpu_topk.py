@@ -1,0 +1,83 @@
+"""GPU top-k on given logits: the selection must be exactly the k largest values
+(ties to the lower positions), in ascending position order, -1 padded.  Covers every
+path of the kernel: spread values (bucket + rank), heavy tails, many duplicates and
+all-equal rows (radix fallback), rows longer than the shared-memory cache."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def expected(lg, L, k):
+    order = np.lexsort((np.arange(L), -lg[:L].astype(np.float64)))[:min(k, L)]
+    out = -np.ones(k, np.int32)
+    out[:order.size] = np.sort(order)
+    return out
+
+
+def run(rows, lens, k, stride=None):
+    from sparse_attention_fp4_gb300 import fp4idx
+    T = len(rows)
+    Lmax = max(1, max(lens))
+    stride = stride or Lmax
+    buf = np.full((T, stride), np.nan, np.float32)
+    for t, r in enumerate(rows):
+        buf[t, :lens[t]] = r[:lens[t]]
+    lg = torch.from_numpy(buf).cuda()
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp4idx.topk(lg, cl, Lmax, k, out, status=status)
+    torch.cuda.synchronize()
+    assert fp4idx.read_status(status) == 0
+    return out.cpu().numpy()
+
+
+def _dist(rng, kind, L):
+    if kind == "normal":
+        return rng.standard_normal(L).astype(np.float32)
+    if kind == "cauchy":
+        return rng.standard_cauchy(L).astype(np.float32)
+    if kind == "outliers":
+        x = rng.standard_normal(L).astype(np.float32)
+        x[rng.choice(L, min(5, L), replace=False)] = np.float32(1e6)
+        return x
+    if kind == "dups":
+        return np.round(rng.standard_normal(L) * 4).astype(np.float32) + np.float32(0.5)
+    if kind == "equal":
+        return np.full(L, 3.25, np.float32)
+    if kind == "positive_narrow":
+        return (100 + rng.random(L) * 1e-3).astype(np.float32)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["normal", "cauchy", "outliers", "dups", "equal", "positive_narrow"])
+@pytest.mark.parametrize("stride_pad", [0, 3])
+def test_topk_distributions(kind, stride_pad):
+    rng = np.random.default_rng(hash(kind) % 1000)
+    lens = [0, 1, 2047, 2048, 2049, 4096, 21000, 32768]
+    rows = [_dist(rng, kind, max(L, 1)) for L in lens]
+    k = 2048
+    got = run(rows, lens, k, stride=max(lens) + stride_pad)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, k)), (kind, t, L)
+
+
+def test_topk_long_rows_outside_the_cache():
+    rng = np.random.default_rng(5)
+    lens = [49152, 50000, 65536]
+    rows = [_dist(rng, kd, L) for kd, L in zip(["normal", "dups", "cauchy"], lens)]
+    got = run(rows, lens, 4096)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, 4096)), t
+
+
+@pytest.mark.parametrize("k", [1, 7, 512, 4096])
+def test_topk_small_and_max_k(k):
+    rng = np.random.default_rng(k)
+    lens = [1, 100, 5000, 17000]
+    rows = [_dist(rng, "normal", L) for L in lens]
+    got = run(rows, lens, k)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, k)), (k, t)
