@@ -243,28 +243,22 @@ class DecodeStep:
         self.topk = torch.empty((self.T, self.k), dtype=torch.int32, device=device)
         torch.cuda.synchronize(device)
 
-    def launch(self, events=None):
+    def calls(self):
+        """The five launches of a step, in order, as (name, callable)."""
         f = self.fp4idx
-        ev = events or [None] * 6
-        if ev[0] is not None:
-            ev[0].record()
-        f.store_k(self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.cs, self.payload, self.scale,
-                  status=self.status)
-        if ev[1] is not None:
-            ev[1].record()
-        f.quant_q(self.q, self.qpos, self.cs, self.qp, self.qs, status=self.status)
-        if ev[2] is not None:
-            ev[2].record()
-        f.build_schedule(self.cl, self.rs, self.sched)
-        if ev[3] is not None:
-            ev[3].record()
-        f.logits(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl, self.max_ctx,
-                 self.sched, self.logits, status=self.status)
-        if ev[4] is not None:
-            ev[4].record()
-        f.topk(self.logits, self.cl, self.max_ctx, self.k, self.topk, status=self.status)
-        if ev[5] is not None:
-            ev[5].record()
+        return [
+            ("store_k", lambda: f.store_k(self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.cs,
+                                          self.payload, self.scale, status=self.status)),
+            ("quant_q", lambda: f.quant_q(self.q, self.qpos, self.cs, self.qp, self.qs, status=self.status)),
+            ("build_schedule", lambda: f.build_schedule(self.cl, self.rs, self.sched)),
+            ("logits", lambda: f.logits(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
+                                        self.max_ctx, self.sched, self.logits, status=self.status)),
+            ("topk", lambda: f.topk(self.logits, self.cl, self.max_ctx, self.k, self.topk, status=self.status)),
+        ]
+
+    def launch(self):
+        for _, fn in self.calls():
+            fn()
 
 
 def run_gpu(args):
@@ -327,18 +321,29 @@ def run_gpu(args):
     value, slowest = aggregate(st.T * K, total_s, device)
     ms_per_step = slowest / K * 1e3
 
-    # per-kernel breakdown on the same stream (direct launches, L2 flushed)
+    # per-kernel breakdown: each launch captured in its own graph and replayed alone
+    # (L2 flushed, a spin kernel ahead of it so no host time falls inside the events)
     Kb = min(K, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(Kb)]
+    subs = []
+    for name, fn in st.calls():
+        sg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sg):
+            fn()
+        subs.append((name, sg))
+    per_times = {name: [] for name, _ in subs}
     for i in range(Kb):
-        flush_l2()
-        torch.cuda._sleep(spin_cycles * 4)
-        st.launch(evs[i])
+        for name, sg in subs:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            flush_l2()
+            torch.cuda._sleep(spin_cycles)
+            e0.record()
+            sg.replay()
+            e1.record()
+            per_times[name].append((e0, e1))
     torch.cuda.synchronize()
-    names = ["store_k", "quant_q", "build_schedule", "logits", "topk"]
-    per = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(Kb)]) * 1e3
-           for j, n in enumerate(names)}
-    logits_us = statistics.mean([evs[i][3].elapsed_time(evs[i][4]) for i in range(Kb)]) * 1e3
+    per = {n: statistics.median([a.elapsed_time(b) for a, b in v]) * 1e3 for n, v in per_times.items()}
+    logits_us = statistics.mean([a.elapsed_time(b) for a, b in per_times["logits"]]) * 1e3
     status = st.fp4idx.read_status(st.status)
 
     ab = algorithmic_bytes(b)

@@ -5,9 +5,11 @@
 // [AMD] Enable FP4 indexer for Deepseek V4 -- Attention runtime: padded rows keep
 // context length 0 (their selection is empty: all -1).
 //
-// One CTA per query row; the row's logits are cached in shared memory as
-// order-preserving 32-bit keys.  Selection = the k largest (ties at the k-th value to the
-// lower positions), found in three steps:
+// One thread-block cluster per query row (1, 2, 4 or 8 CTAs: wide clusters when there are
+// few rows, so a decode batch still fills the GPU).  CTA `rank` owns a contiguous segment
+// of the row and caches it in shared memory as order-preserving 32-bit keys; the cluster
+// combines its statistics in the shared memory of rank 0 (distributed shared memory).
+// Selection = the k largest logits, ties at the k-th value to the lower positions:
 //   1. bucket histogram: 2048 buckets linear in value between the row's min and max.
 //      floor((x - min) * 2047/(max - min)) is non-decreasing in x, so every logit in a
 //      higher bucket is larger than every logit in a lower one; values spread over the
@@ -18,9 +20,13 @@
 //      asc).  When more than kGather remain (many equal values), a radix select over the
 //      exact keys with warp-aggregated atomics takes over.
 //   3. one ordered pass keeps every key above the threshold key and the lowest-indexed
-//      keys equal to it: each thread owns a contiguous run of positions, two block scans
-//      give the output offsets, so the selection comes out sorted by position.
+//      keys equal to it: each thread owns a contiguous run of positions and block and
+//      cluster scans give the output offsets, so the selection comes out sorted.
+#include <cooperative_groups.h>
+
 #include "fp4idx_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace fp4idx {
 namespace {
@@ -30,6 +36,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kGather = 1024;
+constexpr int kMaxCluster = 8;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -97,7 +104,7 @@ __device__ __forceinline__ uint32_t block_reduce(uint32_t v, uint32_t* scratch) 
 }
 
 // Thread whose run of histogram bins (taken from the top) contains the rem-th largest
-// element writes (bin, rem - elements above the bin).  `counts` holds nbins bins.
+// element writes (bin, rem - elements above the bin).
 __device__ __forceinline__ void find_bin_from_top(const int* counts, int rem, int* scratch, int* out_bin,
                                                   int* out_rem) {
   const int tb = (kThreads - 1 - (int)threadIdx.x) * kBinsPerThread;
@@ -121,9 +128,20 @@ __device__ __forceinline__ void find_bin_from_top(const int* counts, int rem, in
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict__ logits, int64_t stride,
+// Cluster-wide state; the copy in rank 0's shared memory is the one the cluster uses.
+struct ClusterState {
+  uint32_t kmin, kmax, kmin2, kmax2;
+  int bin, rem;
+  int nbk;     // elements in the bucket just selected
+  int gcount;  // gathered candidates
+  uint32_t key;
+  int take;
+  int gt[kMaxCluster], eq[kMaxCluster];
+};
+
+__global__ void __launch_bounds__(kThreads, 1) topk_kernel(const float* __restrict__ logits, int64_t stride,
                                                         const int32_t* __restrict__ context_lens, int32_t max_context,
-                                                        int32_t k, int32_t* __restrict__ out, int32_t smem_cap,
+                                                        int32_t k, int32_t* __restrict__ out, int32_t seg_cap,
                                                         int32_t* status) {
   extern __shared__ __align__(16) uint32_t keys[];
   __shared__ int hist[kBins];
@@ -131,25 +149,43 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
   __shared__ int gidx[kGather];
   __shared__ int scratch[kWarps];
   __shared__ uint32_t uscratch[kWarps];
-  __shared__ int sh_bin, sh_rem, sh_gcount;
-  __shared__ uint32_t sh_kmin, sh_kmax;
-  __shared__ uint32_t sh_key;
-  __shared__ int sh_take;
+  __shared__ ClusterState cst;
 
-  const int64_t row = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t row = blockIdx.x / cs;
   const int tid = threadIdx.x;
+  ClusterState* c0 = cluster.map_shared_rank(&cst, 0);
+  int* hist0 = cluster.map_shared_rank(hist, 0);
+  uint32_t* gkey0 = cluster.map_shared_rank(gkey, 0);
+  int* gidx0 = cluster.map_shared_rank(gidx, 0);
+
   int32_t L = __ldg(context_lens + row);
   if (L < 0 || L > max_context) {
-    if (tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
+    if (tid == 0 && rank == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
     L = L < 0 ? 0 : max_context;
   }
   int32_t* o = out + row * k;
-  if (L <= k) {
-    for (int i = tid; i < k; i += kThreads) o[i] = i < L ? i : -1;
+  if (L <= k) {  // the same for every CTA of the cluster; no distributed memory touched
+    for (int i = rank * kThreads + tid; i < k; i += cs * kThreads) o[i] = i < L ? i : -1;
     return;
   }
-  const float* lg = logits + row * stride;
-  const bool cached = L <= smem_cap;
+  int chunk = (L + cs - 1) / cs;
+  chunk = (chunk + 3) & ~3;
+  const int seg0 = min(L, rank * chunk), n = min(L, seg0 + chunk) - seg0;
+  const bool cached = chunk <= seg_cap;
+  const float* lg = logits + row * stride + seg0;
+  if (rank == 0 && tid == 0) {
+    cst.kmin = 0xFFFFFFFFu;
+    cst.kmax = 0u;
+    cst.kmin2 = 0xFFFFFFFFu;
+    cst.kmax2 = 0u;
+    cst.gcount = 0;
+  }
+  for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
+
+  // load the segment (four 16-byte loads in flight per thread), keys and local min/max
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   auto take = [&](int s, float x) {
     const uint32_t u = order_key(x);
@@ -157,22 +193,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
     kmax = max(kmax, u);
     if (cached) keys[s] = u;
   };
-  // The row comes from L2 or HBM: keep four 16-byte loads in flight per thread.
   int s_done = 0;
-  if ((stride & 3) == 0 && (reinterpret_cast<uintptr_t>(lg) & 15) == 0) {
+  if ((reinterpret_cast<uintptr_t>(lg) & 15) == 0) {
     const float4* lg4 = reinterpret_cast<const float4*>(lg);
-    const int L4 = L >> 2;
-    for (int v0 = 0; v0 < L4; v0 += 4 * kThreads) {
+    const int n4 = n >> 2;
+    for (int v0 = 0; v0 < n4; v0 += 4 * kThreads) {
       float4 x[4];
 #pragma unroll
       for (int u = 0; u < 4; u++) {
         const int v = v0 + u * kThreads + tid;
-        x[u] = v < L4 ? __ldg(lg4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[u] = v < n4 ? __ldg(lg4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 4; u++) {
         const int v = v0 + u * kThreads + tid;
-        if (v < L4) {
+        if (v < n4) {
           take(4 * v, x[u].x);
           take(4 * v + 1, x[u].y);
           take(4 * v + 2, x[u].z);
@@ -180,101 +215,128 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
         }
       }
     }
-    s_done = L4 << 2;
+    s_done = n4 << 2;
   }
-  for (int s0 = s_done; s0 < L; s0 += 4 * kThreads) {
+  for (int b0 = s_done; b0 < n; b0 += 4 * kThreads) {
     float x[4];
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const int s = s0 + u * kThreads + tid;
-      x[u] = s < L ? __ldg(lg + s) : 0.f;
+      const int s = b0 + u * kThreads + tid;
+      x[u] = s < n ? __ldg(lg + s) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const int s = s0 + u * kThreads + tid;
-      if (s < L) take(s, x[u]);
+      const int s = b0 + u * kThreads + tid;
+      if (s < n) take(s, x[u]);
     }
   }
-  for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
   kmin = block_reduce<false>(kmin, uscratch);
   kmax = block_reduce<true>(kmax, uscratch);
+  cluster.sync();  // rank 0's state initialised, every histogram zeroed
+  if (tid == 0) {
+    atomicMin(&c0->kmin, kmin);
+    atomicMax(&c0->kmax, kmax);
+  }
+  cluster.sync();
   auto key_at = [&](int s) -> uint32_t { return cached ? keys[s] : order_key(__ldg(lg + s)); };
 
-  // 1. bucket histogram over [min, max]
-  const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
-  for (int s = tid; s < L; s += kThreads) atomicAdd(&hist[lin_bucket(key_value(key_at(s)), lo1, sc1)], 1);
-  if (tid == 0) {
-    sh_gcount = 0;
-    sh_kmin = 0xFFFFFFFFu;
-    sh_kmax = 0u;
-  }
+  // 1. bucket histogram over [min, max], merged into rank 0
+  const float lo1 = key_value(c0->kmin), sc1 = lin_scale(lo1, key_value(c0->kmax));
+  for (int s = tid; s < n; s += kThreads) atomicAdd(&hist[lin_bucket(key_value(key_at(s)), lo1, sc1)], 1);
   __syncthreads();
-  find_bin_from_top(hist, k, scratch, &sh_bin, &sh_rem);
-  const int b1 = sh_bin;
-  int rem = sh_rem;
-  int nb = hist[b1];
-  __syncthreads();  // every thread has read nb before any path clears the histogram
+  if (rank != 0)
+    for (int b = tid; b < kBins; b += kThreads) {
+      const int c = hist[b];
+      if (c) atomicAdd(hist0 + b, c);
+    }
+  cluster.sync();
+  if (rank == 0) {
+    find_bin_from_top(hist, k, scratch, &cst.bin, &cst.rem);
+    if (tid == 0) cst.nbk = hist[cst.bin];
+  }
+  cluster.sync();
+  const int b1 = c0->bin;
+  int rem = c0->rem;
+  int nb = c0->nbk;
+
   // optional refinement of a crowded bucket over its own value range
   float lo2 = 0.0f, sc2 = 0.0f;
   int b2 = -1;
   if (nb > kGather) {
-    for (int s = tid; s < L; s += kThreads) {
+    uint32_t bmin = 0xFFFFFFFFu, bmax = 0u;
+    for (int s = tid; s < n; s += kThreads) {
       const uint32_t u = key_at(s);
       if (lin_bucket(key_value(u), lo1, sc1) == b1) {
-        atomicMin(&sh_kmin, u);
-        atomicMax(&sh_kmax, u);
+        bmin = min(bmin, u);
+        bmax = max(bmax, u);
       }
     }
+    bmin = block_reduce<false>(bmin, uscratch);
+    bmax = block_reduce<true>(bmax, uscratch);
+    if (tid == 0) {
+      atomicMin(&c0->kmin2, bmin);
+      atomicMax(&c0->kmax2, bmax);
+    }
     for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    lo2 = key_value(sh_kmin);
-    sc2 = lin_scale(lo2, key_value(sh_kmax));
-    for (int s = tid; s < L; s += kThreads) {
+    cluster.sync();
+    lo2 = key_value(c0->kmin2);
+    sc2 = lin_scale(lo2, key_value(c0->kmax2));
+    for (int s = tid; s < n; s += kThreads) {
       const float x = key_value(key_at(s));
       if (lin_bucket(x, lo1, sc1) == b1) atomicAdd(&hist[lin_bucket(x, lo2, sc2)], 1);
     }
     __syncthreads();
-    find_bin_from_top(hist, rem, scratch, &sh_bin, &sh_rem);
-    b2 = sh_bin;
-    rem = sh_rem;
-    nb = hist[b2];
-    __syncthreads();
+    if (rank != 0)
+      for (int b = tid; b < kBins; b += kThreads) {
+        const int c = hist[b];
+        if (c) atomicAdd(hist0 + b, c);
+      }
+    cluster.sync();
+    if (rank == 0) {
+      find_bin_from_top(hist, rem, scratch, &cst.bin, &cst.rem);
+      if (tid == 0) cst.nbk = hist[cst.bin];
+    }
+    cluster.sync();
+    b2 = c0->bin;
+    rem = c0->rem;
+    nb = c0->nbk;
   }
-  // membership of the final candidate bucket
   auto in_bucket = [&](uint32_t u) -> bool {
     const float x = key_value(u);
     return lin_bucket(x, lo1, sc1) == b1 && (b2 < 0 || lin_bucket(x, lo2, sc2) == b2);
   };
 
-  // 2. resolve the threshold bucket: threshold key tau and how many keys equal to tau to keep
+  // 2. resolve the bucket: threshold key tau and how many keys equal to tau to keep
   if (nb <= kGather) {
-    for (int s = tid; s < L; s += kThreads) {
+    for (int s = tid; s < n; s += kThreads) {
       const uint32_t u = key_at(s);
       if (in_bucket(u)) {
-        const int slot = atomicAdd(&sh_gcount, 1);
-        gkey[slot] = u;
-        gidx[slot] = s;
+        const int slot = atomicAdd(&c0->gcount, 1);
+        gkey0[slot] = u;
+        gidx0[slot] = seg0 + s;
       }
     }
-    __syncthreads();
-    for (int i = tid; i < nb; i += kThreads) {
-      const uint32_t ki = gkey[i];
-      const int ii = gidx[i];
-      int rank = 0;
-      for (int j = 0; j < nb; j++) {
-        const uint32_t kj = gkey[j];
-        rank += (kj > ki) || (kj == ki && gidx[j] < ii);
-      }
-      if (rank == rem - 1) {
-        int gt = 0;
-        for (int j = 0; j < nb; j++) gt += gkey[j] > ki;
-        sh_key = ki;
-        sh_take = rem - gt;
+    cluster.sync();
+    if (rank == 0) {
+      for (int i = tid; i < nb; i += kThreads) {
+        const uint32_t ki = gkey[i];
+        const int ii = gidx[i];
+        int rk = 0;
+        for (int j = 0; j < nb; j++) {
+          const uint32_t kj = gkey[j];
+          rk += (kj > ki) || (kj == ki && gidx[j] < ii);
+        }
+        if (rk == rem - 1) {
+          int gt = 0;
+          for (int j = 0; j < nb; j++) gt += gkey[j] > ki;
+          cst.key = ki;
+          cst.take = rem - gt;
+        }
       }
     }
-    __syncthreads();
+    cluster.sync();
   } else {
-    // degenerate bucket: exact radix select over the keys inside it (11 + 11 + 10 bits)
+    // crowded bucket (many equal values): exact radix select over its keys (11 + 11 + 10 bits)
     uint32_t prefix = 0, pmask = 0;
     int r = rem;
 #pragma unroll 1
@@ -282,69 +344,91 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
       const int dshift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
       for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-      __syncthreads();
-      for (int s_base = 0; s_base < L; s_base += kThreads) {
+      cluster.sync();
+      for (int s_base = 0; s_base < n; s_base += kThreads) {
         const int s = s_base + tid;
-        bool take = false;
+        bool in = false;
         uint32_t digit = 0;
-        if (s < L) {
+        if (s < n) {
           const uint32_t u = key_at(s);
-          take = in_bucket(u) && (u & pmask) == prefix;
+          in = in_bucket(u) && (u & pmask) == prefix;
           digit = (u >> dshift) & dmask;
         }
-        const unsigned active = __ballot_sync(kFull, take);
-        if (take) {
+        const unsigned active = __ballot_sync(kFull, in);
+        if (in) {
           const unsigned peers = __match_any_sync(active, digit);
           if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
         }
       }
       __syncthreads();
-      find_bin_from_top(hist, r, scratch, &sh_bin, &sh_rem);
-      prefix |= (uint32_t)sh_bin << dshift;
+      if (rank != 0)
+        for (int b = tid; b < kBins; b += kThreads) {
+          const int c = hist[b];
+          if (c) atomicAdd(hist0 + b, c);
+        }
+      cluster.sync();
+      if (rank == 0) find_bin_from_top(hist, r, scratch, &cst.bin, &cst.rem);
+      cluster.sync();
+      prefix |= (uint32_t)c0->bin << dshift;
       pmask |= dmask << dshift;
-      r = sh_rem;
-      __syncthreads();
+      r = c0->rem;
     }
-    if (tid == 0) {
-      sh_key = prefix;
-      sh_take = r;
+    if (rank == 0 && tid == 0) {
+      cst.key = prefix;
+      cst.take = r;
     }
-    __syncthreads();
+    cluster.sync();
   }
-  const uint32_t tau = sh_key;
-  const int take_total = sh_take;
+  const uint32_t tau = c0->key;
+  const int take_total = c0->take;
 
-  // 3. ordered output
-  int chunk = (L + kThreads - 1) / kThreads;
-  chunk |= 1;  // odd stride between threads' runs: conflict-free shared-memory reads
-  const int s0 = min(L, tid * chunk), s1 = min(L, s0 + chunk);
+  // 3. ordered output: per-thread contiguous runs inside this CTA's segment
+  const int tchunk = ((n + kThreads - 1) / kThreads) | 1;  // odd stride: conflict-free reads
+  const int s0 = min(n, tid * tchunk), s1 = min(n, s0 + tchunk);
   int gt = 0, eq = 0;
   for (int s = s0; s < s1; s++) {
     const uint32_t u = key_at(s);
     gt += u > tau;
     eq += u == tau;
   }
-  int tot;
-  const int eq_before = block_excl_scan(eq, scratch, tot);
-  const int take_eq = max(0, min(eq, take_total - eq_before));
-  const int pos = block_excl_scan(gt + take_eq, scratch, tot);
+  int tot_gt, tot_eq;
+  (void)block_excl_scan(gt, scratch, tot_gt);
+  const int eq_local = block_excl_scan(eq, scratch, tot_eq);
+  if (tid == 0) {
+    c0->gt[rank] = tot_gt;
+    c0->eq[rank] = tot_eq;
+  }
+  cluster.sync();
+  int eq_before_cta = 0, sel_before_cta = 0;
+  for (int c = 0; c < rank; c++) {
+    const int e = c0->eq[c];
+    sel_before_cta += c0->gt[c] + max(0, min(e, take_total - eq_before_cta));
+    eq_before_cta += e;
+  }
+  const int take_eq = max(0, min(eq, take_total - eq_before_cta - eq_local));
+  int tot_sel;
+  const int pos = sel_before_cta + block_excl_scan(gt + take_eq, scratch, tot_sel);
   int w = pos, te = 0;
   for (int s = s0; s < s1 && w < k; s++) {
     const uint32_t u = key_at(s);
-    if (u > tau || (u == tau && te++ < take_eq)) o[w++] = s;
+    if (u > tau || (u == tau && te++ < take_eq)) o[w++] = seg0 + s;
   }
-  for (int i = tot + tid; i < k; i += kThreads) o[i] = -1;  // only for non-finite rows
+  if (rank == cs - 1)  // only for rows with non-finite logits can the selection fall short of k
+    for (int i = sel_before_cta + tot_sel + tid; i < k; i += kThreads) o[i] = -1;
+  cluster.sync();  // rank 0's shared memory is read until here
 }
 
 }  // namespace
 
 int32_t topk_smem_cap() { return 49152; }
 
+int topk_cluster_size(int32_t n_rows) {
+  return n_rows <= 19 ? 8 : (n_rows <= 76 ? 4 : (n_rows <= 152 ? 2 : 1));
+}
+
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, int32_t* out, int32_t* status, cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
-  const int32_t cap = min(max_context, topk_smem_cap());
-  const size_t smem = (size_t)(cap > 0 ? cap : 1) * sizeof(uint32_t);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -352,8 +436,22 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  topk_kernel<<<n_rows, kThreads, smem, stream>>>(logits, stride, context_lens, max_context, k, out, cap, status);
-  return cudaGetLastError();
+  const int cs = topk_cluster_size(n_rows);
+  const int chunk = (((max_context + cs - 1) / cs) + 3) & ~3;
+  const int32_t seg_cap = min(chunk, topk_smem_cap());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_rows * cs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)(seg_cap > 0 ? seg_cap : 1) * sizeof(uint32_t);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel, logits, stride, context_lens, max_context, k, out, seg_cap, status);
 }
 
 }  // namespace fp4idx
