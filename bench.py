@@ -34,7 +34,7 @@ UNIT = "query rows/s"
 L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_decode_b64_traffic.json")
 LOGITS_SRC = os.path.join(ROOT, "sparse_attention_fp4_gb300", "csrc", "logits_mxf4.cu")
-KERNELS_PER_STEP = 5  # store_k, quant_q, build_schedule, logits, topk
+KERNELS_PER_STEP = 6  # store_k, quant_q, build_schedule, logits, top-k filter, top-k select
 
 WORKLOADS = {
     "decode_b64": ("decode_batch64", 1001),
@@ -241,6 +241,8 @@ class DecodeStep:
         self.sched = torch.empty(fp4idx.schedule_workspace_bytes(self.T), dtype=torch.uint8, device=device)
         self.logits = torch.empty((self.T, (self.max_ctx + 3) // 4 * 4), dtype=torch.float32, device=device)
         self.topk = torch.empty((self.T, self.k), dtype=torch.int32, device=device)
+        self.topk_ws = torch.empty(fp4idx.topk_workspace_bytes(self.T, self.max_ctx), dtype=torch.uint8,
+                                   device=device)
         torch.cuda.synchronize(device)
 
     def calls(self):
@@ -253,12 +255,35 @@ class DecodeStep:
             ("build_schedule", lambda: f.build_schedule(self.cl, self.rs, self.sched)),
             ("logits", lambda: f.logits(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
                                         self.max_ctx, self.sched, self.logits, status=self.status)),
-            ("topk", lambda: f.topk(self.logits, self.cl, self.max_ctx, self.k, self.topk, status=self.status)),
+            ("topk", lambda: f.topk(self.logits, self.cl, self.max_ctx, self.k, self.topk_ws, self.topk,
+                                    status=self.status)),
         ]
 
     def launch(self):
         for _, fn in self.calls():
             fn()
+
+    def launch_forked(self, side_streams):
+        """The step with its independent launches overlapped: K store, Q quant and the
+        schedule depend on nothing but their inputs, so they run on three streams and the
+        logits wait for all three (the form captured into the step's graph)."""
+        import torch
+        calls = dict(self.calls())
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        done = []
+        for name, st in zip(("store_k", "quant_q", "build_schedule"), side_streams):
+            st.wait_event(start)
+            with torch.cuda.stream(st):
+                calls[name]()
+                ev = torch.cuda.Event()
+                ev.record(st)
+            done.append(ev)
+        for ev in done:
+            cur.wait_event(ev)
+        calls["logits"]()
+        calls["topk"]()
 
 
 def run_gpu(args):
@@ -291,8 +316,9 @@ def run_gpu(args):
         st.launch()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
+    side = [torch.cuda.Stream(device) for _ in range(3)]
     with torch.cuda.graph(g):
-        st.launch()
+        st.launch_forked(side)
     for _ in range(max(3, args.warmup)):
         g.replay()
     torch.cuda.synchronize()
@@ -373,7 +399,7 @@ def run_gpu(args):
             "config": {"workload": b.name, "rows": b.n_rows, "heads": 64, "head_dim": 128, "topk": b.topk,
                        "context_tokens": int(b.context_lens.sum()), "cache_pages": b.num_pages,
                        "step": "K store (newest token per sequence) + Q quant + schedule + logits + top-k, "
-                               "one CUDA graph replay",
+                               "one CUDA graph replay (store, quant and schedule on parallel branches)",
                        "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "kcache_gbs": round(ab["k_cache"] / (logits_us * 1e-6) / 1e9, 1),

@@ -148,8 +148,9 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
  *   max_context         host-known upper bound of context_lens (<= FP4IDX_MAX_CONTEXT)
  *   k                   1..FP4IDX_MAX_TOPK
  *   schedule            built by fp4idx_build_schedule for these rows
- *   workspace           >= fp4idx_logits_workspace_bytes(n_rows, max_context, k) bytes
- *                       (may be 0 bytes when logits_out is given)
+ *   workspace           >= fp4idx_logits_workspace_bytes(n_rows, max_context, k) bytes:
+ *                       a logits buffer (unused when logits_out is given) and the
+ *                       top-k scratch
  *   topk_idx  [n_rows,k] int32 (written): the k highest-logit token indices of each
  *             row in ascending order; all of them when context_len <= k; -1 pads.
  *   logits_out [n_rows, logits_stride] fp32 (nullable): when given, receives
@@ -170,15 +171,19 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
  * select elsewhere.  fp4idx_logits writes logits_out[t][s] for s < context_lens[t]
  * (logits_stride >= max_context; the rest of each row is not written).  fp4idx_topk
  * selects from such a buffer: topk_idx[t] = the k largest of logits[t][0..L_t), ascending
- * positions, -1 padding; ties at the k-th value go to the lower positions.
+ * positions, -1 padding; ties at the k-th value go to the lower positions.  Its scratch
+ * (a candidate list per row) lives in `workspace`, at least
+ * fp4idx_topk_workspace_bytes(n_rows, max_context) bytes, 16-byte aligned.
  */
 int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows, int32_t n_heads,
                   const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
                   int64_t num_seqs, int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
                   int32_t max_context, const void* schedule, size_t schedule_bytes, float* logits_out,
                   int64_t logits_stride, int32_t* status_dev, void* stream);
+size_t fp4idx_topk_workspace_bytes(int64_t max_rows, int32_t max_context);
 int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
-                int32_t max_context, int32_t k, int32_t* topk_idx, int32_t* status_dev, void* stream);
+                int32_t max_context, int32_t k, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                int32_t* status_dev, void* stream);
 
 /* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
  * a test/diagnostic helper, not for the hot path. */

@@ -113,10 +113,20 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
                                                  as_stream(stream)));
 }
 
+// Layout of the logits + top-k workspace: [logits buffer][top-k scratch].
+inline size_t logits_region_bytes(int64_t rows, int32_t max_context) {
+  return ((size_t)rows * (size_t)logits_row_stride(max_context) * sizeof(float) + 255) & ~(size_t)255;
+}
+
+size_t fp4idx_topk_workspace_bytes(int64_t max_rows, int32_t max_context) {
+  if (max_rows < 0 || max_context < 0) return 0;
+  return fp4idx::topk_workspace_bytes(max_rows, max_context);
+}
+
 size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int32_t k) {
   (void)k;
   if (max_rows < 0 || max_context < 0) return 0;
-  return (size_t)max_rows * (size_t)logits_row_stride(max_context) * sizeof(float);
+  return logits_region_bytes(max_rows, max_context) + fp4idx::topk_workspace_bytes(max_rows, max_context);
 }
 
 namespace {
@@ -173,7 +183,8 @@ int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float*
 }
 
 int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
-                int32_t max_context, int32_t k, int32_t* topk_idx, int32_t* status_dev, void* stream) {
+                int32_t max_context, int32_t k, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                int32_t* status_dev, void* stream) {
   if (n_rows < 0 || n_rows > INT32_MAX - 1 || max_context < 0 || k < 1 || k > FP4IDX_MAX_TOPK)
     return FP4IDX_ERR_INVALID_ARG;
   if (max_context > FP4IDX_MAX_CONTEXT) return FP4IDX_ERR_UNSUPPORTED;
@@ -182,8 +193,10 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
       logits_stride < max_context)
     return FP4IDX_ERR_INVALID_ARG;
   if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
-  return from_cuda(fp4idx::launch_topk(logits, logits_stride, context_lens, (int32_t)n_rows, max_context, k, topk_idx,
-                                       status_dev, as_stream(stream)));
+  if (!workspace || !aligned16(workspace)) return FP4IDX_ERR_INVALID_ARG;
+  if (workspace_bytes < fp4idx::topk_workspace_bytes(n_rows, max_context)) return FP4IDX_ERR_WORKSPACE;
+  return from_cuda(fp4idx::launch_topk(logits, logits_stride, context_lens, (int32_t)n_rows, max_context, k,
+                                       workspace, topk_idx, status_dev, as_stream(stream)));
 }
 
 int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
@@ -198,6 +211,8 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
   if (k < 1 || k > FP4IDX_MAX_TOPK) return FP4IDX_ERR_INVALID_ARG;
   if (n_rows == 0) return FP4IDX_OK;
   if (!topk_idx || !aligned4(topk_idx)) return FP4IDX_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return FP4IDX_ERR_INVALID_ARG;
+  if (workspace_bytes < fp4idx_logits_workspace_bytes(n_rows, max_context, k)) return FP4IDX_ERR_WORKSPACE;
   float* buf;
   int64_t stride;
   if (logits_out) {
@@ -206,16 +221,15 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
     stride = logits_stride;
   } else {
     stride = logits_row_stride(max_context);
-    if (!workspace || !aligned16(workspace)) return FP4IDX_ERR_INVALID_ARG;
-    if (workspace_bytes < fp4idx_logits_workspace_bytes(n_rows, max_context, k)) return FP4IDX_ERR_WORKSPACE;
     buf = reinterpret_cast<float*>(workspace);
   }
+  void* topk_ws = reinterpret_cast<uint8_t*>(workspace) + logits_region_bytes(n_rows, max_context);
   cudaStream_t s = as_stream(stream);
   st = launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs, max_pages,
                              row_seq, context_lens, max_context, schedule, buf, stride, status_dev, s);
   if (st != FP4IDX_OK) return st;
-  return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_idx,
-                                       status_dev, s));
+  return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_ws,
+                                       topk_idx, status_dev, s));
 }
 
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream) {

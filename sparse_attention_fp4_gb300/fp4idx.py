@@ -62,7 +62,8 @@ _SIGS = {
                                           _i32, _i32, _vp, _sz, _vp, _sz, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_logits": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
                                      _vp, _sz, _vp, _i64, _vp, _vp]),
-    "fp4idx_topk": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _vp]),
+    "fp4idx_topk_workspace_bytes": (_sz, [_i64, _i32]),
+    "fp4idx_topk": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
     "fp4idx_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
 }
 
@@ -191,7 +192,7 @@ def logits_topk(q_payload, q_scale, w, payload, scale, page_table, row_seq, cont
         _ptr(scale, "scale", _U8, num_pages * 256), num_pages, _ptr(page_table, "page_table", _I32), S, max_pages,
         _ptr(row_seq, "row_seq", _I32, T), _ptr(context_lens, "context_lens", _I32, T), int(max_context), int(k),
         _ptr(schedule, "schedule", _U8), schedule.numel(),
-        _ptr(workspace, "workspace", _U8, nullable=True), workspace.numel() if workspace is not None else 0,
+        _ptr(workspace, "workspace", _U8), workspace.numel(),
         _ptr(topk_idx, "topk_idx", _I32, T * int(k)), _ptr(logits_out, "logits_out", _F32, nullable=True),
         stride, _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_logits_topk", rc)
@@ -212,10 +213,15 @@ def logits(q_payload, q_scale, w, payload, scale, page_table, row_seq, context_l
     _check("fp4idx_logits", rc)
 
 
-def topk(logits_buf, context_lens, max_context, k, topk_idx, status=None, stream=None):
+def topk_workspace_bytes(max_rows, max_context) -> int:
+    return int(_lib.fp4idx_topk_workspace_bytes(int(max_rows), int(max_context)))
+
+
+def topk(logits_buf, context_lens, max_context, k, workspace, topk_idx, status=None, stream=None):
     T = context_lens.numel()
     rc = _lib.fp4idx_topk(_ptr(logits_buf, "logits", _F32), logits_buf.shape[1],
                           _ptr(context_lens, "context_lens", _I32, T), T, int(max_context), int(k),
+                          _ptr(workspace, "workspace", _U8), workspace.numel(),
                           _ptr(topk_idx, "topk_idx", _I32, T * int(k)), _ptr(status, "status", _I32, 1, nullable=True),
                           _stream_ptr(stream))
     _check("fp4idx_topk", rc)

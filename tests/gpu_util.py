@@ -43,12 +43,11 @@ def run_gpu_indexer(b, cos_sin_np, with_logits=True, page_table=None, payload=No
     fp4idx.build_schedule(cl, rs, sched)
     topk = torch.empty((T, k), dtype=torch.int32, device="cuda")
     pt = dev(b.page_table if page_table is None else page_table)
+    ws = torch.empty(fp4idx.logits_workspace_bytes(T, Lmax, k), dtype=torch.uint8, device="cuda")
     if with_logits:
         lg = torch.full((T, Lmax), float("nan"), dtype=torch.float32, device="cuda")
-        ws = None
     else:
         lg = None
-        ws = torch.empty(fp4idx.logits_workspace_bytes(T, Lmax, k), dtype=torch.uint8, device="cuda")
     fp4idx.logits_topk(qp, qs, dev(b.w), payload, scale, pt, rs, cl, Lmax, k, sched, ws, topk, logits_out=lg,
                        status=status)
     torch.cuda.synchronize()

@@ -28,7 +28,8 @@ def run(rows, lens, k, stride=None):
     cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out = torch.empty((T, k), dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fp4idx.topk(lg, cl, Lmax, k, out, status=status)
+    ws = torch.empty(fp4idx.topk_workspace_bytes(T, Lmax), dtype=torch.uint8, device="cuda")
+    fp4idx.topk(lg, cl, Lmax, k, ws, out, status=status)
     torch.cuda.synchronize()
     assert fp4idx.read_status(status) == 0
     return out.cpu().numpy()
@@ -49,10 +50,14 @@ def _dist(rng, kind, L):
         return np.full(L, 3.25, np.float32)
     if kind == "positive_narrow":
         return (100 + rng.random(L) * 1e-3).astype(np.float32)
+    if kind == "signed_zeros":  # -0 and +0 are equal values: ties go to the lower positions
+        x = np.where(rng.random(L) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+        x[rng.random(L) < 0.01] = np.float32(1.0)
+        return x
     raise ValueError(kind)
 
 
-@pytest.mark.parametrize("kind", ["normal", "cauchy", "outliers", "dups", "equal", "positive_narrow"])
+@pytest.mark.parametrize("kind", ["normal", "cauchy", "outliers", "dups", "equal", "positive_narrow", "signed_zeros"])
 @pytest.mark.parametrize("stride_pad", [0, 3])
 def test_topk_distributions(kind, stride_pad):
     rng = np.random.default_rng(hash(kind) % 1000)
