@@ -56,6 +56,7 @@ extern "C" {
 #define FP4IDX_FP8_PAGE_BYTES (64 * 128 + 64 * 4)
 #define FP4IDX_MAX_TOPK 4096
 #define FP4IDX_MAX_CONTEXT 65536
+#define FP4IDX_TOPK_NOALLOC_MAX_BYTES (16u * 1024u * 1024u) /* fixed scratch of fp4idx_topk_noalloc */
 
 typedef enum {
   FP4IDX_OK = 0,
@@ -67,7 +68,8 @@ typedef enum {
   FP4IDX_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its iteration limit */
   FP4IDX_ERR_BAD_POSITION = 7, /* device: RoPE position outside [0, max_pos) */
   FP4IDX_ERR_BAD_LENGTH = 8,   /* device: context length < 0 or above max_context / page-table width */
-  FP4IDX_ERR_SCHEDULE = 9      /* schedule built for another row count or grid */
+  FP4IDX_ERR_SCHEDULE = 9,     /* schedule built for another row count or grid */
+  FP4IDX_ERR_SCRATCH_LIMIT = 10 /* fp4idx_topk_noalloc: the call needs more than its fixed scratch */
 } fp4idx_status;
 
 /* Human-readable name of a status code (static string). */
@@ -184,6 +186,30 @@ size_t fp4idx_topk_workspace_bytes(int64_t max_rows, int32_t max_context);
 int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
                 int32_t max_context, int32_t k, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                 int32_t* status_dev, void* stream);
+
+/*
+ * fp4idx_topk_noalloc -- fp4idx_topk for callers that may not allocate device memory.
+ * The pages this library follows have no counterpart: it is an interface addition.
+ * A serving runtime that gives all of its memory to its own pool at start-up, or a
+ * plug-in host that passes a library only a stream and the call's tensors, cannot hand
+ * fp4idx_topk a workspace; this entry point takes none.
+ *
+ * Same arguments and result as fp4idx_topk, without workspace/workspace_bytes.  The
+ * candidate scratch is a fixed array of the library's device code,
+ * FP4IDX_TOPK_NOALLOC_MAX_BYTES per device; no call allocates or frees anything.
+ *   - Limit: fp4idx_topk_workspace_bytes(n_rows, max_context) must not exceed
+ *     FP4IDX_TOPK_NOALLOC_MAX_BYTES (e.g. 64 rows at max_context 32768 need 8 MiB + 2 KiB);
+ *     a larger call returns FP4IDX_ERR_SCRATCH_LIMIT and enqueues nothing.
+ *   - Setup: the first valid call on each device (with that device current) looks up
+ *     the array's address once; make that first call before any stream capture begins.
+ *     Of the conventions at the top of this file, the one on graph capture is not
+ *     stated for this entry point.
+ *   - Nothing in the array has to start at zero (each call writes the counts it reads).
+ *   - All calls on a device share the array: calls whose kernels may overlap (unordered
+ *     streams, concurrent host threads) race on it.  Order them on one stream.
+ */
+int fp4idx_topk_noalloc(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
+                        int32_t max_context, int32_t k, int32_t* topk_idx, int32_t* status_dev, void* stream);
 
 /* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
  * a test/diagnostic helper, not for the hot path. */

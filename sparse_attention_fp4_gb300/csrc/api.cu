@@ -43,6 +43,7 @@ const char* fp4idx_status_string(int status) {
     case FP4IDX_ERR_BAD_POSITION: return "RoPE position outside the table";
     case FP4IDX_ERR_BAD_LENGTH: return "context length out of range";
     case FP4IDX_ERR_SCHEDULE: return "schedule does not match the call";
+    case FP4IDX_ERR_SCRATCH_LIMIT: return "call needs more than the fixed top-k scratch";
     default: return "unknown status";
   }
 }

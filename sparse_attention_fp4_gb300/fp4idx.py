@@ -28,6 +28,7 @@ STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error", 4: "workspace too small",
     5: "page id or slot outside the cache", 6: "pipeline wait timed out", 7: "RoPE position outside the table",
     8: "context length out of range", 9: "schedule does not match the call",
+    10: "call needs more than the fixed top-k scratch",
 }
 
 
@@ -64,6 +65,7 @@ _SIGS = {
                                      _vp, _sz, _vp, _i64, _vp, _vp]),
     "fp4idx_topk_workspace_bytes": (_sz, [_i64, _i32]),
     "fp4idx_topk": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
+    "fp4idx_topk_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _vp]),
     "fp4idx_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
 }
 
@@ -225,6 +227,19 @@ def topk(logits_buf, context_lens, max_context, k, workspace, topk_idx, status=N
                           _ptr(topk_idx, "topk_idx", _I32, T * int(k)), _ptr(status, "status", _I32, 1, nullable=True),
                           _stream_ptr(stream))
     _check("fp4idx_topk", rc)
+
+
+TOPK_NOALLOC_MAX_BYTES = 16 * 1024 * 1024  # FP4IDX_TOPK_NOALLOC_MAX_BYTES
+
+
+def topk_noalloc(logits_buf, context_lens, max_context, k, topk_idx, status=None, stream=None):
+    """fp4idx_topk with the library's fixed per-device scratch: no workspace argument."""
+    T = context_lens.numel()
+    rc = _lib.fp4idx_topk_noalloc(_ptr(logits_buf, "logits", _F32), logits_buf.shape[1],
+                                  _ptr(context_lens, "context_lens", _I32, T), T, int(max_context), int(k),
+                                  _ptr(topk_idx, "topk_idx", _I32, T * int(k)),
+                                  _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_topk_noalloc", rc)
 
 
 def read_status(status, stream=None) -> int:
