@@ -174,7 +174,8 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
  * (logits_stride >= max_context; the rest of each row is not written).  fp4idx_topk
  * selects from such a buffer: topk_idx[t] = the k largest of logits[t][0..L_t), ascending
  * positions, -1 padding; ties at the k-th value go to the lower positions.  Its scratch
- * (a candidate list per row) lives in `workspace`, at least
+ * (a candidate list per row and per-row arrival counters, which each call clears with
+ * cudaMemsetAsync on `stream`) lives in `workspace`, at least
  * fp4idx_topk_workspace_bytes(n_rows, max_context) bytes, 16-byte aligned.
  */
 int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows, int32_t n_heads,
@@ -198,13 +199,14 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
  * candidate scratch is a fixed array of the library's device code,
  * FP4IDX_TOPK_NOALLOC_MAX_BYTES per device; no call allocates or frees anything.
  *   - Limit: fp4idx_topk_workspace_bytes(n_rows, max_context) must not exceed
- *     FP4IDX_TOPK_NOALLOC_MAX_BYTES (e.g. 64 rows at max_context 32768 need 8 MiB + 2 KiB);
- *     a larger call returns FP4IDX_ERR_SCRATCH_LIMIT and enqueues nothing.
+ *     FP4IDX_TOPK_NOALLOC_MAX_BYTES (up to 85 rows fit at max_context 32768, 42 at
+ *     65536); a larger call returns FP4IDX_ERR_SCRATCH_LIMIT and enqueues nothing.
  *   - Setup: the first valid call on each device (with that device current) looks up
  *     the array's address once; make that first call before any stream capture begins.
  *     Of the conventions at the top of this file, the one on graph capture is not
  *     stated for this entry point.
- *   - Nothing in the array has to start at zero (each call writes the counts it reads).
+ *   - Zero state: the per-row arrival counters in the array must be zero when the
+ *     kernel starts; every call clears them itself (cudaMemsetAsync on `stream`).
  *   - All calls on a device share the array: calls whose kernels may overlap (unordered
  *     streams, concurrent host threads) race on it.  Order them on one stream.
  */

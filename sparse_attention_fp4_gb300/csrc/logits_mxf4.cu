@@ -5,22 +5,30 @@
 // guarded page table; the logits are
 //   logits[t,s] = sum_h w[t,h] * ReLU(q_fp4[t,h] . k_fp4[s]),   s < context_lens[t].
 //
-// GB300 design (one persistent CTA per SM, 11 warps):
+// GB300 design (one persistent CTA per SM, 15 warps):
 //   A tile is 128 tokens = two cache pages, the A operand of an M = 128 MMA laid out as
 //   [block c][page][64 tokens][16 B] (canonical no-swizzle K-major).  A pipeline stage
 //   holds two tiles (four pages).
-//   warp 2  producer: per stage, four TMA tile::gather4 loads of the payload (each
-//           fetches the 1 KB rows (page, c) of two pages for two blocks, landing
-//           directly in the interleaved operand layout) and one gather4 of the four
-//           256 B scale pages; per work item, the group's query rows (one bulk copy
-//           for the payloads, one for the scales).  Page ids are read 32 at a time.
-//   warp 1  MMA issuer: per (stage, query row), two kind::mxf4 MMAs (K = 64 each) per
-//           tile into a 128-column TMEM slot (2 slots): D[128 tokens x 64 heads] per tile.
-//   warp 0  scale transposer: reorders the [page][c][token] scale bytes into the
-//           32 x 16 B atom that tcgen05.cp replicates over the four TMEM lane groups,
-//           issues those copies and signals the MMA issuer with tcgen05.commit, which
-//           keeps every operation but the MMAs off the issuer's serial path.
-//   warps 3-10 epilogue, two per TMEM lane group taking alternate slots: thread =
+//   warps 5-6 producers, taking alternate stages (issuing a gather4 occupies a warp
+//           for about 120 cycles, so one warp alone cannot keep up with the SM's
+//           share of HBM bandwidth): per stage, four TMA tile::gather4 loads of the
+//           payload (each fetches the 1 KB rows (page, c) of two pages for two blocks,
+//           landing directly in the interleaved operand layout) and one gather4 of the
+//           four 256 B scale pages; warp 5 also loads each work item's query rows (one
+//           bulk copy for the payloads, one for the scales).  Page ids are read 32 at
+//           a time.
+//   warps 0-3 scale writers, one per TMEM lane group: per tile, lane m of group m/32
+//           gathers token m's four block-scale bytes from the [page][c][token] scale
+//           pages and writes them with tcgen05.st to lane m, column m/32 of the tile's
+//           four scale columns, where the block-scaled MMA reads row m's scales; per
+//           work item, the query rows' head scales go to every lane group (heads l and
+//           32 + l in lane l).  Four warps on four schedulers keep this transposition,
+//           which every stage needs, off the critical path.
+//   warp 4  MMA issuer: per (stage, query row), two kind::mxf4 MMAs (K = 64 each) per
+//           tile into a 64-column TMEM slot of its own (6 slots): D[128 tokens x 64 heads].
+//           Slots per tile let the epilogue release each tile as soon as it has read
+//           it and keep the MMAs up to three stages ahead of it.
+//   warps 7-14 epilogue, two per TMEM lane group taking alternate slots: thread =
 //           TMEM lane = token; ReLU, head-weighted sum, mask at the row's context
 //           length, coalesced fp32 store.
 // Work items come from the length-balanced schedule (schedule.cuh).  Every wait is
@@ -37,42 +45,47 @@ namespace {
 
 constexpr int kStages = 8;          // pipeline stages, two tiles each
 constexpr int kTilesPerStage = 2;
-constexpr int kSlots = 2;           // TMEM accumulator slots, 128 columns (two tiles) each
+constexpr int kAccSlots = 3;        // TMEM accumulator slots, one (stage, query row) each: 128 columns
 constexpr int kEpiWarps = 8;
-constexpr int kWarps = 3 + kEpiWarps;
+constexpr int kProducers = 2;
+constexpr int kScaleWarps = 4;
+constexpr int kWarps = kScaleWarps + 1 + kProducers + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpSf = 0, kWarpMma = 1, kWarpProducer = 2, kWarpEpi0 = 3;
+constexpr int kWarpMma = kScaleWarps, kWarpProducer = kWarpMma + 1, kWarpEpi0 = kWarpProducer + kProducers;
+static_assert(kStages % kProducers == 0 && kEpiWarps == 8, "stage ownership; four consecutive warps per half");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc = 0;                                     // kSlots x 128 fp32
-constexpr uint32_t kColSfa = kSlots * 128;                          // kStages x 2 atoms x 4
+constexpr uint32_t kColAcc = 0;                                     // kAccSlots x 128 fp32
+constexpr uint32_t kColSfa = kAccSlots * 128;                       // kStages x 2 tiles x 4
 constexpr uint32_t kColSfb = kColSfa + kStages * kTilesPerStage * 4;  // 2 x kGroupMax x 4
 static_assert(kColSfb + 2 * kGroupMax * 4 <= kTmemCols, "tensor memory budget");
-// Slot use u goes to epilogue half u % 2; with an even slot count every slot always
-// belongs to one half, which consumes its uses in order, so a parity wait is never
-// more than one phase ahead of the barrier.
-static_assert(kSlots % 2 == 0, "slots per epilogue half");
+// Every epilogue warp consumes every slot use in order (half h reads tile h), so no
+// parity wait is ever more than one phase ahead of its barrier.
 
 // shared memory layout (bytes from the 1 KB-aligned dynamic base)
 constexpr uint32_t kTileBytes = 8192;   // [c][2 pages][64][16]
 constexpr uint32_t kKPayBytes = kTilesPerStage * kTileBytes;
 constexpr uint32_t kKScBytes = 4 * 256;  // [4 pages][c][64]
-constexpr uint32_t kAtomBytes = 512;     // 32 x 16 B
 constexpr uint32_t kQPayBytes = kGroupMax * 4096;
 constexpr uint32_t kQScBytes = kGroupMax * 256;
 constexpr uint32_t OFF_KPAY = 0;
 constexpr uint32_t OFF_KSC = OFF_KPAY + kStages * kKPayBytes;
-constexpr uint32_t OFF_KATOM = OFF_KSC + kStages * kKScBytes;
-constexpr uint32_t OFF_QPAY = OFF_KATOM + kStages * kTilesPerStage * kAtomBytes;
+constexpr uint32_t OFF_QPAY = OFF_KSC + kStages * kKScBytes;
 constexpr uint32_t OFF_QSC = OFF_QPAY + 2 * kQPayBytes;
-constexpr uint32_t OFF_QATOM = OFF_QSC + 2 * kQScBytes;
-constexpr uint32_t OFF_LEN = OFF_QATOM + 2 * kGroupMax * kAtomBytes;  // per epilogue warp: [kGroupMax] int32
+constexpr uint32_t OFF_LEN = OFF_QSC + 2 * kQScBytes;  // per epilogue warp: [kGroupMax] int32
 constexpr uint32_t OFF_BAR = OFF_LEN + kEpiWarps * kGroupMax * 4;
-constexpr int kNumBars = 3 * kStages + 6 + 2 * kSlots;
-constexpr uint32_t OFF_MISC = OFF_BAR + kNumBars * 8;
+constexpr int kNumBars = 2 * kStages + 6 + kAccSlots;
+// Monotonic arrival counters: per stage buffer, scale-writer warps that finished it
+// (kScaleWarps per use); per accumulator slot, epilogue warps that released it
+// (kEpiWarps per use).  The MMA issuer reads both with plain acquire loads issued
+// together, which costs it one shared-memory round trip where two mbarrier probes
+// (about 200 cycles each) would cost four times as much; counts that only grow
+// cannot alias the way a phase-parity wait can.
+constexpr uint32_t OFF_CNT = OFF_BAR + kNumBars * 8;
+constexpr uint32_t OFF_MISC = OFF_CNT + (kStages + kAccSlots) * 4;
 constexpr uint32_t kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0, "alignment");
@@ -80,14 +93,12 @@ static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0, "a
 // barrier slots
 __device__ __forceinline__ uint32_t bar_kfull(uint32_t b, int s) { return b + OFF_BAR + 8u * s; }
 __device__ __forceinline__ uint32_t bar_kempty(uint32_t b, int s) { return b + OFF_BAR + 8u * (kStages + s); }
-__device__ __forceinline__ uint32_t bar_sfready(uint32_t b, int s) { return b + OFF_BAR + 8u * (2 * kStages + s); }
-__device__ __forceinline__ uint32_t bar_qfull(uint32_t b, int q) { return b + OFF_BAR + 8u * (3 * kStages + q); }
-__device__ __forceinline__ uint32_t bar_qempty(uint32_t b, int q) { return b + OFF_BAR + 8u * (3 * kStages + 2 + q); }
-__device__ __forceinline__ uint32_t bar_qsf(uint32_t b, int q) { return b + OFF_BAR + 8u * (3 * kStages + 4 + q); }
-__device__ __forceinline__ uint32_t bar_accfull(uint32_t b, int s) { return b + OFF_BAR + 8u * (3 * kStages + 6 + s); }
-__device__ __forceinline__ uint32_t bar_accempty(uint32_t b, int s) {
-  return b + OFF_BAR + 8u * (3 * kStages + 6 + kSlots + s);
-}
+__device__ __forceinline__ uint32_t bar_qfull(uint32_t b, int q) { return b + OFF_BAR + 8u * (2 * kStages + q); }
+__device__ __forceinline__ uint32_t bar_qempty(uint32_t b, int q) { return b + OFF_BAR + 8u * (2 * kStages + 2 + q); }
+__device__ __forceinline__ uint32_t bar_qsf(uint32_t b, int q) { return b + OFF_BAR + 8u * (2 * kStages + 4 + q); }
+__device__ __forceinline__ uint32_t bar_accfull(uint32_t b, int s) { return b + OFF_BAR + 8u * (2 * kStages + 6 + s); }
+__device__ __forceinline__ uint32_t cnt_sf(uint32_t b, int s) { return b + OFF_CNT + 4u * s; }
+__device__ __forceinline__ uint32_t cnt_slot(uint32_t b, int s) { return b + OFF_CNT + 4u * (kStages + s); }
 
 struct LogitsParams {
   const uint8_t* q_payload;
@@ -121,6 +132,28 @@ __device__ __forceinline__ bool poll(uint32_t bar, uint32_t parity, const Ctl& c
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (honor_abort && *c.abort) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) {
+        *c.abort = 1;
+        record_error(c.status, FP4IDX_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait, by one thread, until counter a has reached need_a and counter b need_b
+// (wrap-safe comparisons); both loads are issued before either is tested.
+__device__ __forceinline__ bool wait_counts(uint32_t a, uint32_t need_a, uint32_t b, uint32_t need_b, const Ctl& c) {
+  auto ready = [&]() {
+    const uint32_t va = ptx::smem_ld_acquire(a), vb = ptx::smem_ld_acquire(b);
+    return (int32_t)(va - need_a) >= 0 && (int32_t)(vb - need_b) >= 0;
+  };
+  if (ready()) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ready()) return true;
+    if ((it & 63u) == 0) {
+      if (*c.abort) return false;
       if (ptx::globaltimer() - t0 > kTimeoutNs) {
         *c.abort = 1;
         record_error(c.status, FP4IDX_ERR_TIMEOUT);
@@ -182,17 +215,14 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     for (int s = 0; s < kStages; s++) {
       ptx::mbar_init(bar_kfull(sb, s), 1);
       ptx::mbar_init(bar_kempty(sb, s), 1);
-      ptx::mbar_init(bar_sfready(sb, s), 1);
     }
+    for (int i = 0; i < kStages + kAccSlots; i++) reinterpret_cast<uint32_t*>(smem + OFF_CNT)[i] = 0u;
     for (int q = 0; q < 2; q++) {
       ptx::mbar_init(bar_qfull(sb, q), 1);
       ptx::mbar_init(bar_qempty(sb, q), 1);
-      ptx::mbar_init(bar_qsf(sb, q), 1);
+      ptx::mbar_init(bar_qsf(sb, q), kScaleWarps);
     }
-    for (int s = 0; s < kSlots; s++) {
-      ptx::mbar_init(bar_accfull(sb, s), 1);
-      ptx::mbar_init(bar_accempty(sb, s), 4);
-    }
+    for (int s = 0; s < kAccSlots; s++) ptx::mbar_init(bar_accfull(sb, s), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -211,8 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   items.init(sv, blockIdx.x, gridDim.x);
   int32_t g, t0, t1;
 
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
+  if (warp >= kWarpProducer && warp < kWarpEpi0) {
+    // ------------------------------------------------------------ producers
+    const int pw = warp - kWarpProducer;  // issues the stages with kctr % kProducers == pw
     uint32_t kctr = 0, ictr = 0;
     bool ok = true;
     while (ok && items.next(g, t0, t1)) {
@@ -223,14 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       maxlen = min(maxlen, min(p.max_context, p.max_pages * kPage));
       const int32_t npages = (maxlen + kPage - 1) / kPage;
       const int qb = ictr & 1;
-      ok = wait_lane0(bar_qempty(sb, qb), ((ictr >> 1) & 1) ^ 1, ctl);
-      if (!ok) break;
-      if (lane == 0) {
-        const uint32_t qbar = bar_qfull(sb, qb);
-        ptx::mbar_arrive_expect_tx(qbar, (uint32_t)rows * (4096u + 256u));
-        ptx::bulk_g2s(sb + OFF_QPAY + qb * kQPayBytes, p.q_payload + (int64_t)r0 * 4096, rows * 4096u, qbar);
-        ptx::bulk_g2s(sb + OFF_QSC + qb * kQScBytes, p.q_scale + (int64_t)r0 * 256, rows * 256u, qbar);
-        if (!seq_ok) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
+      if (pw == 0) {
+        ok = wait_lane0(bar_qempty(sb, qb), ((ictr >> 1) & 1) ^ 1, ctl);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t qbar = bar_qfull(sb, qb);
+          ptx::mbar_arrive_expect_tx(qbar, (uint32_t)rows * (4096u + 256u));
+          ptx::bulk_g2s(sb + OFF_QPAY + qb * kQPayBytes, p.q_payload + (int64_t)r0 * 4096, rows * 4096u, qbar);
+          ptx::bulk_g2s(sb + OFF_QSC + qb * kQScBytes, p.q_scale + (int64_t)r0 * 256, rows * 256u, qbar);
+          if (!seq_ok) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
+        }
       }
       const int32_t* pt = p.page_table + (int64_t)(seq_ok ? seq : 0) * p.max_pages;
       // lane l holds the physical page of logical page 2*chunk + l (16 tiles per chunk);
@@ -243,12 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       int32_t chunk = t0;
       int32_t pid_cur = fetch(chunk);
       int32_t pid_next = fetch(chunk + 16);
-      for (int32_t i = t0; i < t1; i += kTilesPerStage) {
+      for (int32_t i = t0; i < t1; i += kTilesPerStage, kctr++) {
         if (i - chunk >= 16) {
           chunk += 16;
           pid_cur = pid_next;
           pid_next = fetch(chunk + 16);
         }
+        if ((int)(kctr % kProducers) != pw) continue;
         const int s = kctr % kStages;
         ok = wait_lane0(bar_kempty(sb, s), ((kctr / kStages) & 1) ^ 1, ctl);
         if (!ok) break;
@@ -276,24 +310,27 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           gather4(sb + OFF_KSC + s * kKScBytes, &sc_map, q0, q1, q2, q3, kbar);
         }
         __syncwarp();
-        kctr++;
       }
-      ictr++;
+      ictr++;  // also after a failed stage wait: this item's query copies were issued
     }
-    // Tail: every copy issued must land, and (when not aborting) every stage must be
-    // released by the MMAs that read it, before the CTA may exit.
+    // Tail: every copy a warp issued must land, and (when not aborting) every stage must
+    // be released by the MMAs that read it, before the CTA may exit.  kctr stops at the
+    // stage a failed wait was for, which this warp did not issue.
     for (uint32_t u = (kctr > (uint32_t)kStages ? kctr - kStages : 0); u < kctr; u++) {
+      if ((int)(u % kProducers) != pw) continue;
       wait_lane0(bar_kfull(sb, u % kStages), (u / kStages) & 1, ctl, false);
       if (!*abort_flag) wait_lane0(bar_kempty(sb, u % kStages), (u / kStages) & 1, ctl);
     }
-    for (uint32_t u = (ictr > 2u ? ictr - 2 : 0); u < ictr; u++) {
-      wait_lane0(bar_qfull(sb, u & 1), (u >> 1) & 1, ctl, false);
-      if (!*abort_flag) wait_lane0(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
+    if (pw == 0) {
+      for (uint32_t u = (ictr > 2u ? ictr - 2 : 0); u < ictr; u++) {
+        wait_lane0(bar_qfull(sb, u & 1), (u >> 1) & 1, ctl, false);
+        if (!*abort_flag) wait_lane0(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
+      }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
-      uint32_t kctr = 0, ictr = 0, sctr = 0;
+      uint32_t kctr = 0, ictr = 0, ucnt = 0;
       bool ok = true;
       constexpr uint32_t kIdesc0 = ptx::idesc_mxf4(64, 0, 0);
       constexpr uint32_t kIdesc1 = ptx::idesc_mxf4(64, 2, 2);
@@ -307,13 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
         for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
           const int s = kctr % kStages;
           const int tiles = stage_tiles(i, t1);
-          // the stage's tiles landed and their scale atoms are in tensor memory
-          ok = poll(bar_sfready(sb, s), (kctr / kStages) & 1, ctl, true);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          for (int r = 0; r < rows; r++) {
-            const int slot = sctr % kSlots;
-            ok = poll(bar_accempty(sb, slot), ((sctr / kSlots) & 1) ^ 1, ctl, true);
+          // the stage's tiles landed with their scales in tensor memory (every scale
+          // writer done with this use of the buffer), and each row's accumulator slot
+          // is free (every epilogue warp released its previous use)
+          const uint32_t need_sf = (uint32_t)kScaleWarps * (kctr / kStages + 1);
+          for (int r = 0; r < rows; r++, ucnt++) {
+            const int slot = ucnt % kAccSlots;
+            ok = wait_counts(cnt_sf(sb, s), need_sf, cnt_slot(sb, slot), (uint32_t)kEpiWarps * (ucnt / kAccSlots),
+                             ctl);
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t b0 = sb + OFF_QPAY + qb * kQPayBytes + r * 4096;
@@ -327,7 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
                             sfa, sfbt, 1);
             }
             ptx::mma_commit(bar_accfull(sb, slot));
-            sctr++;
           }
           if (!ok) break;
           ptx::mma_commit(bar_kempty(sb, s));
@@ -338,8 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
         ictr++;
       }
     }
-  } else if (warp == kWarpSf) {
-    // ------------------------------------------------------------ scale transposer
+  } else if (warp < kScaleWarps) {
+    // ------------------------------------------------------------ scale writers
+    const int qd = warp;  // TMEM lane group: tile rows 32*qd .. 32*qd + 31
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     uint32_t kctr = 0, ictr = 0;
     bool ok = true;
     while (ok && items.next(g, t0, t1)) {
@@ -348,47 +387,33 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       ok = wait_warp(bar_qfull(sb, qb), (ictr >> 1) & 1, ctl);
       if (!ok) break;
       for (int r = 0; r < rows; r++) {
-        // query rows: B operand of 64 heads; atom row r0 holds heads r0 and 32 + r0
-        const uint8_t* src = smem + OFF_QSC + qb * kQScBytes + r * 256;  // [c][64 heads]
-        uint4 v;
-        v.x = pack4(src[lane], src[64 + lane], src[128 + lane], src[192 + lane]);
-        v.y = pack4(src[32 + lane], src[96 + lane], src[160 + lane], src[224 + lane]);
-        v.z = 0u;
-        v.w = 0u;
-        *reinterpret_cast<uint4*>(smem + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes + lane * 16) = v;
+        // query row r: B operand of 64 heads, the same in every lane group; lane l holds
+        // heads l and 32 + l in the row's first two scale columns
+        const uint8_t* src = smem + OFF_QSC + qb * kQScBytes + r * 256 + lane;  // [c][64 heads]
+        const uint32_t w0 = pack4(src[0], src[64], src[128], src[192]);
+        const uint32_t w1 = pack4(src[32], src[96], src[160], src[224]);
+        ptx::tmem_st4(tmem + lane_base + kColSfb + (qb * kGroupMax + r) * 4, w0, w1, 0u, 0u);
       }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        for (int r = 0; r < rows; r++)
-          ptx::tmem_cp_sf_atom(tmem + kColSfb + (qb * kGroupMax + r) * 4,
-                               sb + OFF_QATOM + (qb * kGroupMax + r) * kAtomBytes);
-        ptx::mma_commit(bar_qsf(sb, qb));  // arrives once the copies have completed
-      }
+      if (lane == 0) ptx::mbar_arrive(bar_qsf(sb, qb));
       for (int32_t i = t0; i < t1; i += kTilesPerStage) {
         const int s = kctr % kStages;
         const int tiles = stage_tiles(i, t1);
         ok = wait_warp(bar_kfull(sb, s), (kctr / kStages) & 1, ctl);
         if (!ok) break;
         for (int a = 0; a < tiles; a++) {
-          // tile a: A operand of 128 tokens, token m = 64*page + j; atom row r0 holds tokens
-          // r0, 32 + r0 (first page) and 64 + r0, 96 + r0 (second page)
-          const uint8_t* src = smem + OFF_KSC + s * kKScBytes + a * 512;  // [page][c][64]
-          uint4 v;
-          v.x = pack4(src[lane], src[64 + lane], src[128 + lane], src[192 + lane]);
-          v.y = pack4(src[32 + lane], src[96 + lane], src[160 + lane], src[224 + lane]);
-          v.z = pack4(src[256 + lane], src[320 + lane], src[384 + lane], src[448 + lane]);
-          v.w = pack4(src[288 + lane], src[352 + lane], src[416 + lane], src[480 + lane]);
-          *reinterpret_cast<uint4*>(smem + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes + lane * 16) = v;
+          // tile a: token m = 32*qd + lane is token 32*(qd & 1) + lane of page 2a + qd/2
+          const uint8_t* src = smem + OFF_KSC + s * kKScBytes + (2 * a + (qd >> 1)) * 256 + (qd & 1) * 32 + lane;
+          const uint32_t wv = pack4(src[0], src[64], src[128], src[192]);
+          ptx::tmem_st4(tmem + lane_base + kColSfa + (s * kTilesPerStage + a) * 4, qd == 0 ? wv : 0u,
+                        qd == 1 ? wv : 0u, qd == 2 ? wv : 0u, qd == 3 ? wv : 0u);
         }
-        ptx::fence_proxy_async_smem();
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          for (int a = 0; a < tiles; a++)
-            ptx::tmem_cp_sf_atom(tmem + kColSfa + (s * kTilesPerStage + a) * 4,
-                                 sb + OFF_KATOM + (s * kTilesPerStage + a) * kAtomBytes);
-          ptx::mma_commit(bar_sfready(sb, s));  // arrives once the copies have completed
-        }
+        if (lane == 0) ptx::smem_add_release(cnt_sf(sb, s), 1u);
         kctr++;
       }
       ictr++;
@@ -396,11 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - kWarpEpi0;  // 0..7: private copy of the group's lengths
-    const int half = ew >> 2;         // takes slots with sctr % 2 == half
+    const int half = ew >> 2;         // reads tile `half` of every slot use
     const int quad = warp & 3;        // TMEM lanes this warp may read
     const int m = quad * 32 + lane;   // token row of a tile
     int32_t* lsm = reinterpret_cast<int32_t*>(smem + OFF_LEN) + ew * kGroupMax;
-    uint32_t sctr = 0;
+    uint32_t ucnt = 0;
     bool ok = true;
     while (ok && items.next(g, t0, t1)) {
       const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
@@ -416,23 +441,25 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       __syncwarp();
       for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
         const int tiles = stage_tiles(i, t1);
-        for (int r = 0; r < rows; r++, sctr++) {
-          if ((int)(sctr & 1) != half) continue;
-          const int slot = sctr % kSlots;
-          ok = wait_warp(bar_accfull(sb, slot), (sctr / kSlots) & 1, ctl);
-          if (!ok) break;
-          ptx::tc_fence_after();
+        for (int r = 0; r < rows && ok; r++) {
           const float* wr = p.w + (int64_t)(r0 + r) * 64;  // same address in every lane: L1 broadcast
           const int32_t L = lsm[r];
           float* orow = p.out + (int64_t)(r0 + r) * p.out_stride;
-          for (int a = 0; a < tiles; a++) {
+          {
+            const int a = half;
+            const int slot = ucnt % kAccSlots;
+            ok = wait_warp(bar_accfull(sb, slot), (ucnt / kAccSlots) & 1, ctl);
+            ucnt++;
+            if (!ok) break;
+            ptx::tc_fence_after();
             float d[64];
-            ptx::tmem_ld64_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + slot * 128 + a * 64, d);
-            if (a == tiles - 1) {
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(bar_accempty(sb, slot));
-            }
+            if (a < tiles) ptx::tmem_ld64_sync(tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + slot * 128 + a * 64, d);
+            // released as soon as read (also by a warp with no tile here: every epilogue
+            // warp arrives once per use)
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::smem_add_release(cnt_slot(sb, slot), 1u);
+            if (a >= tiles) continue;
             const int32_t tok = (i + a) * kTileTokens + m;
             if (tok < L) {
               float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;

@@ -6,37 +6,44 @@
 // context length 0 (their selection is empty: all -1).
 //
 // Selection = the k largest logits of a row, ties at the k-th value to the lower
-// positions, emitted in ascending position order.  Two launches:
-//   filter (one CTA per row and 4,096-token chunk): every CTA of a row takes the same
-//     fixed sample of 1,024 logits and derives the same conservative threshold bucket
-//     (a linear 256-bucket histogram of the sample, cut about four standard deviations
-//     beyond the expected position of the k-th largest), then writes the positions of
-//     its chunk's logits at or above it, in order, into the chunk's own region of a
-//     candidate buffer: no cross-CTA synchronisation;
-//   select (one CTA per row): concatenates the chunk regions in order, gathers the
-//     candidates' logits, finds the key of the k-th largest by radix select (11 + 11 + 10
-//     bits) and emits the keys above it and the lowest-positioned keys equal to it.
-// The sample decides speed, never the result: when fewer than k or more than kCapB
-// logits pass, the select launch runs the exact path over the whole row (2048 buckets
-// linear in value between the row's min and max, a refinement of a crowded bucket over
-// its own range, the bucket's candidates ranked exactly, radix select when a bucket is
-// all ties).
+// positions, emitted in ascending position order.  One launch, grid (rows, chunks of
+// 4,096 tokens):
+//   every CTA of a row takes the same fixed sample of 1,024 of the row's logits and
+//     derives the same conservative threshold (a linear 256-bucket histogram of the
+//     sample, cut about four standard deviations beyond the expected place of the k-th
+//     largest), then writes the keys and positions of its chunk's logits at or above it,
+//     in order, into the chunk's own region of a candidate buffer;
+//   the last CTA of the row to finish (a fence, then an arrival counter; nobody waits)
+//     concatenates the regions in order, buckets the candidates linearly between their
+//     min and max, ranks the boundary bucket's members exactly and emits the keys above
+//     the k-th and the lowest-positioned ones equal to it.
+// The threshold is superset-closed (a value that passes lets every larger one pass), so
+// with at least k candidates the candidates hold the whole answer.  The sample decides
+// speed, never the result: with fewer than k or more than kCapB candidates the last CTA
+// runs the exact path over the whole row (2048 linear buckets between the row's min and
+// max, a refinement of a crowded bucket over its own range, the bucket ranked exactly,
+// radix select when a bucket is all ties).
 #include "fp4idx_internal.cuh"
+
+#include <atomic>
 
 namespace fp4idx {
 namespace {
 
-constexpr int kThreads = 512;          // select launch
-constexpr int kFilterThreads = 256;    // filter launch
-constexpr int kChunk = 4096;           // tokens per filter CTA (16 per thread)
-constexpr int kCapB = 8192;            // candidates the select launch keeps in shared memory
-constexpr int kMaxChunks = (FP4IDX_MAX_CONTEXT + kChunk - 1) / kChunk;
+
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 4096;                  // tokens per CTA: 8 per thread
+constexpr int kPer = kChunk / kThreads;
+constexpr int kCapB = 8192;                   // candidates the selecting CTA holds in shared memory
+constexpr int kMaxChunks = (FP4IDX_MAX_CONTEXT + kChunk - 1) / kChunk;
 constexpr int kBins = 2048;
 constexpr int kBinsPerThread = kBins / kThreads;
-constexpr int kGather = 1024;
-constexpr int kSample = 1024;    // sample for the filter threshold
+constexpr int kGather = 1024;                 // largest boundary bucket ranked by direct counting
+constexpr int kSample = 1024;                 // logits per row behind the candidate threshold
 constexpr int kSampleBins = 256;
+constexpr size_t kDynSmem = kCapB * (sizeof(uint32_t) + sizeof(uint16_t));
+static_assert(kSampleBins <= kThreads && kMaxChunks <= 32 && kSample % kThreads == 0, "layout");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Order-preserving key; -0 maps to +0 so that equal values are equal keys.
@@ -201,215 +208,75 @@ __device__ int emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int
   return total;
 }
 
-
-// Exclusive scan over a block of NT threads (any multiple of 32 up to 1024).
-template <int NT>
-__device__ __forceinline__ int scan_nt(int v, int* scratch, int& total) {
-  constexpr int W = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += n;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < W ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += n;
-    }
-    if (lane < W) scratch[lane] = w;
-  }
-  __syncthreads();
-  const int before = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
-  total = scratch[W - 1];
-  __syncthreads();
-  return before;
-}
-
-template <int NT, bool kMax>
-__device__ __forceinline__ uint32_t reduce_nt(uint32_t v, uint32_t* scratch) {
-  constexpr int W = NT / 32;
+// Block-wide min and max of uint32 keys in one barrier round; scratch holds 2 * kWarps.
+__device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, uint32_t* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const uint32_t n = __shfl_xor_sync(kFull, v, o);
-    v = kMax ? max(v, n) : min(v, n);
+    mn = min(mn, __shfl_xor_sync(kFull, mn, o));
+    mx = max(mx, __shfl_xor_sync(kFull, mx, o));
   }
-  if (lane == 0) scratch[warp] = v;
+  if (lane == 0) {
+    scratch[warp] = mn;
+    scratch[kWarps + warp] = mx;
+  }
   __syncthreads();
-  uint32_t r = scratch[0];
-  for (int i = 1; i < W; i++) r = kMax ? max(r, scratch[i]) : min(r, scratch[i]);
+  mn = scratch[0];
+  mx = scratch[kWarps];
+#pragma unroll
+  for (int i = 1; i < kWarps; i++) {
+    mn = min(mn, scratch[i]);
+    mx = max(mx, scratch[kWarps + i]);
+  }
   __syncthreads();
-  return r;
 }
 
-// ------------------------------------------------------------------ filter launch
-// grid (chunks, rows).  Writes cnt[row][c] and the chunk's candidate positions, in order,
-// at cand[row][c * kChunk ...].
-__global__ void __launch_bounds__(kFilterThreads) topk_filter_kernel(const float* __restrict__ logits,
-                                                                     int64_t stride,
-                                                                     const int32_t* __restrict__ context_lens,
-                                                                     int32_t max_context, int32_t k,
-                                                                     int32_t* __restrict__ cand, int64_t cstride,
-                                                                     int32_t* __restrict__ cnt, int32_t nch) {
-  constexpr int NT = kFilterThreads;
-  constexpr int kPer = kChunk / NT;  // 16 consecutive tokens per thread
-  __shared__ int hist[kSampleBins];
-  __shared__ int scratch[NT / 32];
-  __shared__ uint32_t uscratch[NT / 32];
-  __shared__ int sh_blo;
-  const int64_t row = blockIdx.y;
-  const int c = blockIdx.x;
+struct Shared {
+  int hist[kBins];
+  uint32_t gkey[kGather];
+  int gidx[kGather];
+  int scratch[kWarps];
+  uint32_t uscratch[2 * kWarps];
+  int coff[kMaxChunks + 1];
+  int bin, rem, gcount, take, blo, last;
+  uint32_t key;
+};
+
+// Members of the boundary bucket (nb <= kGather of them, keys from key_of) ranked by
+// direct counting: sets sh.key to the rem-th largest and sh.take to how many keys equal
+// to it the selection takes.  `in_bucket(i)` says whether element i is a member.
+template <class KeyFn, class InFn>
+__device__ void rank_bucket(int n, KeyFn key_of, InFn in_bucket, int nb, int rem, Shared& sh) {
   const int tid = threadIdx.x;
-  int32_t L = __ldg(context_lens + row);
-  L = L < 0 ? 0 : (L > max_context ? max_context : L);
-  const int c0 = c * kChunk;
-  if (L <= k || c0 >= L) {
-    if (tid == 0) cnt[row * nch + c] = 0;
-    return;
-  }
-  const float* lg = logits + row * stride;
-  // the row's fixed sample: positions floor(i * L / kSample)
-  uint32_t sk[kSample / NT];
-  uint32_t smin = 0xFFFFFFFFu, smax = 0u;
-#pragma unroll
-  for (int j = 0; j < kSample / NT; j++) {
-    const int i = j * NT + tid;
-    sk[j] = order_key(__ldg(lg + (int)(((int64_t)i * L) / kSample)));
-    smin = min(smin, sk[j]);
-    smax = max(smax, sk[j]);
-  }
-  // this thread's 16 tokens (issued now, used after the threshold is known)
-  float x[kPer];
-  const int t0 = c0 + tid * kPer;
-  const bool vec = ((reinterpret_cast<uintptr_t>(lg + t0) & 15) == 0) && t0 + kPer <= L;
-  if (vec) {
-#pragma unroll
-    for (int q = 0; q < kPer / 4; q++) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(lg + t0) + q);
-      x[4 * q] = v.x;
-      x[4 * q + 1] = v.y;
-      x[4 * q + 2] = v.z;
-      x[4 * q + 3] = v.w;
+  for (int i = tid; i < n; i += kThreads) {
+    if (in_bucket(i)) {
+      const int slot = atomicAdd(&sh.gcount, 1);
+      sh.gkey[slot] = key_of(i);
+      sh.gidx[slot] = i;
     }
-  } else {
-#pragma unroll
-    for (int q = 0; q < kPer; q++) x[q] = t0 + q < L ? __ldg(lg + t0 + q) : 0.f;
   }
-  for (int b = tid; b < kSampleBins; b += NT) hist[b] = 0;
-  smin = reduce_nt<NT, false>(smin, uscratch);
-  smax = reduce_nt<NT, true>(smax, uscratch);
-  const float lo = key_value(smin);
-  const float sc = lin_scale(lo, key_value(smax)) * ((float)kSampleBins / (float)kBins);
-  auto bucket = [&](float v) -> int {
-    const int b = lin_bucket(v, lo, sc);
-    return b >= kSampleBins ? kSampleBins - 1 : b;
-  };
-#pragma unroll
-  for (int j = 0; j < kSample / NT; j++) atomicAdd(&hist[bucket(key_value(sk[j]))], 1);
   __syncthreads();
-  // keep the expected share of k in the sample plus four standard deviations
-  const float q = (float)k / (float)L;
-  const float mean = q * (float)kSample;
-  const int need = min(kSample, (int)ceilf(mean + 4.0f * sqrtf(mean * (1.0f - q)) + 8.0f));
-  const int mine = hist[kSampleBins - 1 - tid];  // NT == kSampleBins
-  int tot;
-  const int above = scan_nt<NT>(mine, scratch, tot);
-  if (above < need && need <= above + mine) sh_blo = kSampleBins - 1 - tid;
-  __syncthreads();
-  const int blo = sh_blo;
-  // order-preserving compaction of this chunk's passing tokens
-  unsigned flags = 0;
-  int nmine = 0;
-#pragma unroll
-  for (int qq = 0; qq < kPer; qq++) {
-    const bool in = t0 + qq < L && bucket(x[qq]) >= blo;
-    flags |= (unsigned)in << qq;
-    nmine += in;
+  for (int i = tid; i < nb; i += kThreads) {
+    const uint32_t ki = sh.gkey[i];
+    const int ii = sh.gidx[i];
+    int rk = 0, gt = 0;
+    for (int j = 0; j < nb; j++) {
+      const uint32_t kj = sh.gkey[j];
+      gt += kj > ki;
+      rk += (kj > ki) || (kj == ki && sh.gidx[j] < ii);
+    }
+    if (rk == rem - 1) {
+      sh.key = ki;
+      sh.take = rem - gt;
+    }
   }
-  int total;
-  int w = scan_nt<NT>(nmine, scratch, total);
-  int32_t* dst = cand + row * cstride + c0;
-#pragma unroll
-  for (int qq = 0; qq < kPer; qq++)
-    if (flags & (1u << qq)) dst[w++] = t0 + qq;
-  if (tid == 0) cnt[row * nch + c] = total;
+  __syncthreads();
 }
 
-// ------------------------------------------------------------------ select launch
-__global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* __restrict__ logits, int64_t stride,
-                                                                  const int32_t* __restrict__ context_lens,
-                                                                  int32_t max_context, int32_t k,
-                                                                  const int32_t* __restrict__ cand, int64_t cstride,
-                                                                  const int32_t* __restrict__ cnt, int32_t nch,
-                                                                  int32_t* __restrict__ out, int32_t* status) {
-  extern __shared__ __align__(16) uint32_t dyn[];  // ckey[kCapB], then cpos[kCapB]
-  __shared__ int hist[kBins];
-  __shared__ uint32_t gkey[kGather];
-  __shared__ int gidx[kGather];
-  __shared__ int scratch[kWarps];
-  __shared__ uint32_t uscratch[kWarps];
-  __shared__ int coff[kMaxChunks + 1];
-  __shared__ int sh_bin, sh_rem, sh_gcount;
-  __shared__ uint32_t sh_key;
-  __shared__ int sh_take;
-  uint32_t* ckey = dyn;
-  int* cpos = reinterpret_cast<int*>(dyn + kCapB);
-
-  const int64_t row = blockIdx.x;
+// Exact selection over the whole row, read from global memory: the path for rows whose
+// candidate set came out too small or too large.
+__device__ void select_whole_row(const float* lg, int L, int k, int32_t* o, Shared& sh) {
   const int tid = threadIdx.x;
-  int32_t L = __ldg(context_lens + row);
-  if (L < 0 || L > max_context) {
-    if (tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
-    L = L < 0 ? 0 : max_context;
-  }
-  int32_t* o = out + row * k;
-  if (L <= k) {
-    for (int i = tid; i < k; i += kThreads) o[i] = i < L ? i : -1;
-    return;
-  }
-  const float* lg = logits + row * stride;
-  if (tid < 32) {  // chunk offsets into the concatenated candidate list
-    int run = 0;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int c = c0 + tid;
-      int v = c < nch ? __ldg(cnt + row * nch + c) : 0;
-      int x = v;
-#pragma unroll
-      for (int o2 = 1; o2 < 32; o2 <<= 1) {
-        const int n = __shfl_up_sync(kFull, x, o2);
-        if (tid >= o2) x += n;
-      }
-      if (c < nch) coff[c] = run + x - v;
-      run += __shfl_sync(kFull, x, 31);
-    }
-    if (tid == 0) coff[nch] = run;
-  }
-  __syncthreads();
-  const int m = coff[nch];
-  if (m >= k && m <= kCapB) {
-    // gather the candidates (positions in order, and their keys)
-    for (int i = tid; i < m; i += kThreads) {
-      int c = 0;
-      while (coff[c + 1] <= i) c++;
-      const int pos = __ldg(cand + row * cstride + (int64_t)c * kChunk + (i - coff[c]));
-      cpos[i] = pos;
-      ckey[i] = order_key(__ldg(lg + pos));
-    }
-    __syncthreads();
-    auto ck = [&](int i) -> uint32_t { return ckey[i]; };
-    radix_select(m, ck, [](int) { return true; }, k, hist, scratch, &sh_bin, &sh_rem, &sh_key, &sh_take);
-    const int got = emit_ordered(m, ck, [&](int i) { return cpos[i]; }, sh_key, sh_take, o, k, scratch);
-    for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
-    return;
-  }
-
-  // ---- exact path over the whole row, read from global memory (L2)
   auto key_at = [&](int s) -> uint32_t { return order_key(__ldg(lg + s)); };
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   for (int s = tid; s < L; s += kThreads) {
@@ -417,18 +284,16 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
     kmin = min(kmin, u);
     kmax = max(kmax, u);
   }
-  kmin = block_reduce<false>(kmin, uscratch);
-  kmax = block_reduce<true>(kmax, uscratch);
+  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
+  if (tid == 0) sh.gcount = 0;
+  block_minmax(kmin, kmax, sh.uscratch);
   const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
-  for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-  if (tid == 0) sh_gcount = 0;
+  for (int s = tid; s < L; s += kThreads) atomicAdd(&sh.hist[lin_bucket(key_value(key_at(s)), lo1, sc1)], 1);
   __syncthreads();
-  for (int s = tid; s < L; s += kThreads) atomicAdd(&hist[lin_bucket(key_value(key_at(s)), lo1, sc1)], 1);
-  __syncthreads();
-  find_bin_from_top(hist, k, scratch, &sh_bin, &sh_rem);
-  const int b1 = sh_bin;
-  int rem = sh_rem;
-  int nb = hist[b1];
+  find_bin_from_top(sh.hist, k, sh.scratch, &sh.bin, &sh.rem);
+  const int b1 = sh.bin;
+  int rem = sh.rem;
+  int nb = sh.hist[b1];
   __syncthreads();  // every thread has read nb before any path clears the histogram
   float lo2 = 0.0f, sc2 = 0.0f;
   int b2 = -1;
@@ -441,94 +306,281 @@ __global__ void __launch_bounds__(kThreads, 2) topk_select_kernel(const float* _
         bmax = max(bmax, u);
       }
     }
-    bmin = block_reduce<false>(bmin, uscratch);
-    bmax = block_reduce<true>(bmax, uscratch);
+    for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
+    block_minmax(bmin, bmax, sh.uscratch);
     lo2 = key_value(bmin);
     sc2 = lin_scale(lo2, key_value(bmax));
-    for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-    __syncthreads();
     for (int s = tid; s < L; s += kThreads) {
       const float x = key_value(key_at(s));
-      if (lin_bucket(x, lo1, sc1) == b1) atomicAdd(&hist[lin_bucket(x, lo2, sc2)], 1);
+      if (lin_bucket(x, lo1, sc1) == b1) atomicAdd(&sh.hist[lin_bucket(x, lo2, sc2)], 1);
     }
     __syncthreads();
-    find_bin_from_top(hist, rem, scratch, &sh_bin, &sh_rem);
-    b2 = sh_bin;
-    rem = sh_rem;
-    nb = hist[b2];
+    find_bin_from_top(sh.hist, rem, sh.scratch, &sh.bin, &sh.rem);
+    b2 = sh.bin;
+    rem = sh.rem;
+    nb = sh.hist[b2];
     __syncthreads();
   }
-  auto in_bucket = [&](uint32_t u) -> bool {
-    const float x = key_value(u);
+  auto in_bucket = [&](int s) -> bool {
+    const float x = key_value(key_at(s));
     return lin_bucket(x, lo1, sc1) == b1 && (b2 < 0 || lin_bucket(x, lo2, sc2) == b2);
   };
   if (nb <= kGather) {
-    for (int s = tid; s < L; s += kThreads) {
-      const uint32_t u = key_at(s);
-      if (in_bucket(u)) {
-        const int slot = atomicAdd(&sh_gcount, 1);
-        gkey[slot] = u;
-        gidx[slot] = s;
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < nb; i += kThreads) {
-      const uint32_t ki = gkey[i];
-      const int ii = gidx[i];
-      int rk = 0;
-      for (int j = 0; j < nb; j++) {
-        const uint32_t kj = gkey[j];
-        rk += (kj > ki) || (kj == ki && gidx[j] < ii);
-      }
-      if (rk == rem - 1) {
-        int gt = 0;
-        for (int j = 0; j < nb; j++) gt += gkey[j] > ki;
-        sh_key = ki;
-        sh_take = rem - gt;
-      }
-    }
-    __syncthreads();
+    rank_bucket(L, key_at, in_bucket, nb, rem, sh);
   } else {
-    radix_select(L, key_at, [&](int s) { return in_bucket(key_at(s)); }, rem, hist, scratch, &sh_bin, &sh_rem,
-                 &sh_key, &sh_take);
+    radix_select(L, key_at, in_bucket, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
   }
-  const int got = emit_ordered(L, key_at, [](int s) { return s; }, sh_key, sh_take, o, k, scratch);
+  const int got = emit_ordered(L, key_at, [](int s) { return s; }, sh.key, sh.take, o, k, sh.scratch);
+  for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
+}
+
+// grid (rows, chunks).  Candidate regions: cand_key/cand_pos[row * cstride + chunk * kChunk
+// ...], counts cnt[row * nch + chunk], arrival counters arrivals[row] (zero at launch).
+__global__ void __launch_bounds__(kThreads, 3) topk_kernel(const float* __restrict__ logits, int64_t stride,
+                                                        const int32_t* __restrict__ context_lens, int32_t max_context,
+                                                        int32_t k, uint32_t* cand_key, uint16_t* cand_pos,
+                                                        int64_t cstride, int32_t* cnt, int32_t nch,
+                                                        unsigned int* arrivals, int32_t* __restrict__ out,
+                                                        int32_t* status) {
+  extern __shared__ __align__(16) uint32_t dyn[];  // ckey[kCapB], then cpos[kCapB] (uint16)
+  __shared__ Shared sh;
+  const int64_t row = blockIdx.x;
+  const int c = blockIdx.y;
+  const int tid = threadIdx.x;
+  int32_t L = __ldg(context_lens + row);
+  if (L < 0 || L > max_context) {
+    if (c == 0 && tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
+    L = L < 0 ? 0 : max_context;
+  }
+  int32_t* o = out + row * k;
+  if (L <= k) {
+    if (c == 0)
+      for (int i = tid; i < k; i += kThreads) o[i] = i < L ? i : -1;
+    return;
+  }
+  const int c0 = c * kChunk;
+  if (c0 >= L) return;
+  const int nrow = (L + kChunk - 1) / kChunk;  // CTAs of this row that take part
+  const float* lg = logits + row * stride;
+
+  // ---- the row's fixed sample and this CTA's tokens.  The sample is 128 runs of 8
+  // adjacent logits starting at floor(r * L / 128) rounded down to 8 (two float4 loads a
+  // run) when the row is 16-byte aligned and L >= 1024, else single logits at
+  // floor(i * L / 1024).
+  float sv[kSample / kThreads];
+  if ((reinterpret_cast<uintptr_t>(lg) & 15) == 0 && L >= kSample) {
+    static_assert(kSample / kThreads == 2 && kSample / 8 <= kThreads, "two sample logits a thread");
+    const int run = tid >> 2, part = tid & 3;  // 128 runs x 4 threads; a thread takes 2 logits
+    const int p0 = ((int)(((int64_t)run * L) / (kSample / 8)) & ~7) + 2 * part;
+    const float2 v = __ldg(reinterpret_cast<const float2*>(lg + p0));
+    sv[0] = v.x;
+    sv[1] = v.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < kSample / kThreads; j++)
+      sv[j] = __ldg(lg + (int)(((int64_t)(j * kThreads + tid) * L) / kSample));
+  }
+  float x[kPer];
+  const int t0 = c0 + tid * kPer;
+  if (((reinterpret_cast<uintptr_t>(lg + t0) & 15) == 0) && t0 + kPer <= L) {
+#pragma unroll
+    for (int q = 0; q < kPer / 4; q++) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(lg + t0) + q);
+      x[4 * q] = v.x;
+      x[4 * q + 1] = v.y;
+      x[4 * q + 2] = v.z;
+      x[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < kPer; q++) x[q] = t0 + q < L ? __ldg(lg + t0 + q) : 0.0f;
+  }
+  if (tid < kSampleBins) sh.hist[tid] = 0;
+  uint32_t smin = 0xFFFFFFFFu, smax = 0u;
+#pragma unroll
+  for (int j = 0; j < kSample / kThreads; j++) {
+    smin = min(smin, order_key(sv[j]));
+    smax = max(smax, order_key(sv[j]));
+  }
+  block_minmax(smin, smax, sh.uscratch);  // its barrier also orders the histogram clear
+  const float lo = key_value(smin);
+  const float sc = lin_scale(lo, key_value(smax)) * ((float)kSampleBins / (float)kBins);
+  auto sbucket = [&](float v) -> int {
+    const int b = lin_bucket(v, lo, sc);
+    return b >= kSampleBins ? kSampleBins - 1 : b;
+  };
+#pragma unroll
+  for (int j = 0; j < kSample / kThreads; j++) atomicAdd(&sh.hist[sbucket(sv[j])], 1);
+  __syncthreads();
+  // threshold bucket: keep the sample's expected share of k plus four standard deviations
+  const float q = (float)k / (float)L;
+  const float mean = q * (float)kSample;
+  const int need = min(kSample, (int)ceilf(mean + 4.0f * sqrtf(mean * (1.0f - q)) + 8.0f));
+  const int mine = tid < kSampleBins ? sh.hist[kSampleBins - 1 - tid] : 0;
+  int tot;
+  const int above = block_excl_scan(mine, sh.scratch, tot);
+  if (tid < kSampleBins && above < need && need <= above + mine) sh.blo = kSampleBins - 1 - tid;
+  __syncthreads();
+  const int blo = sh.blo;
+
+  // ---- order-preserving compaction of this chunk's candidates
+  unsigned flags = 0;
+  int nmine = 0;
+#pragma unroll
+  for (int qq = 0; qq < kPer; qq++) {
+    const bool in = t0 + qq < L && sbucket(x[qq]) >= blo;
+    flags |= (unsigned)in << qq;
+    nmine += in;
+  }
+  int total;
+  int w = block_excl_scan(nmine, sh.scratch, total);
+  const int64_t base = row * cstride + c0;
+#pragma unroll
+  for (int qq = 0; qq < kPer; qq++) {
+    if (flags & (1u << qq)) {
+      cand_key[base + w] = order_key(x[qq]);
+      cand_pos[base + w] = (uint16_t)(t0 + qq);  // positions < FP4IDX_MAX_CONTEXT = 65536
+      w++;
+    }
+  }
+  if (tid == 0) cnt[row * nch + c] = total;
+  // publish (block barrier, then one thread's device-scope fence: the release pattern of a
+  // grid barrier), then count arrivals: the row's last CTA to arrive selects
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const bool last = atomicAdd(arrivals + row, 1u) == (unsigned)(nrow - 1);
+    if (last) __threadfence();
+    sh.last = last;
+  }
+  __syncthreads();
+  if (!sh.last) return;
+
+  // ---- selection by the last CTA: concatenate the regions in chunk (= position) order
+  uint32_t* ckey = dyn;
+  uint16_t* cpos = reinterpret_cast<uint16_t*>(dyn + kCapB);
+  if (tid < 32) {
+    const int v = tid < nrow ? min(max(__ldcg(cnt + row * nch + tid), 0), kChunk) : 0;
+    int xs = v;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const int n = __shfl_up_sync(kFull, xs, o2);
+      if (tid >= o2) xs += n;
+    }
+    if (tid < nrow) sh.coff[tid] = xs - v;
+    if (tid == 31) sh.coff[nrow] = xs;
+  }
+  if (tid == 0) sh.gcount = 0;
+  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
+  __syncthreads();
+  const int m = sh.coff[nrow];
+  if (m < k || m > kCapB) {
+    select_whole_row(lg, L, k, o, sh);
+    return;
+  }
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  constexpr int kBatch = 8;  // loads a thread keeps in flight at once
+#pragma unroll 1
+  for (int i0 = 0; i0 < m; i0 += kBatch * kThreads) {
+    uint32_t kk[kBatch];
+    uint16_t pp[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; u++) {
+      const int i = i0 + u * kThreads + tid;
+      if (i < m) {
+        int lo = 0, hi = nrow;  // chunk of element i: coff[lo] <= i < coff[lo + 1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (sh.coff[mid] <= i) lo = mid; else hi = mid;
+        }
+        const int64_t gi = row * cstride + (int64_t)lo * kChunk + (i - sh.coff[lo]);
+        kk[u] = __ldcg(cand_key + gi);
+        pp[u] = __ldcg(cand_pos + gi);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; u++) {
+      const int i = i0 + u * kThreads + tid;
+      if (i < m) {
+        ckey[i] = kk[u];
+        cpos[i] = pp[u];
+        kmin = min(kmin, kk[u]);
+        kmax = max(kmax, kk[u]);
+      }
+    }
+  }
+  block_minmax(kmin, kmax, sh.uscratch);  // also publishes ckey/cpos
+  const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
+  for (int i = tid; i < m; i += kThreads) atomicAdd(&sh.hist[lin_bucket(key_value(ckey[i]), lo1, sc1)], 1);
+  __syncthreads();
+  find_bin_from_top(sh.hist, k, sh.scratch, &sh.bin, &sh.rem);
+  const int b1 = sh.bin, rem = sh.rem, nb = sh.hist[b1];
+  __syncthreads();  // every thread has read nb before the radix path clears the histogram
+  auto ck = [&](int i) -> uint32_t { return ckey[i]; };
+  auto in_b1 = [&](int i) -> bool { return lin_bucket(key_value(ckey[i]), lo1, sc1) == b1; };
+  if (nb <= kGather) {
+    rank_bucket(m, ck, in_b1, nb, rem, sh);
+  } else {
+    radix_select(m, ck, in_b1, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
+  }
+  const int got = emit_ordered(m, ck, [&](int i) { return (int)cpos[i]; }, sh.key, sh.take, o, k, sh.scratch);
   for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
 }
 
 inline int num_chunks(int32_t max_context) { return (max(max_context, 1) + kChunk - 1) / kChunk; }
-inline int64_t cand_stride(int32_t max_context) { return ((int64_t)max(max_context, 1) + 3) / 4 * 4; }
+inline int64_t cand_stride(int32_t max_context) { return ((int64_t)max(max_context, 1) + 7) / 8 * 8; }
+inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Workspace: [candidate keys u32][candidate positions u16][chunk counts i32][arrivals u32].
+struct Layout {
+  size_t pos, cnt, arr, total;
+};
+inline Layout layout(int64_t n_rows, int32_t max_context) {
+  const size_t cells = (size_t)n_rows * (size_t)cand_stride(max_context);
+  Layout l;
+  l.pos = align256(cells * sizeof(uint32_t));
+  l.cnt = l.pos + align256(cells * sizeof(uint16_t));
+  l.arr = l.cnt + align256((size_t)n_rows * (size_t)num_chunks(max_context) * sizeof(int32_t));
+  l.total = l.arr + align256((size_t)n_rows * sizeof(uint32_t));
+  return l;
+}
+
+__global__ void topk_clear_kernel(unsigned int* arrivals, int32_t n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) arrivals[i] = 0u;
+}
+
+std::atomic<bool> g_attr_done[64];
 
 }  // namespace
 
-size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context) {
-  const size_t c = (size_t)n_rows * (size_t)cand_stride(max_context) * sizeof(int32_t);
-  const size_t n = (size_t)n_rows * (size_t)num_chunks(max_context) * sizeof(int32_t);
-  return ((c + 15) & ~(size_t)15) + ((n + 15) & ~(size_t)15);
-}
+size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context) { return layout(n_rows, max_context).total; }
 
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,
                         cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(2 * kCapB * sizeof(uint32_t)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int nch = num_chunks(max_context);
-  const int64_t cst = cand_stride(max_context);
-  int32_t* cand = reinterpret_cast<int32_t*>(workspace);
-  const size_t cbytes = (((size_t)n_rows * (size_t)cst * sizeof(int32_t)) + 15) & ~(size_t)15;
-  int32_t* cnt = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(workspace) + cbytes);
-  topk_filter_kernel<<<dim3(nch, n_rows), kFilterThreads, 0, stream>>>(logits, stride, context_lens, max_context, k,
-                                                                       cand, cst, cnt, nch);
-  cudaError_t e = cudaGetLastError();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  topk_select_kernel<<<n_rows, kThreads, 2 * kCapB * sizeof(uint32_t), stream>>>(
-      logits, stride, context_lens, max_context, k, cand, cst, cnt, nch, out, status);
+  if (dev < 0 || dev >= 64 || !g_attr_done[dev].load()) {
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+    if (e != cudaSuccess) return e;
+    // both kernels keep the SM's largest shared-memory split: no reconfiguration between them
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_clear_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) g_attr_done[dev].store(true);
+  }
+  const Layout l = layout(n_rows, max_context);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  topk_clear_kernel<<<(n_rows + 255) / 256, 256, 0, stream>>>(reinterpret_cast<unsigned int*>(ws + l.arr), n_rows);
+  const int nch = num_chunks(max_context);
+  topk_kernel<<<dim3((unsigned)n_rows, (unsigned)nch), kThreads, kDynSmem, stream>>>(
+      logits, stride, context_lens, max_context, k, reinterpret_cast<uint32_t*>(ws),
+      reinterpret_cast<uint16_t*>(ws + l.pos), cand_stride(max_context), reinterpret_cast<int32_t*>(ws + l.cnt), nch,
+      reinterpret_cast<unsigned int*>(ws + l.arr), out, status);
   return cudaGetLastError();
 }
 

@@ -17,9 +17,10 @@
 // array's device address once (cudaGetSymbolAddress) and keeps it for later calls on the
 // same device; make that first call before any stream capture begins.
 //
-// Zero state: nothing in the array needs to start at zero.  The filter launch writes
-// every (row, chunk) candidate count before the select launch reads it, and candidate
-// positions are read only up to those counts.  So no call clears the array.
+// Zero state: the per-row arrival counters (the row's last CTA to arrive does the
+// selection) must be zero when the kernel starts, so every call clears them with
+// cudaMemsetAsync on its stream before the launch.  Candidate counts and lists are
+// written before they are read and need no clearing.
 //
 // Every call on a device uses the same array.  Calls whose kernels may overlap (on
 // streams with no ordering between them, or from host threads at once) race on it and

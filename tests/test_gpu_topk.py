@@ -86,3 +86,38 @@ def test_topk_small_and_max_k(k):
     got = run(rows, lens, k)
     for t, L in enumerate(lens):
         assert np.array_equal(got[t], expected(rows[t], L, k)), (k, t)
+
+
+@pytest.mark.parametrize("kind", ["normal", "dups"])
+def test_topk_chunk_boundaries(kind):
+    rng = np.random.default_rng(11)
+    lens = [2049, 4095, 4096, 4097, 8191, 8192, 8193, 12289, 65535]
+    rows = [_dist(rng, kind, L) for L in lens]
+    got = run(rows, lens, 2048, stride=65536 + 1)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, 2048)), (kind, t, L)
+
+
+def _sample_positions(L, n=1024):
+    return (np.arange(n, dtype=np.int64) * L) // n
+
+
+def test_topk_rows_that_mislead_the_sample():
+    """The candidate threshold comes from a fixed strided sample of each row.  Rows built
+    so that the sample overstates it (too few candidates) or understates it (too many)
+    must still come out exact."""
+    rng = np.random.default_rng(12)
+    lens = [32768, 20000, 32768, 9000]
+    rows = []
+    for i, L in enumerate(lens):
+        sp = _sample_positions(L)
+        if i % 2 == 0:  # sample spread over [0, 100], every other logit in [0, 1)
+            x = rng.random(L).astype(np.float32)
+            x[sp] = np.linspace(0, 100, sp.size, dtype=np.float32)
+        else:  # sample spread over [0, 1], every other logit just below its top
+            x = (0.99 + 0.001 * rng.random(L)).astype(np.float32)
+            x[sp] = np.linspace(0, 1, sp.size, dtype=np.float32)
+        rows.append(x)
+    got = run(rows, lens, 2048)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, 2048)), t

@@ -81,9 +81,11 @@ def test_noalloc_matches_workspace_topk_on_two_calls_in_a_row():
 def test_noalloc_limit():
     from sparse_attention_fp4_gb300 import fp4idx
     Lmax, k = 65536, 2048
-    fits, too_many = 63, 64
-    assert fp4idx.topk_workspace_bytes(fits, Lmax) <= fp4idx.TOPK_NOALLOC_MAX_BYTES
-    assert fp4idx.topk_workspace_bytes(too_many, Lmax) > fp4idx.TOPK_NOALLOC_MAX_BYTES
+    fits = 1
+    while fp4idx.topk_workspace_bytes(fits + 1, Lmax) <= fp4idx.TOPK_NOALLOC_MAX_BYTES:
+        fits += 1
+    too_many = fits + 1
+    assert fits >= 16
     rng = np.random.default_rng(78)
     lens = [int(v) for v in rng.integers(Lmax // 2, Lmax + 1, size=too_many)]
     lens[0] = Lmax
