@@ -5,16 +5,16 @@
 // guarded page table; the logits are
 //   logits[t,s] = sum_h w[t,h] * ReLU(q_fp4[t,h] . k_fp4[s]),   s < context_lens[t].
 //
-// GB300 design (one persistent CTA per SM, 15 warps):
+// GB300 design (one persistent CTA per SM, 16 warps):
 //   A tile is 128 tokens = two cache pages, the A operand of an M = 128 MMA laid out as
 //   [block c][page][64 tokens][16 B] (canonical no-swizzle K-major).  A pipeline stage
 //   holds two tiles (four pages).
-//   warps 5-6 producers, taking alternate stages (issuing a gather4 occupies a warp
+//   warps 6-7 producers, taking alternate stages (issuing a gather4 occupies a warp
 //           for about 120 cycles, so one warp alone cannot keep up with the SM's
 //           share of HBM bandwidth): per stage, four TMA tile::gather4 loads of the
 //           payload (each fetches the 1 KB rows (page, c) of two pages for two blocks,
 //           landing directly in the interleaved operand layout) and one gather4 of the
-//           four 256 B scale pages; warp 5 also loads each work item's query rows (one
+//           four 256 B scale pages; warp 6 also loads each work item's query rows (one
 //           bulk copy for the payloads, one for the scales).  Page ids are read 32 at
 //           a time.
 //   warps 0-3 scale writers, one per TMEM lane group: per tile, lane m of group m/32
@@ -24,11 +24,14 @@
 //           work item, the query rows' head scales go to every lane group (heads l and
 //           32 + l in lane l).  Four warps on four schedulers keep this transposition,
 //           which every stage needs, off the critical path.
-//   warp 4  MMA issuer: per (stage, query row), two kind::mxf4 MMAs (K = 64 each) per
+//   warps 4-5 MMA issuers (lane 0 of each), taking alternate stages: a lone issuing
+//           thread runs its per-stage path of dependent instructions at a few cycles
+//           each, which made it the pipeline's bottleneck.  Per (stage, query row), two
+//           kind::mxf4 MMAs (K = 64 each) per
 //           tile into a 64-column TMEM slot of its own (6 slots): D[128 tokens x 64 heads].
 //           Slots per tile let the epilogue release each tile as soon as it has read
 //           it and keep the MMAs up to three stages ahead of it.
-//   warps 7-14 epilogue, two per TMEM lane group taking alternate slots: thread =
+//   warps 8-15 epilogue, two per TMEM lane group (half h reads tile h): thread =
 //           TMEM lane = token; ReLU, head-weighted sum, mask at the row's context
 //           length, coalesced fp32 store.
 // Work items come from the length-balanced schedule (schedule.cuh).  Every wait is
@@ -49,12 +52,15 @@ constexpr int kAccSlots = 3;        // TMEM accumulator slots, one (stage, query
 constexpr int kEpiWarps = 8;
 constexpr int kProducers = 2;
 constexpr int kScaleWarps = 4;
-constexpr int kWarps = kScaleWarps + 1 + kProducers + kEpiWarps;
+constexpr int kMmaWarps = 2;
+constexpr int kWarps = kScaleWarps + kMmaWarps + kProducers + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpMma = kScaleWarps, kWarpProducer = kWarpMma + 1, kWarpEpi0 = kWarpProducer + kProducers;
-static_assert(kStages % kProducers == 0 && kEpiWarps == 8, "stage ownership; four consecutive warps per half");
+constexpr int kWarpMma = kScaleWarps, kWarpProducer = kWarpMma + kMmaWarps, kWarpEpi0 = kWarpProducer + kProducers;
+static_assert(kStages % kProducers == 0 && kStages % kMmaWarps == 0 && kEpiWarps == 8,
+              "stage ownership; four consecutive warps per epilogue half");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr uint32_t kSuspendNs = 20000;  // upper bound of one suspended probe
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
@@ -75,7 +81,8 @@ constexpr uint32_t OFF_KPAY = 0;
 constexpr uint32_t OFF_KSC = OFF_KPAY + kStages * kKPayBytes;
 constexpr uint32_t OFF_QPAY = OFF_KSC + kStages * kKScBytes;
 constexpr uint32_t OFF_QSC = OFF_QPAY + 2 * kQPayBytes;
-constexpr uint32_t OFF_LEN = OFF_QSC + 2 * kQScBytes;  // per epilogue warp: [kGroupMax] int32
+constexpr uint32_t OFF_WEPI = OFF_QSC + 2 * kQScBytes;  // per epilogue warp: the item's head weights, [kGroupMax][64] fp32
+constexpr uint32_t OFF_LEN = OFF_WEPI + kEpiWarps * kGroupMax * 256;  // per epilogue warp: [kGroupMax] int32
 constexpr uint32_t OFF_BAR = OFF_LEN + kEpiWarps * kGroupMax * 4;
 constexpr int kNumBars = 2 * kStages + 6 + kAccSlots;
 // Monotonic arrival counters: per stage buffer, scale-writer warps that finished it
@@ -88,7 +95,7 @@ constexpr uint32_t OFF_CNT = OFF_BAR + kNumBars * 8;
 constexpr uint32_t OFF_MISC = OFF_CNT + (kStages + kAccSlots) * 4;
 constexpr uint32_t kSmemBytes = OFF_MISC + 16;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0, "alignment");
+static_assert(OFF_BAR % 8 == 0 && OFF_QPAY % 1024 == 0 && OFF_KSC % 128 == 0 && OFF_WEPI % 16 == 0, "alignment");
 
 // barrier slots
 __device__ __forceinline__ uint32_t bar_kfull(uint32_t b, int s) { return b + OFF_BAR + 8u * s; }
@@ -125,12 +132,14 @@ struct Ctl {
 
 // Bounded poll of an mbarrier phase by the calling thread.  False on timeout (which
 // raises the abort flag) or, when honor_abort, once another warp has aborted.
+// A waiting thread stays suspended between probes (up to kSuspendNs each) instead of
+// spinning, so that waiters leave their scheduler's issue slots to the working warps.
 __device__ __forceinline__ bool poll(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if ((it & 7u) == 0) {
       if (honor_abort && *c.abort) return false;
       if (ptx::globaltimer() - t0 > kTimeoutNs) {
         *c.abort = 1;
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     for (int i = 0; i < kStages + kAccSlots; i++) reinterpret_cast<uint32_t*>(smem + OFF_CNT)[i] = 0u;
     for (int q = 0; q < 2; q++) {
       ptx::mbar_init(bar_qfull(sb, q), 1);
-      ptx::mbar_init(bar_qempty(sb, q), 1);
+      ptx::mbar_init(bar_qempty(sb, q), kMmaWarps);  // each issuer commits once per item
       ptx::mbar_init(bar_qsf(sb, q), kScaleWarps);
     }
     for (int s = 0; s < kAccSlots; s++) ptx::mbar_init(bar_accfull(sb, s), 1);
@@ -327,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
         if (!*abort_flag) wait_lane0(bar_qempty(sb, u & 1), (u >> 1) & 1, ctl);
       }
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer (one thread)
+  } else if (warp >= kWarpMma && warp < kWarpMma + kMmaWarps) {
+    // ------------------------------------------------------------ MMA issuers (lane 0)
+    const int mw = warp - kWarpMma;  // issues the stages with kctr % kMmaWarps == mw
     if (lane == 0) {
       uint32_t kctr = 0, ictr = 0, ucnt = 0;
       bool ok = true;
@@ -337,21 +347,26 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       while (ok && items.next(g, t0, t1)) {
         const int32_t rows = sv.row0[g + 1] - sv.row0[g];
         const int qb = ictr & 1;
-        // query rows landed and their scale atoms are in tensor memory
-        ok = poll(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl, true);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
+        bool q_ready = false;
+        for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage, kctr++, ucnt += rows) {
+          if ((int)(kctr % kMmaWarps) != mw) continue;
+          if (!q_ready) {
+            // query rows landed and their scales are in tensor memory
+            ok = poll(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl, true);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            q_ready = true;
+          }
           const int s = kctr % kStages;
           const int tiles = stage_tiles(i, t1);
           // the stage's tiles landed with their scales in tensor memory (every scale
           // writer done with this use of the buffer), and each row's accumulator slot
           // is free (every epilogue warp released its previous use)
           const uint32_t need_sf = (uint32_t)kScaleWarps * (kctr / kStages + 1);
-          for (int r = 0; r < rows; r++, ucnt++) {
-            const int slot = ucnt % kAccSlots;
-            ok = wait_counts(cnt_sf(sb, s), need_sf, cnt_slot(sb, slot), (uint32_t)kEpiWarps * (ucnt / kAccSlots),
-                             ctl);
+          for (int r = 0; r < rows; r++) {
+            const uint32_t u = ucnt + r;
+            const int slot = u % kAccSlots;
+            ok = wait_counts(cnt_sf(sb, s), need_sf, cnt_slot(sb, slot), (uint32_t)kEpiWarps * (u / kAccSlots), ctl);
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t b0 = sb + OFF_QPAY + qb * kQPayBytes + r * 4096;
@@ -368,10 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           }
           if (!ok) break;
           ptx::mma_commit(bar_kempty(sb, s));
-          kctr++;
         }
         if (!ok) break;
-        ptx::mma_commit(bar_qempty(sb, qb));
+        // this issuer is done with the item's queries: once its MMAs have read them, or at
+        // once when it issued none for this item
+        if (q_ready)
+          ptx::mma_commit(bar_qempty(sb, qb));
+        else
+          ptx::mbar_arrive(bar_qempty(sb, qb));
         ictr++;
       }
     }
@@ -425,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     const int quad = warp & 3;        // TMEM lanes this warp may read
     const int m = quad * 32 + lane;   // token row of a tile
     int32_t* lsm = reinterpret_cast<int32_t*>(smem + OFF_LEN) + ew * kGroupMax;
+    float* wsm = reinterpret_cast<float*>(smem + OFF_WEPI) + ew * kGroupMax * 64;  // this warp's copy
     uint32_t ucnt = 0;
     bool ok = true;
     while (ok && items.next(g, t0, t1)) {
@@ -438,11 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
         }
         lsm[lane] = L;
       }
+      // the group's head weights, copied once per item into this warp's own shared memory
+      // (read back as broadcast shared loads, off the global-load scoreboard)
+      for (int j = lane; j < rows * 16; j += 32)
+        reinterpret_cast<float4*>(wsm)[j] = __ldg(reinterpret_cast<const float4*>(p.w + (int64_t)r0 * 64) + j);
       __syncwarp();
       for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
         const int tiles = stage_tiles(i, t1);
         for (int r = 0; r < rows && ok; r++) {
-          const float* wr = p.w + (int64_t)(r0 + r) * 64;  // same address in every lane: L1 broadcast
+          const float* wr = wsm + r * 64;  // same address in every lane: shared-memory broadcast
           const int32_t L = lsm[r];
           float* orow = p.out + (int64_t)(r0 + r) * p.out_stride;
           {
@@ -462,16 +486,19 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
             if (a >= tiles) continue;
             const int32_t tok = (i + a) * kTileTokens + m;
             if (tok < L) {
-              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+              // sum_h w_h * ReLU(d_h): scalar ReLU, packed pair FMAs, eight partial sums
+              // (head h goes to partial h mod 8) so that the dependent chains are short
+              float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, a4 = 0.f, a5 = 0.f, a6 = 0.f, a7 = 0.f;
 #pragma unroll
-              for (int h = 0; h < 64; h += 4) {
-                const float4 wv = __ldg(reinterpret_cast<const float4*>(wr + h));
-                a0 = fmaf(wv.x, fmaxf(d[h + 0], 0.f), a0);
-                a1 = fmaf(wv.y, fmaxf(d[h + 1], 0.f), a1);
-                a2 = fmaf(wv.z, fmaxf(d[h + 2], 0.f), a2);
-                a3 = fmaf(wv.w, fmaxf(d[h + 3], 0.f), a3);
+              for (int h = 0; h < 64; h += 8) {
+                const float4 wv = *reinterpret_cast<const float4*>(wr + h);
+                const float4 wu = *reinterpret_cast<const float4*>(wr + h + 4);
+                ptx::ffma2(a0, a1, wv.x, wv.y, fmaxf(d[h + 0], 0.f), fmaxf(d[h + 1], 0.f));
+                ptx::ffma2(a2, a3, wv.z, wv.w, fmaxf(d[h + 2], 0.f), fmaxf(d[h + 3], 0.f));
+                ptx::ffma2(a4, a5, wu.x, wu.y, fmaxf(d[h + 4], 0.f), fmaxf(d[h + 5], 0.f));
+                ptx::ffma2(a6, a7, wu.z, wu.w, fmaxf(d[h + 6], 0.f), fmaxf(d[h + 7], 0.f));
               }
-              orow[tok] = (a0 + a1) + (a2 + a3);
+              orow[tok] = ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
             }
           }
         }

@@ -36,6 +36,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete may stay suspended (not
+// issuing) for up to `suspend_ns` before the probe returns false; it resumes as soon as
+// the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- bulk copy (TMA engine, non-tensor)
 // Global -> this CTA's shared memory, completion counted on `bar` (bytes).  Both addresses
 // 16-byte aligned, size a multiple of 16.
@@ -124,6 +139,15 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
                "r"(d)
                : "memory");
 }
+// Packed pair FMA: (acc.x, acc.y) += (a.x * b.x, a.y * b.y), each lane rounded once.
+__device__ __forceinline__ void ffma2(float& acc_x, float& acc_y, float a_x, float a_y, float b_x, float b_y) {
+  asm("{\n\t.reg .b64 pa, pb, pc;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%0, %1};\n\t"
+      "fma.rn.f32x2 pc, pa, pb, pc;\n\tmov.b64 {%0, %1}, pc;\n\t}"
+      : "+f"(acc_x), "+f"(acc_y)
+      : "f"(a_x), "f"(a_y), "f"(b_x), "f"(b_y));
+}
+
 // Shared-memory counters with release/acquire ordering at CTA scope.
 __device__ __forceinline__ void smem_add_release(uint32_t addr, uint32_t v) {
   asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
