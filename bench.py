@@ -34,7 +34,7 @@ UNIT = "query rows/s"
 L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_decode_b64_traffic.json")
 LOGITS_SRC = os.path.join(ROOT, "sparse_attention_fp4_gb300", "csrc", "logits_mxf4.cu")
-KERNELS_PER_STEP = 5  # store_k, quant_q, build_schedule, logits, top-k (+ one memset node)
+KERNELS_PER_STEP = 5  # store_k, quant_q, build_schedule, logits, top-k (the fused call needs no clearing launch)
 
 WORKLOADS = {
     "decode_b64": ("decode_batch64", 1001),
@@ -251,6 +251,8 @@ class DecodeStep:
         self.topk = torch.empty((self.T, self.k), dtype=torch.int32, device=device)
         self.topk_ws = torch.empty(fp4idx.topk_workspace_bytes(self.T, self.max_ctx), dtype=torch.uint8,
                                    device=device)
+        self.fused_ws = torch.empty(fp4idx.logits_workspace_bytes(self.T, self.max_ctx, self.k), dtype=torch.uint8,
+                                    device=device)
         torch.cuda.synchronize(device)
 
     def calls(self):
@@ -267,16 +269,31 @@ class DecodeStep:
                                     status=self.status)),
         ]
 
+    def logits_topk(self):
+        """The fused entry point a caller uses for the read side: logits into the
+        workspace, then the top-k selection (whose counters the logits launch clears)."""
+        self.fp4idx.logits_topk(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
+                                self.max_ctx, self.k, self.sched, self.fused_ws, self.topk, status=self.status)
+
     def launch(self):
         for _, fn in self.calls():
             fn()
 
+    def launch_user(self):
+        """The step as a caller issues it, in order on one stream: K store, Q quant,
+        schedule, then the fused logits + top-k call."""
+        calls = dict(self.calls())
+        for name in ("store_k", "quant_q", "build_schedule"):
+            calls[name]()
+        self.logits_topk()
+
     def launch_forked(self, side_streams, marks=None):
         """The step with its independent launches overlapped: K store, Q quant and the
-        schedule depend on nothing but their inputs, so they run on three streams and the
-        logits wait for all three (the form captured into the step's graph).  `marks`, three
-        timing events, are recorded before the logits, between logits and top-k, and after
-        the top-k, on the stream that launches both."""
+        schedule depend on nothing but their inputs, so they run on three streams, and the
+        fused logits + top-k call waits for all three (the form captured into the step's
+        graph).  With `marks` (three timing events) the read side is issued as its two
+        separate calls instead, with the marks recorded before the logits, between logits
+        and top-k, and after the top-k."""
         import torch
         calls = dict(self.calls())
         cur = torch.cuda.current_stream()
@@ -292,14 +309,14 @@ class DecodeStep:
             done.append(ev)
         for ev in done:
             cur.wait_event(ev)
-        if marks:
+        if marks:  # separate calls, so that each kernel can be timed
             marks[0].record(cur)
-        calls["logits"]()
-        if marks:
+            calls["logits"]()
             marks[1].record(cur)
-        calls["topk"]()
-        if marks:
+            calls["topk"]()
             marks[2].record(cur)
+        else:
+            self.logits_topk()
 
 
 def run_gpu(args):
@@ -445,8 +462,8 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1,ue8m0)->f32", "data": "synthetic",
             "config": {"workload": b.name, "rows": b.n_rows, "heads": 64, "head_dim": 128, "topk": b.topk,
                        "context_tokens": int(b.context_lens.sum()), "cache_pages": b.num_pages,
-                       "step": "K store (newest token per sequence) + Q quant + schedule + logits + top-k, "
-                               "one CUDA graph replay (store, quant and schedule on parallel branches)",
+                       "step": "K store (newest token per sequence) + Q quant + schedule + fused logits/top-k "
+                               "call, one CUDA graph replay (store, quant and schedule on parallel branches)",
                        "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "kcache_gbs": round(ab["k_cache"] / (logits_us * 1e-6) / 1e9, 1),
@@ -465,7 +482,8 @@ def run_gpu(args):
 
 def run_e2e(st, args, flush_l2):
     """Same metric through the C ABI with host buffers: every step copies its inputs from
-    pinned host memory, runs the five calls and reads the selection back."""
+    pinned host memory, makes the four calls a caller makes (K store, Q quant, schedule,
+    fused logits + top-k) and reads the selection back."""
     import torch
     b = st.b
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -478,6 +496,24 @@ def run_e2e(st, args, flush_l2):
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = out.numel() * out.element_size()
     K = min(args.steps, 200)
+
+    def step():
+        for key, t in h.items():
+            dst[key].copy_(t, non_blocking=True)
+        st.launch_user()
+        out.copy_(st.topk, non_blocking=True)
+
+    # the step as a serving loop replays it: one CUDA graph holding the copies in from
+    # pinned host memory, the four calls and the copy of the selection back
+    s = torch.cuda.Stream(st.device)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
     times = []
     for i in range(K + 3):
         flush_l2()
@@ -485,17 +521,18 @@ def run_e2e(st, args, flush_l2):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        for key, t in h.items():
-            dst[key].copy_(t, non_blocking=True)
-        st.launch()
-        out.copy_(st.topk, non_blocking=True)
+        g.replay()
         e1.record()
         e1.synchronize()
         if i >= 3:
             times.append(e0.elapsed_time(e1) / 1e3)
+    ok = np.array_equal(out.numpy(), st.topk.cpu().numpy())
     value, _ = aggregate(st.T * K, sum(times), st.device)
     return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": K, "ms_per_step": round(sum(times) / K * 1e3, 4)}
+            "steps": K, "ms_per_step": round(sum(times) / K * 1e3, 4),
+            "how": "one CUDA graph replay per step: host-to-device copies of the step's inputs from pinned memory, "
+                   "the store/quant/schedule/logits-top-k calls, device-to-host copy of the selection",
+            "selection_read_back_matches": bool(ok)}
 
 
 # ------------------------------------------------------------------ the CPU oracle (baseline / reference arm)

@@ -556,9 +556,13 @@ std::atomic<bool> g_attr_done[64];
 
 size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context) { return layout(n_rows, max_context).total; }
 
+uint32_t* topk_arrival_counters(void* workspace, int64_t n_rows, int32_t max_context) {
+  return reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + layout(n_rows, max_context).arr);
+}
+
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool counters_zeroed) {
   if (n_rows == 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -575,7 +579,8 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
   }
   const Layout l = layout(n_rows, max_context);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  topk_clear_kernel<<<(n_rows + 255) / 256, 256, 0, stream>>>(reinterpret_cast<unsigned int*>(ws + l.arr), n_rows);
+  if (!counters_zeroed)
+    topk_clear_kernel<<<(n_rows + 255) / 256, 256, 0, stream>>>(reinterpret_cast<unsigned int*>(ws + l.arr), n_rows);
   const int nch = num_chunks(max_context);
   topk_kernel<<<dim3((unsigned)n_rows, (unsigned)nch), kThreads, kDynSmem, stream>>>(
       logits, stride, context_lens, max_context, k, reinterpret_cast<uint32_t*>(ws),
