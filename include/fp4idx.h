@@ -174,9 +174,9 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
  * (logits_stride >= max_context; the rest of each row is not written).  fp4idx_topk
  * selects from such a buffer: topk_idx[t] = the k largest of logits[t][0..L_t), ascending
  * positions, -1 padding; ties at the k-th value go to the lower positions.  Its scratch
- * (a candidate list per row and per-row arrival counters, which each call clears with
- * cudaMemsetAsync on `stream`) lives in `workspace`, at least
- * fp4idx_topk_workspace_bytes(n_rows, max_context) bytes, 16-byte aligned.
+ * (per row, room for the candidate list when it does not fit in shared memory) lives in
+ * `workspace`, at least fp4idx_topk_workspace_bytes(n_rows, max_context) bytes, 16-byte
+ * aligned; nothing in it needs to be initialised.
  */
 int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows, int32_t n_heads,
                   const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
@@ -205,8 +205,8 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
  *     the array's address once; make that first call before any stream capture begins.
  *     Of the conventions at the top of this file, the one on graph capture is not
  *     stated for this entry point.
- *   - Zero state: the per-row arrival counters in the array must be zero when the
- *     kernel starts; every call clears them itself (cudaMemsetAsync on `stream`).
+ *   - Nothing in the array needs to start at zero: a call writes every candidate it
+ *     reads back.
  *   - All calls on a device share the array: calls whose kernels may overlap (unordered
  *     streams, concurrent host threads) race on it.  Order them on one stream.
  */

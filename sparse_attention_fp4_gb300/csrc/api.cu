@@ -158,13 +158,13 @@ int launch_logits_checked(const uint8_t* q_payload, const uint8_t* q_scale, cons
                           const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
                           int64_t num_seqs, int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
                           int32_t max_context, const void* schedule, float* buf, int64_t stride, int32_t* status_dev,
-                          cudaStream_t s, uint32_t* zero_words = nullptr, int32_t n_zero = 0) {
+                          cudaStream_t s) {
   int32_t grid = 0;
   int st = device_sms(&grid);
   if (st != FP4IDX_OK) return st;
   return from_cuda(fp4idx::launch_logits_mxf4(q_payload, q_scale, w, (int32_t)n_rows, payload, scale, num_pages,
                                               page_table, num_seqs, max_pages, row_seq, context_lens, max_context,
-                                              schedule, grid, buf, stride, zero_words, n_zero, status_dev, s));
+                                              schedule, grid, buf, stride, status_dev, s));
 }
 
 }  // namespace
@@ -226,13 +226,11 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
   }
   void* topk_ws = reinterpret_cast<uint8_t*>(workspace) + logits_region_bytes(n_rows, max_context);
   cudaStream_t s = as_stream(stream);
-  // the logits launch clears the top-k arrival counters, so the top-k needs no clearing launch
   st = launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs, max_pages,
-                             row_seq, context_lens, max_context, schedule, buf, stride, status_dev, s,
-                             fp4idx::topk_arrival_counters(topk_ws, n_rows, max_context), (int32_t)n_rows);
+                             row_seq, context_lens, max_context, schedule, buf, stride, status_dev, s);
   if (st != FP4IDX_OK) return st;
   return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_ws,
-                                       topk_idx, status_dev, s, /*counters_zeroed=*/true));
+                                       topk_idx, status_dev, s));
 }
 
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream) {

@@ -37,14 +37,10 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
                                const int32_t* page_table, int64_t num_seqs, int32_t max_pages,
                                const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
                                const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
-                               uint32_t* zero_words, int32_t n_zero, int32_t* status, cudaStream_t stream);
+                               int32_t* status, cudaStream_t stream);
 size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context);
-// The top-k scratch holds per-row arrival counters that must be zero when the top-k
-// kernel starts: launch_topk clears them with a small kernel unless counters_zeroed says
-// an earlier launch on the stream (the fused logits launch) already has.
-uint32_t* topk_arrival_counters(void* workspace, int64_t n_rows, int32_t max_context);
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,
-                        cudaStream_t stream, bool counters_zeroed = false);
+                        cudaStream_t stream);
 
 }  // namespace fp4idx

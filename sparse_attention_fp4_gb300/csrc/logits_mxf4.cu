@@ -122,8 +122,6 @@ struct LogitsParams {
   const void* schedule;
   float* out;
   int64_t out_stride;
-  uint32_t* zero_words;  // words this launch clears for a later launch on the stream (may be null)
-  int32_t n_zero;
   int32_t* status;
 };
 
@@ -210,8 +208,6 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = ptx::smem_addr(smem);
-  // words a following launch needs zeroed (the top-k arrival counters of the fused call)
-  for (int32_t i = blockIdx.x * kThreads + threadIdx.x; i < p.n_zero; i += gridDim.x * kThreads) p.zero_words[i] = 0u;
 
   // The schedule must describe exactly these rows and this grid.
   const SchedView sv = sched_view(const_cast<void*>(p.schedule), p.n_rows);
@@ -554,7 +550,7 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
                                const int32_t* page_table, int64_t num_seqs, int32_t max_pages,
                                const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
                                const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
-                               uint32_t* zero_words, int32_t n_zero, int32_t* status, cudaStream_t stream) {
+                               int32_t* status, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(logits_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -581,8 +577,6 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
   prm.schedule = schedule;
   prm.out = out;
   prm.out_stride = out_stride;
-  prm.zero_words = zero_words;
-  prm.n_zero = zero_words ? n_zero : 0;
   prm.status = status;
   logits_mxf4_kernel<<<num_ctas, kThreads, kSmemBytes, stream>>>(pay_map, sc_map, prm);
   return cudaGetLastError();

@@ -6,23 +6,23 @@
 // context length 0 (their selection is empty: all -1).
 //
 // Selection = the k largest logits of a row, ties at the k-th value to the lower
-// positions, emitted in ascending position order.  One launch, grid (rows, chunks of
-// 4,096 tokens):
-//   every CTA of a row takes the same fixed sample of 1,024 of the row's logits and
-//     derives the same conservative threshold (a linear 256-bucket histogram of the
-//     sample, cut about four standard deviations beyond the expected place of the k-th
-//     largest), then writes the keys and positions of its chunk's logits at or above it,
-//     in order, into the chunk's own region of a candidate buffer;
-//   the last CTA of the row to finish (a fence, then an arrival counter; nobody waits)
-//     concatenates the regions in order, buckets the candidates linearly between their
-//     min and max, ranks the boundary bucket's members exactly and emits the keys above
-//     the k-th and the lowest-positioned ones equal to it.
+// positions, emitted in ascending position order.  One CTA of 512 threads per row and
+// no communication between CTAs (every hand-off between CTAs -- a global candidate list,
+// a fence and an arrival counter -- cost microseconds of latency on this path):
+//   1. a fixed sample of 1,024 of the row's logits (128 runs of 8 adjacent logits) gives
+//      a conservative threshold: a linear 256-bucket histogram of the sample, cut about
+//      four standard deviations beyond the expected place of the k-th largest;
+//   2. the row, 32 logits per thread held in registers (blocks of 16,384 tokens, read as
+//      float4 groups interleaved across the threads so that loads coalesce), is compacted
+//      in position order into the candidates at or above the threshold: in shared memory
+//      when they fit (kCapB), else in the caller's workspace;
+//   3. the candidates are bucketed linearly between their min and max (2,048 buckets),
+//      the boundary bucket is ranked exactly (radix select when it is crowded with
+//      ties), and the keys above the k-th plus the lowest-positioned equal ones are
+//      emitted in order.
 // The threshold is superset-closed (a value that passes lets every larger one pass), so
-// with at least k candidates the candidates hold the whole answer.  The sample decides
-// speed, never the result: with fewer than k or more than kCapB candidates the last CTA
-// runs the exact path over the whole row (2048 linear buckets between the row's min and
-// max, a refinement of a crowded bucket over its own range, the bucket ranked exactly,
-// radix select when a bucket is all ties).
+// with at least k candidates they hold the whole answer: the sample decides speed, never
+// the result.  With fewer than k candidates the exact path runs over the whole row.
 #include "fp4idx_internal.cuh"
 
 #include <atomic>
@@ -30,20 +30,20 @@
 namespace fp4idx {
 namespace {
 
-
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 4096;                  // tokens per CTA: 8 per thread
-constexpr int kPer = kChunk / kThreads;
-constexpr int kCapB = 8192;                   // candidates the selecting CTA holds in shared memory
-constexpr int kMaxChunks = (FP4IDX_MAX_CONTEXT + kChunk - 1) / kChunk;
+constexpr int kPer = 32;                      // logits a thread holds per block
+constexpr int kBlockTokens = kThreads * kPer; // 32,768
+constexpr int kCapB = 8192;                   // candidates kept in shared memory
 constexpr int kBins = 2048;
 constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kGather = 1024;                 // largest boundary bucket ranked by direct counting
 constexpr int kSample = 1024;                 // logits per row behind the candidate threshold
 constexpr int kSampleBins = 256;
 constexpr size_t kDynSmem = kCapB * (sizeof(uint32_t) + sizeof(uint16_t));
-static_assert(kSampleBins <= kThreads && kMaxChunks <= 32 && kSample % kThreads == 0, "layout");
+constexpr int kSamplePer = kSample / kThreads;  // sample logits a thread loads
+static_assert(kSampleBins <= kThreads && kSample % kThreads == 0 && kBins % kThreads == 0 && kPer % 8 == 0,
+              "layout");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Order-preserving key; -0 maps to +0 so that equal values are equal keys.
@@ -183,9 +183,36 @@ __device__ void radix_select(int n, KeyFn key_of, MemberFn member, int rem, int*
 // Emit, in index order, every element i < n whose key is above tau and the first
 // take_total (in index order) whose key equals tau: o[...] = pos_of(i).  Each thread owns a
 // contiguous run of indices; two block scans give the output offsets.  Returns the count.
+// Exclusive block scan of a 64-bit value; `total` gets the block sum.
+__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t* scratch, uint64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t n = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint64_t w = lane < kWarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t n = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < kWarps) scratch[lane] = w;
+  }
+  __syncthreads();
+  const uint64_t before = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
+  total = scratch[kWarps - 1];
+  __syncthreads();
+  return before;
+}
+
 template <class KeyFn, class PosFn>
 __device__ int emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int take_total, int32_t* o, int k,
-                            int* scratch) {
+                            uint64_t* scratch) {
   const int tid = threadIdx.x;
   const int run = ((n + kThreads - 1) / kThreads) | 1;  // odd stride: conflict-free reads
   const int i0 = min(n, tid * run), i1 = min(n, i0 + run);
@@ -195,11 +222,14 @@ __device__ int emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int
     gt += u > tau;
     eq += u == tau;
   }
-  int tot;
-  const int eq_before = block_excl_scan(eq, scratch, tot);
-  const int take_eq = max(0, min(eq, take_total - eq_before));
-  int total;
-  int w = block_excl_scan(gt + take_eq, scratch, total);
+  // one scan of (greater, equal) counts: the equal keys are taken greedily in index
+  // order, so the keys equal to tau taken before this thread's run are min(E, take)
+  uint64_t tot;
+  const uint64_t pre = block_excl_scan64(((uint64_t)gt << 32) | (uint32_t)eq, scratch, tot);
+  const int G = (int)(pre >> 32), E = (int)(uint32_t)pre;
+  const int take_eq = max(0, min(eq, take_total - E));
+  int w = G + min(E, take_total);
+  const int total = (int)(tot >> 32) + min((int)(uint32_t)tot, take_total);
   int te = 0;
   for (int i = i0; i < i1 && w < k; i++) {
     const uint32_t u = key_of(i);
@@ -232,12 +262,14 @@ __device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, uint32_
 }
 
 struct Shared {
+  uint32_t wsum[kWarps][kPer / 8];
+  uint32_t gsum[kPer / 8];
+  uint64_t scratch64[kWarps];
   int hist[kBins];
   uint32_t gkey[kGather];
   int gidx[kGather];
   int scratch[kWarps];
   uint32_t uscratch[2 * kWarps];
-  int coff[kMaxChunks + 1];
   int bin, rem, gcount, take, blo, last;
   uint32_t key;
 };
@@ -330,79 +362,141 @@ __device__ void select_whole_row(const float* lg, int L, int k, int32_t* o, Shar
   } else {
     radix_select(L, key_at, in_bucket, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
   }
-  const int got = emit_ordered(L, key_at, [](int s) { return s; }, sh.key, sh.take, o, k, sh.scratch);
+  const int got = emit_ordered(L, key_at, [](int s) { return s; }, sh.key, sh.take, o, k, sh.scratch64);
   for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
 }
 
-// grid (rows, chunks).  Candidate regions: cand_key/cand_pos[row * cstride + chunk * kChunk
-// ...], counts cnt[row * nch + chunk], arrival counters arrivals[row] (zero at launch).
-__global__ void __launch_bounds__(kThreads, 3) topk_kernel(const float* __restrict__ logits, int64_t stride,
-                                                        const int32_t* __restrict__ context_lens, int32_t max_context,
-                                                        int32_t k, uint32_t* cand_key, uint16_t* cand_pos,
-                                                        int64_t cstride, int32_t* cnt, int32_t nch,
-                                                        unsigned int* arrivals, int32_t* __restrict__ out,
-                                                        int32_t* status) {
+
+constexpr int kGroups = kPer / 4;  // float4 groups a thread holds per block
+
+// Position of element e of this thread's group j in a block starting at `base`: groups are
+// interleaved across the threads (group j of thread t covers base + 4*(j*kThreads + t)),
+// so each warp-wide 16-byte load reads 512 contiguous bytes.
+__device__ __forceinline__ int elem_pos(int base, int j, int e) {
+  return base + 4 * (j * kThreads + (int)threadIdx.x) + e;
+}
+
+// This thread's kPer logits of the block starting at `base`; past L reads nothing and
+// yields 0.
+__device__ __forceinline__ void load_block(const float* lg, int base, int L, float* x) {
+  const bool vec = (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
+#pragma unroll
+  for (int j = 0; j < kGroups; j++) {
+    const int p0 = elem_pos(base, j, 0);
+    if (vec && p0 + 4 <= L) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(lg + p0));
+      x[4 * j] = v.x;
+      x[4 * j + 1] = v.y;
+      x[4 * j + 2] = v.z;
+      x[4 * j + 3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; e++) x[4 * j + e] = p0 + e < L ? __ldg(lg + p0 + e) : 0.0f;
+    }
+  }
+}
+
+// Exclusive prefix, in (group, thread) order, of this thread's per-group counts c[j]
+// (each at most 4): off[j] = sum of all counts of groups before j plus those of lower
+// threads in group j.  Counts travel two to a register in 16-bit halves (a block total
+// is at most 4 * kThreads = 4096).  Returns the block total.
+__device__ __forceinline__ int group_scan(const int* c, int* off, uint32_t (*wsum)[kGroups / 2], uint32_t* gsum) {
+  constexpr int P = kGroups / 2;
+  static_assert(kWarps <= 32, "one warp scans the warp sums");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t v[P], x[P];
+#pragma unroll
+  for (int i = 0; i < P; i++) x[i] = v[i] = (uint32_t)c[2 * i] | ((uint32_t)c[2 * i + 1] << 16);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < P; i++) {
+      const uint32_t n = __shfl_up_sync(kFull, x[i], o);
+      if (lane >= o) x[i] += n;
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < P; i++) wsum[warp][i] = x[i];
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the kWarps warp sums; gsum = per-group block totals
+    uint32_t y[P], z[P];
+#pragma unroll
+    for (int i = 0; i < P; i++) z[i] = y[i] = lane < kWarps ? wsum[lane][i] : 0u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+      for (int i = 0; i < P; i++) {
+        const uint32_t n = __shfl_up_sync(kFull, z[i], o);
+        if (lane >= o) z[i] += n;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < P; i++) {
+      if (lane < kWarps) wsum[lane][i] = z[i] - y[i];
+      if (lane == kWarps - 1) gsum[i] = z[i];
+    }
+  }
+  __syncthreads();
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < P; i++) {
+    const uint32_t pre = x[i] - v[i] + wsum[warp][i];  // within-group exclusive prefix, packed
+    const uint32_t tot = gsum[i];
+    off[2 * i] = base + (int)(pre & 0xFFFFu);
+    base += (int)(tot & 0xFFFFu);
+    off[2 * i + 1] = base + (int)(pre >> 16);
+    base += (int)(tot >> 16);
+  }
+  __syncthreads();  // wsum / gsum may be reused
+  return base;
+}
+
+// One CTA per row.  cand_key/cand_pos + row * cstride: the row's region of the workspace,
+// used when its candidates do not fit in shared memory.
+__global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __restrict__ logits, int64_t stride,
+                                                               const int32_t* __restrict__ context_lens,
+                                                               int32_t max_context, int32_t k, uint32_t* cand_key,
+                                                               uint16_t* cand_pos, int64_t cstride,
+                                                               int32_t* __restrict__ out, int32_t* status) {
   extern __shared__ __align__(16) uint32_t dyn[];  // ckey[kCapB], then cpos[kCapB] (uint16)
   __shared__ Shared sh;
   const int64_t row = blockIdx.x;
-  const int c = blockIdx.y;
   const int tid = threadIdx.x;
   int32_t L = __ldg(context_lens + row);
   if (L < 0 || L > max_context) {
-    if (c == 0 && tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
+    if (tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
     L = L < 0 ? 0 : max_context;
   }
   int32_t* o = out + row * k;
   if (L <= k) {
-    if (c == 0)
-      for (int i = tid; i < k; i += kThreads) o[i] = i < L ? i : -1;
+    for (int i = tid; i < k; i += kThreads) o[i] = i < L ? i : -1;
     return;
   }
-  const int c0 = c * kChunk;
-  if (c0 >= L) return;
-  const int nrow = (L + kChunk - 1) / kChunk;  // CTAs of this row that take part
   const float* lg = logits + row * stride;
 
-  // ---- the row's fixed sample and this CTA's tokens.  The sample is 128 runs of 8
-  // adjacent logits starting at floor(r * L / 128) rounded down to 8 (two float4 loads a
-  // run) when the row is 16-byte aligned and L >= 1024, else single logits at
-  // floor(i * L / 1024).
-  float sv[kSample / kThreads];
-  if ((reinterpret_cast<uintptr_t>(lg) & 15) == 0 && L >= kSample) {
-    static_assert(kSample / kThreads == 2 && kSample / 8 <= kThreads, "two sample logits a thread");
-    const int run = tid >> 2, part = tid & 3;  // 128 runs x 4 threads; a thread takes 2 logits
-    const int p0 = ((int)(((int64_t)run * L) / (kSample / 8)) & ~7) + 2 * part;
-    const float2 v = __ldg(reinterpret_cast<const float2*>(lg + p0));
-    sv[0] = v.x;
-    sv[1] = v.y;
-  } else {
+  // ---- 1. threshold from the row's fixed sample: 128 runs of 8 adjacent logits starting
+  // at floor(r * L / 128) rounded down to 8 (single logits at floor(i * L / 1024) for
+  // rows shorter than 1024)
+  float sv[kSamplePer];
 #pragma unroll
-    for (int j = 0; j < kSample / kThreads; j++)
-      sv[j] = __ldg(lg + (int)(((int64_t)(j * kThreads + tid) * L) / kSample));
+  for (int j = 0; j < kSamplePer; j++) {
+    const int i = j * kThreads + tid;
+    const int sp = L >= kSample ? (((int)(((int64_t)(i >> 3) * L) / (kSample / 8)) & ~7) + (i & 7))
+                                : (int)(((int64_t)i * L) / kSample);
+    sv[j] = __ldg(lg + sp);
   }
   float x[kPer];
-  const int t0 = c0 + tid * kPer;
-  if (((reinterpret_cast<uintptr_t>(lg + t0) & 15) == 0) && t0 + kPer <= L) {
-#pragma unroll
-    for (int q = 0; q < kPer / 4; q++) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(lg + t0) + q);
-      x[4 * q] = v.x;
-      x[4 * q + 1] = v.y;
-      x[4 * q + 2] = v.z;
-      x[4 * q + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < kPer; q++) x[q] = t0 + q < L ? __ldg(lg + t0 + q) : 0.0f;
-  }
+  load_block(lg, 0, L, x);  // issued before the threshold is known
   if (tid < kSampleBins) sh.hist[tid] = 0;
   uint32_t smin = 0xFFFFFFFFu, smax = 0u;
 #pragma unroll
-  for (int j = 0; j < kSample / kThreads; j++) {
+  for (int j = 0; j < kSamplePer; j++) {
     smin = min(smin, order_key(sv[j]));
     smax = max(smax, order_key(sv[j]));
   }
-  block_minmax(smin, smax, sh.uscratch);  // its barrier also orders the histogram clear
+  block_minmax(smin, smax, sh.uscratch);  // its barriers also order the histogram clear
   const float lo = key_value(smin);
   const float sc = lin_scale(lo, key_value(smax)) * ((float)kSampleBins / (float)kBins);
   auto sbucket = [&](float v) -> int {
@@ -410,9 +504,9 @@ __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const float* __restri
     return b >= kSampleBins ? kSampleBins - 1 : b;
   };
 #pragma unroll
-  for (int j = 0; j < kSample / kThreads; j++) atomicAdd(&sh.hist[sbucket(sv[j])], 1);
+  for (int j = 0; j < kSamplePer; j++) atomicAdd(&sh.hist[sbucket(sv[j])], 1);
   __syncthreads();
-  // threshold bucket: keep the sample's expected share of k plus four standard deviations
+  // keep the sample's expected share of k plus four standard deviations
   const float q = (float)k / (float)L;
   const float mean = q * (float)kSample;
   const int need = min(kSample, (int)ceilf(mean + 4.0f * sqrtf(mean * (1.0f - q)) + 8.0f));
@@ -422,170 +516,136 @@ __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const float* __restri
   if (tid < kSampleBins && above < need && need <= above + mine) sh.blo = kSampleBins - 1 - tid;
   __syncthreads();
   const int blo = sh.blo;
+  // the cut as a key: bucket blo starts at lo + blo / sc.  Any key threshold keeps the
+  // candidate set superset-closed, so the rounding of this edge cannot change the result.
+  const uint32_t kthr = (blo == 0 || !(sc > 0.0f)) ? 0u : order_key(lo + (float)blo / sc);
 
-  // ---- order-preserving compaction of this chunk's candidates
-  unsigned flags = 0;
-  int nmine = 0;
+  // ---- 2. order-preserving compaction of the candidates, block by block.  Candidate i
+  // lives in shared memory for i < kCapB and in the row's workspace region beyond.
+  uint32_t* const ckey_s = dyn;
+  uint16_t* const cpos_s = reinterpret_cast<uint16_t*>(dyn + kCapB);
+  uint32_t* const ckey_g = cand_key + row * cstride;
+  uint16_t* const cpos_g = cand_pos + row * cstride;
+  const int nblocks = (L + kBlockTokens - 1) / kBlockTokens;
+  int m = 0;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int blk = 0; blk < nblocks; blk++) {
+    const int base = blk * kBlockTokens;
+    if (blk > 0) load_block(lg, base, L, x);
+    unsigned flags = 0;
+    int cnt[kGroups], off[kGroups];
 #pragma unroll
-  for (int qq = 0; qq < kPer; qq++) {
-    const bool in = t0 + qq < L && sbucket(x[qq]) >= blo;
-    flags |= (unsigned)in << qq;
-    nmine += in;
-  }
-  int total;
-  int w = block_excl_scan(nmine, sh.scratch, total);
-  const int64_t base = row * cstride + c0;
+    for (int j = 0; j < kGroups; j++) {
+      const int p0 = elem_pos(base, j, 0);
+      cnt[j] = 0;
 #pragma unroll
-  for (int qq = 0; qq < kPer; qq++) {
-    if (flags & (1u << qq)) {
-      cand_key[base + w] = order_key(x[qq]);
-      cand_pos[base + w] = (uint16_t)(t0 + qq);  // positions < FP4IDX_MAX_CONTEXT = 65536
-      w++;
+      for (int e = 0; e < 4; e++) {
+        const bool in = p0 + e < L && order_key(x[4 * j + e]) >= kthr;
+        flags |= (unsigned)in << (4 * j + e);
+        cnt[j] += in;
+      }
     }
-  }
-  if (tid == 0) cnt[row * nch + c] = total;
-  // publish (block barrier, then one thread's device-scope fence: the release pattern of a
-  // grid barrier), then count arrivals: the row's last CTA to arrive selects
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const bool last = atomicAdd(arrivals + row, 1u) == (unsigned)(nrow - 1);
-    if (last) __threadfence();
-    sh.last = last;
-  }
-  __syncthreads();
-  if (!sh.last) return;
-
-  // ---- selection by the last CTA: concatenate the regions in chunk (= position) order
-  uint32_t* ckey = dyn;
-  uint16_t* cpos = reinterpret_cast<uint16_t*>(dyn + kCapB);
-  if (tid < 32) {
-    const int v = tid < nrow ? min(max(__ldcg(cnt + row * nch + tid), 0), kChunk) : 0;
-    int xs = v;
+    const int total = group_scan(cnt, off, sh.wsum, sh.gsum);
+    if (m + total <= kCapB) {  // the common case, uniform over the CTA: branch-free stores
 #pragma unroll
-    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-      const int n = __shfl_up_sync(kFull, xs, o2);
-      if (tid >= o2) xs += n;
+      for (int j = 0; j < kGroups; j++) {
+        int w = m + off[j];
+        const int p0 = elem_pos(base, j, 0);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const bool in = (flags >> (4 * j + e)) & 1u;
+          const uint32_t u = order_key(x[4 * j + e]);
+          if (in) {
+            ckey_s[w] = u;
+            cpos_s[w] = (uint16_t)(p0 + e);  // positions < FP4IDX_MAX_CONTEXT = 65536
+          }
+          kmin = min(kmin, in ? u : 0xFFFFFFFFu);
+          kmax = max(kmax, in ? u : 0u);
+          w += in;
+        }
+      }
+    } else {  // candidates past kCapB go to the row's workspace region
+#pragma unroll
+      for (int j = 0; j < kGroups; j++) {
+        int w = m + off[j];
+        const int p0 = elem_pos(base, j, 0);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          if (flags & (1u << (4 * j + e))) {
+            const uint32_t u = order_key(x[4 * j + e]);
+            if (w < kCapB) {
+              ckey_s[w] = u;
+              cpos_s[w] = (uint16_t)(p0 + e);
+            } else {
+              ckey_g[w] = u;
+              cpos_g[w] = (uint16_t)(p0 + e);
+            }
+            kmin = min(kmin, u);
+            kmax = max(kmax, u);
+            w++;
+          }
+        }
+      }
     }
-    if (tid < nrow) sh.coff[tid] = xs - v;
-    if (tid == 31) sh.coff[nrow] = xs;
+    m += total;
   }
-  if (tid == 0) sh.gcount = 0;
-  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
-  __syncthreads();
-  const int m = sh.coff[nrow];
-  if (m < k || m > kCapB) {
+  if (m < k) {  // the threshold was too high for this row: exact path over the whole row
     select_whole_row(lg, L, k, o, sh);
     return;
   }
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  constexpr int kBatch = 8;  // loads a thread keeps in flight at once
-#pragma unroll 1
-  for (int i0 = 0; i0 < m; i0 += kBatch * kThreads) {
-    uint32_t kk[kBatch];
-    uint16_t pp[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; u++) {
-      const int i = i0 + u * kThreads + tid;
-      if (i < m) {
-        int lo = 0, hi = nrow;  // chunk of element i: coff[lo] <= i < coff[lo + 1]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (sh.coff[mid] <= i) lo = mid; else hi = mid;
-        }
-        const int64_t gi = row * cstride + (int64_t)lo * kChunk + (i - sh.coff[lo]);
-        kk[u] = __ldcg(cand_key + gi);
-        pp[u] = __ldcg(cand_pos + gi);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; u++) {
-      const int i = i0 + u * kThreads + tid;
-      if (i < m) {
-        ckey[i] = kk[u];
-        cpos[i] = pp[u];
-        kmin = min(kmin, kk[u]);
-        kmax = max(kmax, kk[u]);
-      }
-    }
-  }
-  block_minmax(kmin, kmax, sh.uscratch);  // also publishes ckey/cpos
+
+  // ---- 3. selection among the candidates (m >= k)
+  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
+  if (tid == 0) sh.gcount = 0;
+  block_minmax(kmin, kmax, sh.uscratch);  // its barriers also publish the candidates
   const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
-  for (int i = tid; i < m; i += kThreads) atomicAdd(&sh.hist[lin_bucket(key_value(ckey[i]), lo1, sc1)], 1);
+  auto ck = [&](int i) -> uint32_t { return i < kCapB ? ckey_s[i] : __ldcg(ckey_g + i); };
+  auto cpos = [&](int i) -> int { return i < kCapB ? (int)cpos_s[i] : (int)__ldcg(cpos_g + i); };
+  for (int i = tid; i < m; i += kThreads) atomicAdd(&sh.hist[lin_bucket(key_value(ck(i)), lo1, sc1)], 1);
   __syncthreads();
   find_bin_from_top(sh.hist, k, sh.scratch, &sh.bin, &sh.rem);
   const int b1 = sh.bin, rem = sh.rem, nb = sh.hist[b1];
   __syncthreads();  // every thread has read nb before the radix path clears the histogram
-  auto ck = [&](int i) -> uint32_t { return ckey[i]; };
-  auto in_b1 = [&](int i) -> bool { return lin_bucket(key_value(ckey[i]), lo1, sc1) == b1; };
+  auto in_b1 = [&](int i) -> bool { return lin_bucket(key_value(ck(i)), lo1, sc1) == b1; };
   if (nb <= kGather) {
     rank_bucket(m, ck, in_b1, nb, rem, sh);
   } else {
     radix_select(m, ck, in_b1, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
   }
-  const int got = emit_ordered(m, ck, [&](int i) { return (int)cpos[i]; }, sh.key, sh.take, o, k, sh.scratch);
+  const int got = emit_ordered(m, ck, cpos, sh.key, sh.take, o, k, sh.scratch64);
   for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
 }
 
-inline int num_chunks(int32_t max_context) { return (max(max_context, 1) + kChunk - 1) / kChunk; }
 inline int64_t cand_stride(int32_t max_context) { return ((int64_t)max(max_context, 1) + 7) / 8 * 8; }
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
-
-// Workspace: [candidate keys u32][candidate positions u16][chunk counts i32][arrivals u32].
-struct Layout {
-  size_t pos, cnt, arr, total;
-};
-inline Layout layout(int64_t n_rows, int32_t max_context) {
-  const size_t cells = (size_t)n_rows * (size_t)cand_stride(max_context);
-  Layout l;
-  l.pos = align256(cells * sizeof(uint32_t));
-  l.cnt = l.pos + align256(cells * sizeof(uint16_t));
-  l.arr = l.cnt + align256((size_t)n_rows * (size_t)num_chunks(max_context) * sizeof(int32_t));
-  l.total = l.arr + align256((size_t)n_rows * sizeof(uint32_t));
-  return l;
-}
-
-__global__ void topk_clear_kernel(unsigned int* arrivals, int32_t n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) arrivals[i] = 0u;
-}
 
 std::atomic<bool> g_attr_done[64];
 
 }  // namespace
 
-size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context) { return layout(n_rows, max_context).total; }
-
-uint32_t* topk_arrival_counters(void* workspace, int64_t n_rows, int32_t max_context) {
-  return reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + layout(n_rows, max_context).arr);
+// Workspace: per row, a spill region for its candidate keys (u32) and positions (u16).
+size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context) {
+  const size_t cells = (size_t)n_rows * (size_t)cand_stride(max_context);
+  return align256(cells * sizeof(uint32_t)) + align256(cells * sizeof(uint16_t));
 }
 
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,
-                        cudaStream_t stream, bool counters_zeroed) {
+                        cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !g_attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-    if (e != cudaSuccess) return e;
-    // both kernels keep the SM's largest shared-memory split: no reconfiguration between them
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_clear_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) g_attr_done[dev].store(true);
   }
-  const Layout l = layout(n_rows, max_context);
+  const size_t cells = (size_t)n_rows * (size_t)cand_stride(max_context);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  if (!counters_zeroed)
-    topk_clear_kernel<<<(n_rows + 255) / 256, 256, 0, stream>>>(reinterpret_cast<unsigned int*>(ws + l.arr), n_rows);
-  const int nch = num_chunks(max_context);
-  topk_kernel<<<dim3((unsigned)n_rows, (unsigned)nch), kThreads, kDynSmem, stream>>>(
+  topk_row_kernel<<<(unsigned)n_rows, kThreads, kDynSmem, stream>>>(
       logits, stride, context_lens, max_context, k, reinterpret_cast<uint32_t*>(ws),
-      reinterpret_cast<uint16_t*>(ws + l.pos), cand_stride(max_context), reinterpret_cast<int32_t*>(ws + l.cnt), nch,
-      reinterpret_cast<unsigned int*>(ws + l.arr), out, status);
+      reinterpret_cast<uint16_t*>(ws + align256(cells * sizeof(uint32_t))), cand_stride(max_context), out, status);
   return cudaGetLastError();
 }
 

@@ -17,10 +17,9 @@
 // array's device address once (cudaGetSymbolAddress) and keeps it for later calls on the
 // same device; make that first call before any stream capture begins.
 //
-// Zero state: the per-row arrival counters (the row's last CTA to arrive does the
-// selection) must be zero when the kernel starts, so every call clears them with
-// cudaMemsetAsync on its stream before the launch.  Candidate counts and lists are
-// written before they are read and need no clearing.
+// Zero state: nothing in the array needs to start at zero.  A row's candidates go there
+// only when they do not fit in shared memory, and each call reads back only the
+// candidates it wrote itself.  So no call clears the array.
 //
 // Every call on a device uses the same array.  Calls whose kernels may overlap (on
 // streams with no ordering between them, or from host threads at once) race on it and
