@@ -40,7 +40,7 @@ constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kGather = 1024;                 // largest boundary bucket ranked by direct counting
 constexpr int kSample = 1024;                 // logits per row behind the candidate threshold
 constexpr int kSampleBins = 256;
-constexpr size_t kDynSmem = kCapB * (sizeof(uint32_t) + sizeof(uint16_t));
+constexpr size_t kDynSmem = kCapB * (sizeof(uint32_t) + sizeof(uint16_t)) + FP4IDX_MAX_TOPK * sizeof(int32_t);
 constexpr int kSamplePer = kSample / kThreads;  // sample logits a thread loads
 static_assert(kSampleBins <= kThreads && kSample % kThreads == 0 && kBins % kThreads == 0 && kPer % 8 == 0,
               "layout");
@@ -210,9 +210,11 @@ __device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t* scra
   return before;
 }
 
+// Writes o[0..k): the selected positions in index order, then -1.  They are staged in
+// shared memory (`stage`, k entries) and copied out with coalesced stores.
 template <class KeyFn, class PosFn>
-__device__ int emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int take_total, int32_t* o, int k,
-                            uint64_t* scratch) {
+__device__ void emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int take_total, int32_t* o, int k,
+                             uint64_t* scratch, int32_t* stage) {
   const int tid = threadIdx.x;
   const int run = ((n + kThreads - 1) / kThreads) | 1;  // odd stride: conflict-free reads
   const int i0 = min(n, tid * run), i1 = min(n, i0 + run);
@@ -233,9 +235,11 @@ __device__ int emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int
   int te = 0;
   for (int i = i0; i < i1 && w < k; i++) {
     const uint32_t u = key_of(i);
-    if (u > tau || (u == tau && te++ < take_eq)) o[w++] = pos_of(i);
+    if (u > tau || (u == tau && te++ < take_eq)) stage[w++] = pos_of(i);
   }
-  return total;
+  __syncthreads();
+  const int got = min(total, k);  // below k only for rows with non-finite logits
+  for (int i = threadIdx.x; i < k; i += kThreads) o[i] = i < got ? stage[i] : -1;
 }
 
 // Block-wide min and max of uint32 keys in one barrier round; scratch holds 2 * kWarps.
@@ -307,7 +311,7 @@ __device__ void rank_bucket(int n, KeyFn key_of, InFn in_bucket, int nb, int rem
 
 // Exact selection over the whole row, read from global memory: the path for rows whose
 // candidate set came out too small or too large.
-__device__ void select_whole_row(const float* lg, int L, int k, int32_t* o, Shared& sh) {
+__device__ void select_whole_row(const float* lg, int L, int k, int32_t* o, Shared& sh, int32_t* stage) {
   const int tid = threadIdx.x;
   auto key_at = [&](int s) -> uint32_t { return order_key(__ldg(lg + s)); };
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
@@ -362,8 +366,7 @@ __device__ void select_whole_row(const float* lg, int L, int k, int32_t* o, Shar
   } else {
     radix_select(L, key_at, in_bucket, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
   }
-  const int got = emit_ordered(L, key_at, [](int s) { return s; }, sh.key, sh.take, o, k, sh.scratch64);
-  for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
+  emit_ordered(L, key_at, [](int s) { return s; }, sh.key, sh.take, o, k, sh.scratch64, stage);
 }
 
 
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __re
                                                                int32_t max_context, int32_t k, uint32_t* cand_key,
                                                                uint16_t* cand_pos, int64_t cstride,
                                                                int32_t* __restrict__ out, int32_t* status) {
-  extern __shared__ __align__(16) uint32_t dyn[];  // ckey[kCapB], then cpos[kCapB] (uint16)
+  extern __shared__ __align__(16) uint32_t dyn[];  // ckey[kCapB], cpos[kCapB] (uint16), stage[k]
   __shared__ Shared sh;
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
@@ -475,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __re
     return;
   }
   const float* lg = logits + row * stride;
+  int32_t* const stage = reinterpret_cast<int32_t*>(dyn + kCapB + kCapB / 2);  // after ckey and cpos
 
   // ---- 1. threshold from the row's fixed sample: 128 runs of 8 adjacent logits starting
   // at floor(r * L / 128) rounded down to 8 (single logits at floor(i * L / 1024) for
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __re
     m += total;
   }
   if (m < k) {  // the threshold was too high for this row: exact path over the whole row
-    select_whole_row(lg, L, k, o, sh);
+    select_whole_row(lg, L, k, o, sh, stage);
     return;
   }
 
@@ -612,8 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __re
   } else {
     radix_select(m, ck, in_b1, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
   }
-  const int got = emit_ordered(m, ck, cpos, sh.key, sh.take, o, k, sh.scratch64);
-  for (int i = got + tid; i < k; i += kThreads) o[i] = -1;  // only rows with non-finite logits
+  emit_ordered(m, ck, cpos, sh.key, sh.take, o, k, sh.scratch64, stage);
 }
 
 inline int64_t cand_stride(int32_t max_context) { return ((int64_t)max(max_context, 1) + 7) / 8 * 8; }
