@@ -174,9 +174,10 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
  * (logits_stride >= max_context; the rest of each row is not written).  fp4idx_topk
  * selects from such a buffer: topk_idx[t] = the k largest of logits[t][0..L_t), ascending
  * positions, -1 padding; ties at the k-th value go to the lower positions.  Its scratch
- * (per row, room for the candidate list when it does not fit in shared memory) lives in
- * `workspace`, at least fp4idx_topk_workspace_bytes(n_rows, max_context) bytes, 16-byte
- * aligned; nothing in it needs to be initialised.
+ * (per row, the sort keys of the positions past the first 32,768, which do not fit in
+ * shared memory; at least 256 bytes even when max_context <= 32768) lives in `workspace`,
+ * at least fp4idx_topk_workspace_bytes(n_rows, max_context) bytes, 16-byte aligned;
+ * nothing in it needs to be initialised.
  */
 int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows, int32_t n_heads,
                   const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
@@ -196,16 +197,17 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
  * fp4idx_topk a workspace; this entry point takes none.
  *
  * Same arguments and result as fp4idx_topk, without workspace/workspace_bytes.  The
- * candidate scratch is a fixed array of the library's device code,
+ * top-k scratch is a fixed array of the library's device code,
  * FP4IDX_TOPK_NOALLOC_MAX_BYTES per device; no call allocates or frees anything.
  *   - Limit: fp4idx_topk_workspace_bytes(n_rows, max_context) must not exceed
- *     FP4IDX_TOPK_NOALLOC_MAX_BYTES (up to 85 rows fit at max_context 32768, 42 at
- *     65536); a larger call returns FP4IDX_ERR_SCRATCH_LIMIT and enqueues nothing.
+ *     FP4IDX_TOPK_NOALLOC_MAX_BYTES (any row count fits at max_context <= 32768, up to
+ *     128 rows at 65536); a larger call returns FP4IDX_ERR_SCRATCH_LIMIT and enqueues
+ *     nothing.
  *   - Setup: the first valid call on each device (with that device current) looks up
  *     the array's address once; make that first call before any stream capture begins.
  *     Of the conventions at the top of this file, the one on graph capture is not
  *     stated for this entry point.
- *   - Nothing in the array needs to start at zero: a call writes every candidate it
+ *   - Nothing in the array needs to start at zero: a call writes every key it
  *     reads back.
  *   - All calls on a device share the array: calls whose kernels may overlap (unordered
  *     streams, concurrent host threads) race on it.  Order them on one stream.

@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     bool ok = true;
     while (ok && items.next(g, t0, t1)) {
       const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
-      const int32_t seq = __ldg(p.row_seq + r0);
+      const int32_t seq = sv.seq[g];  // row_seq of the group's rows, copied by the schedule
       const bool seq_ok = seq >= 0 && (int64_t)seq < p.num_seqs;
       int32_t maxlen = sv.maxlen[g];
       maxlen = min(maxlen, min(p.max_context, p.max_pages * kPage));

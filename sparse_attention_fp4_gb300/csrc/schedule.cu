@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
         mx = L > mx ? L : mx;
       }
       s.maxlen[g] = mx;
+      s.seq[g] = row_seq[r0];
       cost = ceil_div64(mx, kTileTokens) * (int64_t)(kTileCost + (r1 - r0));
     }
     int64_t tot;

@@ -33,6 +33,8 @@ struct SchedView {
   SchedHeader* hdr;
   int32_t* row0;     // [n_rows + 1] first row of each group (entry n_groups = n_rows)
   int32_t* maxlen;   // [n_rows] largest clamped context length in the group
+  int32_t* seq;      // [n_rows] the group's sequence (row_seq of its rows), so that a work
+                     // item's first page-table read need not wait on a row_seq load
   int64_t* prefix;   // [n_rows + 1] exclusive prefix of group costs
   int32_t* cta_g0;   // [num_ctas] first group whose cost interval ends after the CTA's range start
 };
@@ -41,6 +43,7 @@ __host__ __device__ inline size_t sched_align16(size_t x) { return (x + 15) & ~(
 
 __host__ __device__ inline size_t sched_bytes(int64_t n_rows, int64_t num_ctas) {
   size_t b = sched_align16(sizeof(SchedHeader));
+  b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
@@ -56,6 +59,8 @@ __host__ __device__ inline SchedView sched_view(void* base, int64_t n_rows) {
   v.row0 = reinterpret_cast<int32_t*>(p);
   p += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   v.maxlen = reinterpret_cast<int32_t*>(p);
+  p += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
+  v.seq = reinterpret_cast<int32_t*>(p);
   p += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   v.prefix = reinterpret_cast<int64_t*>(p);
   p += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));

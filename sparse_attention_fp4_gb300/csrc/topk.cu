@@ -6,23 +6,22 @@
 // context length 0 (their selection is empty: all -1).
 //
 // Selection = the k largest logits of a row, ties at the k-th value to the lower
-// positions, emitted in ascending position order.  One CTA of 512 threads per row and
-// no communication between CTAs (every hand-off between CTAs -- a global candidate list,
-// a fence and an arrival counter -- cost microseconds of latency on this path):
-//   1. a fixed sample of 1,024 of the row's logits (128 runs of 8 adjacent logits) gives
-//      a conservative threshold: a linear 256-bucket histogram of the sample, cut about
-//      four standard deviations beyond the expected place of the k-th largest;
-//   2. the row, 32 logits per thread held in registers (blocks of 16,384 tokens, read as
-//      float4 groups interleaved across the threads so that loads coalesce), is compacted
-//      in position order into the candidates at or above the threshold: in shared memory
-//      when they fit (kCapB), else in the caller's workspace;
-//   3. the candidates are bucketed linearly between their min and max (2,048 buckets),
-//      the boundary bucket is ranked exactly (radix select when it is crowded with
-//      ties), and the keys above the k-th plus the lowest-positioned equal ones are
-//      emitted in order.
-// The threshold is superset-closed (a value that passes lets every larger one pass), so
-// with at least k candidates they hold the whole answer: the sample decides speed, never
-// the result.  With fewer than k candidates the exact path runs over the whole row.
+// positions, emitted in ascending position order.  One CTA of 1,024 threads per row, no
+// communication between CTAs (every hand-off between CTAs -- a global candidate list, a
+// fence and an arrival counter -- cost microseconds of latency on this path), and an
+// exact plan with no sampling:
+//   1. the row is read once with coalesced 16-byte loads and turned into order-preserving
+//      uint32 keys.  They stay in shared memory (the first kRes of them; the rest of a
+//      longer row goes to the row's region of the caller's workspace), while a 4,096-bin
+//      histogram counts their top 12 bits (sign, exponent, three mantissa bits);
+//   2. a scan of the histogram from the top finds the bin B that holds the k-th largest
+//      key and how many of B's keys the selection still needs;
+//   3. two radix passes over the keys, each counting only the keys still in the running
+//      (10 + 10 low bits), resolve the k-th key tau and how many keys equal to tau are
+//      taken;
+//   4. one ordered pass emits every key above tau and the lowest-positioned keys equal to
+//      it: per thread a bit mask over a contiguous run of positions, one block scan of the
+//      mask counts, then the set bits are written out.
 #include "fp4idx_internal.cuh"
 
 #include <atomic>
@@ -30,21 +29,26 @@
 namespace fp4idx {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPer = 32;                      // logits a thread holds per block
-constexpr int kBlockTokens = kThreads * kPer; // 32,768
-constexpr int kCapB = 8192;                   // candidates kept in shared memory
-constexpr int kBins = 2048;
-constexpr int kBinsPerThread = kBins / kThreads;
-constexpr int kGather = 1024;                 // largest boundary bucket ranked by direct counting
-constexpr int kSample = 1024;                 // logits per row behind the candidate threshold
-constexpr int kSampleBins = 256;
-constexpr size_t kDynSmem = kCapB * (sizeof(uint32_t) + sizeof(uint16_t)) + FP4IDX_MAX_TOPK * sizeof(int32_t);
-constexpr int kSamplePer = kSample / kThreads;  // sample logits a thread loads
-static_assert(kSampleBins <= kThreads && kSample % kThreads == 0 && kBins % kThreads == 0 && kPer % 8 == 0,
-              "layout");
+constexpr int kRes = 32768;    // keys a CTA keeps in shared memory
+constexpr int kHistBits = 12;  // top bits of the key counted by the first histogram
+constexpr int kHist = 1 << kHistBits;
+constexpr int kLowBits = 32 - kHistBits;  // bits the radix passes resolve inside bin B
+constexpr int kDigitBits = kLowBits / 2;
+constexpr int kDigits = 1 << kDigitBits;
+constexpr int kU = 8;                 // 16-byte loads in flight per thread
+constexpr int kEmitGroups = 8192;     // groups of four positions per emit block (<= 36 mask bits a thread)
+static_assert(kWarps == 32 && kHist % (32 * kWarps) == 0 && kDigits == kThreads, "layout");
+static_assert(kLowBits == 2 * kDigitBits, "two digit passes");
+static_assert(kHist >= FP4IDX_MAX_TOPK, "the histogram doubles as the output stage");
+static_assert(4 * kEmitGroups <= 65535, "16-bit block counts in the emit scan");
 constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Dynamic shared memory: hist[kHist] (int; reused as the stage of the k outputs), then
+// keys[res].
+constexpr size_t kFixedSmem = kHist * sizeof(int);
+static_assert(kFixedSmem % 16 == 0, "keys start 16-byte aligned");
 
 // Order-preserving key; -0 maps to +0 so that equal values are equal keys.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -52,419 +56,206 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
+struct Shared {
+  uint32_t scratch[kWarps];
+  int bin, rem;
+};
 
-// Linear bucket of value x over [lo, lo + 2047/scale]; scale = 0 puts everything in bucket 0.
-__device__ __forceinline__ int lin_bucket(float x, float lo, float scale) {
-  const float v = (x - lo) * scale;
-  if (!(v >= 0.0f)) return 0;  // also NaN
-  return v >= (float)(kBins - 1) ? kBins - 1 : (int)v;
-}
-
-__device__ __forceinline__ float lin_scale(float lo, float hi) {
-  const float range = hi - lo;
-  return (range > 0.0f && range < INFINITY) ? (float)(kBins - 1) / range : 0.0f;
-}
-
-// Exclusive block scan of an int; `total` gets the block sum.
-__device__ __forceinline__ int block_excl_scan(int v, int* scratch, int& total) {
+// Exclusive block scan of a uint32 (sums wrap modulo 2^32); `total` gets the block sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch, uint32_t& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  uint32_t x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(kFull, x, o);
+    const uint32_t n = __shfl_up_sync(kFull, x, o);
     if (lane >= o) x += n;
   }
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    int w = lane < kWarps ? scratch[lane] : 0;
+  uint32_t w = scratch[lane];  // kWarps == 32: every warp scans the warp sums itself
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += n;
-    }
-    if (lane < kWarps) scratch[lane] = w;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(kFull, w, o);
+    if (lane >= o) w += n;
   }
-  __syncthreads();
-  const int before = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
-  total = scratch[kWarps - 1];
-  __syncthreads();
+  const uint32_t before = __shfl_sync(kFull, w, warp) - scratch[warp] + x - v;
+  total = __shfl_sync(kFull, w, 31);
+  __syncthreads();  // scratch may be reused
   return before;
 }
 
-template <bool kMax>
-__device__ __forceinline__ uint32_t block_reduce(uint32_t v, uint32_t* scratch) {
+// Over kPerLane * 32 * kWarps bins counted from the top (warp 0, lane 0 own the highest
+// bins): the bin that holds the rank-th largest element (1 <= rank <= the total) into
+// sh.bin, and rank minus the elements in the bins above it into sh.rem.  Two barriers;
+// the last one makes the result visible to the whole CTA.
+template <int kPerLane>
+__device__ __forceinline__ void find_bin_from_top(const int* counts, int rank, Shared& sh) {
+  static_assert(kPerLane == 1 || kPerLane == 4, "one or four bins a lane");
+  constexpr int kPerWarp = kPerLane * 32;
+  constexpr int kBins = kPerWarp * kWarps;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint32_t n = __shfl_xor_sync(kFull, v, o);
-    v = kMax ? max(v, n) : min(v, n);
+  const int lo = kBins - warp * kPerWarp - (lane + 1) * kPerLane;  // this lane's lowest bin
+  int c[kPerLane];
+  if constexpr (kPerLane == 4) {
+    const int4 v = *reinterpret_cast<const int4*>(counts + lo);
+    c[0] = v.x;
+    c[1] = v.y;
+    c[2] = v.z;
+    c[3] = v.w;
+  } else {
+    c[0] = counts[lo];
   }
-  if (lane == 0) scratch[warp] = v;
+  int s = 0;
+#pragma unroll
+  for (int j = 0; j < kPerLane; j++) s += c[j];
+  int x = s;  // inclusive scan from the top lane down
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) sh.scratch[warp] = (uint32_t)x;
   __syncthreads();
-  uint32_t r = scratch[0];
-  for (int i = 1; i < kWarps; i++) r = kMax ? max(r, scratch[i]) : min(r, scratch[i]);
+  const int ws = (int)sh.scratch[lane];
+  int wx = ws;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, wx, o);
+    if (lane >= o) wx += n;
+  }
+  const unsigned hit = __ballot_sync(kFull, wx - ws < rank && rank <= wx);
+  const int W = __ffs(hit) - 1;  // the warp whose bins hold the rank-th element
+  if (warp == W) {
+    const int above = __shfl_sync(kFull, wx - ws, W) + x - s;
+    if (above < rank && rank <= above + s) {
+      int acc = above;
+#pragma unroll
+      for (int j = kPerLane - 1; j >= 0; j--) {
+        if (acc < rank && rank <= acc + c[j]) {
+          sh.bin = lo + j;
+          sh.rem = rank - acc;
+        }
+        acc += c[j];
+      }
+    }
+  }
   __syncthreads();
+}
+
+// This thread's group v of four logits (positions 4v .. 4v+3); past L reads nothing.
+__device__ __forceinline__ float4 load_group(const float* lg, bool vec, int v, int L) {
+  const int i = 4 * v;
+  if (vec && i + 4 <= L) return __ldg(reinterpret_cast<const float4*>(lg) + v);
+  float4 r;
+  r.x = i < L ? __ldg(lg + i) : 0.0f;
+  r.y = i + 1 < L ? __ldg(lg + i + 1) : 0.0f;
+  r.z = i + 2 < L ? __ldg(lg + i + 2) : 0.0f;
+  r.w = i + 3 < L ? __ldg(lg + i + 3) : 0.0f;
   return r;
 }
 
-// Thread whose run of histogram bins (taken from the top) contains the rem-th largest
-// element writes (bin, rem - elements above the bin).
-__device__ __forceinline__ void find_bin_from_top(const int* counts, int rem, int* scratch, int* out_bin,
-                                                  int* out_rem) {
-  const int tb = (kThreads - 1 - (int)threadIdx.x) * kBinsPerThread;
-  int mine = 0;
-#pragma unroll
-  for (int j = 0; j < kBinsPerThread; j++) mine += counts[tb + j];
-  int tot;
-  const int above = block_excl_scan(mine, scratch, tot);
-  if (above < rem && rem <= above + mine) {
-    int acc = above;
-    for (int j = kBinsPerThread - 1; j >= 0; j--) {
-      const int c = counts[tb + j];
-      if (acc < rem && rem <= acc + c) {
-        *out_bin = tb + j;
-        *out_rem = rem - acc;
-        break;
-      }
-      acc += c;
-    }
+// The row's keys: positions below res in shared memory, the rest in the row's spill
+// region of the workspace (res is a multiple of 4, so a group of four is in one place).
+struct RowKeys {
+  uint32_t* sm;
+  uint32_t* spill;
+  int res;
+  __device__ __forceinline__ uint4 get(int v) const {
+    const int i = 4 * v;
+    if (i < res) return *reinterpret_cast<const uint4*>(sm + i);
+    return __ldcg(reinterpret_cast<const uint4*>(spill + (i - res)));
   }
-  __syncthreads();
-}
-
-// Radix select (11 + 11 + 10 bits, warp-aggregated shared-memory atomics) over the elements
-// i < n with member(i): the key of the rem-th largest and how many elements equal to it a
-// selection of rem must take.  Results in *tau, *take (shared).
-template <class KeyFn, class MemberFn>
-__device__ void radix_select(int n, KeyFn key_of, MemberFn member, int rem, int* hist, int* scratch, int* sh_bin,
-                             int* sh_rem, uint32_t* tau, int* take) {
-  const int tid = threadIdx.x;
-  uint32_t prefix = 0, pmask = 0;
-  int r = rem;
-#pragma unroll 1
-  for (int pass = 0; pass < 3; pass++) {
-    const int dshift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
-    for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += kThreads) {
-      const int i = i0 + tid;
-      bool in = false;
-      uint32_t digit = 0;
-      if (i < n && member(i)) {
-        const uint32_t u = key_of(i);
-        in = (u & pmask) == prefix;
-        digit = (u >> dshift) & dmask;
-      }
-      const unsigned active = __ballot_sync(kFull, in);
-      if (in) {
-        const unsigned peers = __match_any_sync(active, digit);
-        if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
-      }
-    }
-    __syncthreads();
-    find_bin_from_top(hist, r, scratch, sh_bin, sh_rem);
-    prefix |= (uint32_t)*sh_bin << dshift;
-    pmask |= dmask << dshift;
-    r = *sh_rem;
-    __syncthreads();
+  __device__ __forceinline__ void put(int v, uint4 q) const {
+    const int i = 4 * v;
+    if (i < res) *reinterpret_cast<uint4*>(sm + i) = q;
+    else *reinterpret_cast<uint4*>(spill + (i - res)) = q;
   }
-  if (tid == 0) {
-    *tau = prefix;
-    *take = r;
-  }
-  __syncthreads();
-}
-
-// Emit, in index order, every element i < n whose key is above tau and the first
-// take_total (in index order) whose key equals tau: o[...] = pos_of(i).  Each thread owns a
-// contiguous run of indices; two block scans give the output offsets.  Returns the count.
-// Exclusive block scan of a 64-bit value; `total` gets the block sum.
-__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t* scratch, uint64_t& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t n = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += n;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint64_t w = lane < kWarps ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint64_t n = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += n;
-    }
-    if (lane < kWarps) scratch[lane] = w;
-  }
-  __syncthreads();
-  const uint64_t before = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
-  total = scratch[kWarps - 1];
-  __syncthreads();
-  return before;
-}
-
-// Writes o[0..k): the selected positions in index order, then -1.  They are staged in
-// shared memory (`stage`, k entries) and copied out with coalesced stores.
-template <class KeyFn, class PosFn>
-__device__ void emit_ordered(int n, KeyFn key_of, PosFn pos_of, uint32_t tau, int take_total, int32_t* o, int k,
-                             uint64_t* scratch, int32_t* stage) {
-  const int tid = threadIdx.x;
-  const int run = ((n + kThreads - 1) / kThreads) | 1;  // odd stride: conflict-free reads
-  const int i0 = min(n, tid * run), i1 = min(n, i0 + run);
-  int gt = 0, eq = 0;
-  for (int i = i0; i < i1; i++) {
-    const uint32_t u = key_of(i);
-    gt += u > tau;
-    eq += u == tau;
-  }
-  // one scan of (greater, equal) counts: the equal keys are taken greedily in index
-  // order, so the keys equal to tau taken before this thread's run are min(E, take)
-  uint64_t tot;
-  const uint64_t pre = block_excl_scan64(((uint64_t)gt << 32) | (uint32_t)eq, scratch, tot);
-  const int G = (int)(pre >> 32), E = (int)(uint32_t)pre;
-  const int take_eq = max(0, min(eq, take_total - E));
-  int w = G + min(E, take_total);
-  const int total = (int)(tot >> 32) + min((int)(uint32_t)tot, take_total);
-  int te = 0;
-  for (int i = i0; i < i1 && w < k; i++) {
-    const uint32_t u = key_of(i);
-    if (u > tau || (u == tau && te++ < take_eq)) stage[w++] = pos_of(i);
-  }
-  __syncthreads();
-  const int got = min(total, k);  // below k only for rows with non-finite logits
-  for (int i = threadIdx.x; i < k; i += kThreads) o[i] = i < got ? stage[i] : -1;
-}
-
-// Block-wide min and max of uint32 keys in one barrier round; scratch holds 2 * kWarps.
-__device__ __forceinline__ void block_minmax(uint32_t& mn, uint32_t& mx, uint32_t* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(kFull, mn, o));
-    mx = max(mx, __shfl_xor_sync(kFull, mx, o));
-  }
-  if (lane == 0) {
-    scratch[warp] = mn;
-    scratch[kWarps + warp] = mx;
-  }
-  __syncthreads();
-  mn = scratch[0];
-  mx = scratch[kWarps];
-#pragma unroll
-  for (int i = 1; i < kWarps; i++) {
-    mn = min(mn, scratch[i]);
-    mx = max(mx, scratch[kWarps + i]);
-  }
-  __syncthreads();
-}
-
-struct Shared {
-  uint32_t wsum[kWarps][kPer / 8];
-  uint32_t gsum[kPer / 8];
-  uint64_t scratch64[kWarps];
-  int hist[kBins];
-  uint32_t gkey[kGather];
-  int gidx[kGather];
-  int scratch[kWarps];
-  uint32_t uscratch[2 * kWarps];
-  int bin, rem, gcount, take, blo, last;
-  uint32_t key;
 };
 
-// Members of the boundary bucket (nb <= kGather of them, keys from key_of) ranked by
-// direct counting: sets sh.key to the rem-th largest and sh.take to how many keys equal
-// to it the selection takes.  `in_bucket(i)` says whether element i is a member.
-template <class KeyFn, class InFn>
-__device__ void rank_bucket(int n, KeyFn key_of, InFn in_bucket, int nb, int rem, Shared& sh) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < n; i += kThreads) {
-    if (in_bucket(i)) {
-      const int slot = atomicAdd(&sh.gcount, 1);
-      sh.gkey[slot] = key_of(i);
-      sh.gidx[slot] = i;
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < nb; i += kThreads) {
-    const uint32_t ki = sh.gkey[i];
-    const int ii = sh.gidx[i];
-    int rk = 0, gt = 0;
-    for (int j = 0; j < nb; j++) {
-      const uint32_t kj = sh.gkey[j];
-      gt += kj > ki;
-      rk += (kj > ki) || (kj == ki && sh.gidx[j] < ii);
-    }
-    if (rk == rem - 1) {
-      sh.key = ki;
-      sh.take = rem - gt;
-    }
-  }
-  __syncthreads();
+__device__ __forceinline__ uint32_t lane_of(const uint4& q, int e) {
+  return e == 0 ? q.x : (e == 1 ? q.y : (e == 2 ? q.z : q.w));
 }
 
-// Exact selection over the whole row, read from global memory: the path for rows whose
-// candidate set came out too small or too large.
-__device__ void select_whole_row(const float* lg, int L, int k, int32_t* o, Shared& sh, int32_t* stage) {
+// One radix pass: per digit (key >> shift) & (kDigits - 1), the number of the row's keys
+// whose bits from match_shift up equal `match`.  Ends with the digit picked for `rank`.
+__device__ __forceinline__ void digit_pass(const RowKeys& keys, int L, int ng, uint32_t match, int match_shift,
+                                           int shift, int rank, int* hist, Shared& sh) {
   const int tid = threadIdx.x;
-  auto key_at = [&](int s) -> uint32_t { return order_key(__ldg(lg + s)); };
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int s = tid; s < L; s += kThreads) {
-    const uint32_t u = key_at(s);
-    kmin = min(kmin, u);
-    kmax = max(kmax, u);
-  }
-  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
-  if (tid == 0) sh.gcount = 0;
-  block_minmax(kmin, kmax, sh.uscratch);
-  const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
-  for (int s = tid; s < L; s += kThreads) atomicAdd(&sh.hist[lin_bucket(key_value(key_at(s)), lo1, sc1)], 1);
+  hist[tid] = 0;  // kDigits == kThreads
   __syncthreads();
-  find_bin_from_top(sh.hist, k, sh.scratch, &sh.bin, &sh.rem);
-  const int b1 = sh.bin;
-  int rem = sh.rem;
-  int nb = sh.hist[b1];
-  __syncthreads();  // every thread has read nb before any path clears the histogram
-  float lo2 = 0.0f, sc2 = 0.0f;
-  int b2 = -1;
-  if (nb > kGather) {  // refine a crowded bucket over its own value range
-    uint32_t bmin = 0xFFFFFFFFu, bmax = 0u;
-    for (int s = tid; s < L; s += kThreads) {
-      const uint32_t u = key_at(s);
-      if (lin_bucket(key_value(u), lo1, sc1) == b1) {
-        bmin = min(bmin, u);
-        bmax = max(bmax, u);
+#pragma unroll 4
+  for (int v = tid; v < ng; v += kThreads) {
+    const uint4 q = keys.get(v);
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const uint32_t u = lane_of(q, e);
+      if ((u >> match_shift) == match && 4 * v + e < L) atomicAdd(&hist[(u >> shift) & (kDigits - 1)], 1);
+    }
+  }
+  __syncthreads();
+  find_bin_from_top<1>(hist, rank, sh);
+}
+
+// Writes o[0..k): every position i < L whose key is above tau and the first take_total
+// (by position) whose key equals tau, ascending, then -1.  Positions go in blocks of
+// kEmitGroups groups of four; in a block each thread owns a contiguous run of groups (an
+// odd number of them, so that the 16-byte shared-memory reads of a quarter warp hit
+// distinct banks) and marks its keys above tau and equal to tau in two bit masks.  One
+// block scan of the packed mask counts gives the output offsets.  The positions are
+// staged in `stage` (k ints) and copied out coalesced.
+__device__ void emit_ordered(const RowKeys& keys, int L, int ng, uint32_t tau, int take_total, int32_t* o, int k,
+                             Shared& sh, int32_t* stage) {
+  const int tid = threadIdx.x;
+  int g_done = 0, e_done = 0;  // keys above / equal to tau in earlier blocks
+  for (int b0 = 0; b0 < ng; b0 += kEmitGroups) {
+    const int nbg = min(kEmitGroups, ng - b0);
+    const int run = ((nbg + kThreads - 1) / kThreads) | 1;
+    const int g0 = b0 + min(nbg, tid * run), g1 = b0 + min(nbg, tid * run + run);
+    uint64_t gtm = 0, eqm = 0;
+    for (int g = g0; g < g1; g++) {
+      const uint4 q = keys.get(g);
+      const int bit = 4 * (g - g0);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        const uint32_t u = lane_of(q, e);
+        const bool in = 4 * g + e < L;
+        gtm |= (uint64_t)(in && u > tau) << (bit + e);
+        eqm |= (uint64_t)(in && u == tau) << (bit + e);
       }
     }
-    for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
-    block_minmax(bmin, bmax, sh.uscratch);
-    lo2 = key_value(bmin);
-    sc2 = lin_scale(lo2, key_value(bmax));
-    for (int s = tid; s < L; s += kThreads) {
-      const float x = key_value(key_at(s));
-      if (lin_bucket(x, lo1, sc1) == b1) atomicAdd(&sh.hist[lin_bucket(x, lo2, sc2)], 1);
+    const int gt = __popcll(gtm), eq = __popcll(eqm);
+    uint32_t tot;  // gt in the low 16 bits, eq in the high 16 (a block has at most 32,768 keys)
+    const uint32_t pre = block_excl_scan((uint32_t)gt | ((uint32_t)eq << 16), sh.scratch, tot);
+    const int G = g_done + (int)(pre & 0xFFFFu), E = e_done + (int)(pre >> 16);
+    // the keys equal to tau are taken greedily in position order: keep this run's first
+    // take_eq of them
+    const int take_eq = max(0, min(eq, take_total - E));
+    for (int drop = eq - take_eq; drop > 0; drop--) eqm &= ~(1ull << (63 - __clzll(eqm)));
+    uint64_t sel = gtm | eqm;
+    int w = G + min(E, take_total);
+    while (sel) {
+      const int b = __ffsll(sel) - 1;
+      sel &= sel - 1;
+      if (w < k) stage[w] = 4 * g0 + b;
+      w++;
     }
-    __syncthreads();
-    find_bin_from_top(sh.hist, rem, sh.scratch, &sh.bin, &sh.rem);
-    b2 = sh.bin;
-    rem = sh.rem;
-    nb = sh.hist[b2];
-    __syncthreads();
-  }
-  auto in_bucket = [&](int s) -> bool {
-    const float x = key_value(key_at(s));
-    return lin_bucket(x, lo1, sc1) == b1 && (b2 < 0 || lin_bucket(x, lo2, sc2) == b2);
-  };
-  if (nb <= kGather) {
-    rank_bucket(L, key_at, in_bucket, nb, rem, sh);
-  } else {
-    radix_select(L, key_at, in_bucket, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
-  }
-  emit_ordered(L, key_at, [](int s) { return s; }, sh.key, sh.take, o, k, sh.scratch64, stage);
-}
-
-
-constexpr int kGroups = kPer / 4;  // float4 groups a thread holds per block
-
-// Position of element e of this thread's group j in a block starting at `base`: groups are
-// interleaved across the threads (group j of thread t covers base + 4*(j*kThreads + t)),
-// so each warp-wide 16-byte load reads 512 contiguous bytes.
-__device__ __forceinline__ int elem_pos(int base, int j, int e) {
-  return base + 4 * (j * kThreads + (int)threadIdx.x) + e;
-}
-
-// This thread's kPer logits of the block starting at `base`; past L reads nothing and
-// yields 0.
-__device__ __forceinline__ void load_block(const float* lg, int base, int L, float* x) {
-  const bool vec = (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
-#pragma unroll
-  for (int j = 0; j < kGroups; j++) {
-    const int p0 = elem_pos(base, j, 0);
-    if (vec && p0 + 4 <= L) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(lg + p0));
-      x[4 * j] = v.x;
-      x[4 * j + 1] = v.y;
-      x[4 * j + 2] = v.z;
-      x[4 * j + 3] = v.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; e++) x[4 * j + e] = p0 + e < L ? __ldg(lg + p0 + e) : 0.0f;
-    }
-  }
-}
-
-// Exclusive prefix, in (group, thread) order, of this thread's per-group counts c[j]
-// (each at most 4): off[j] = sum of all counts of groups before j plus those of lower
-// threads in group j.  Counts travel two to a register in 16-bit halves (a block total
-// is at most 4 * kThreads = 4096).  Returns the block total.
-__device__ __forceinline__ int group_scan(const int* c, int* off, uint32_t (*wsum)[kGroups / 2], uint32_t* gsum) {
-  constexpr int P = kGroups / 2;
-  static_assert(kWarps <= 32, "one warp scans the warp sums");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t v[P], x[P];
-#pragma unroll
-  for (int i = 0; i < P; i++) x[i] = v[i] = (uint32_t)c[2 * i] | ((uint32_t)c[2 * i + 1] << 16);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-    for (int i = 0; i < P; i++) {
-      const uint32_t n = __shfl_up_sync(kFull, x[i], o);
-      if (lane >= o) x[i] += n;
-    }
-  }
-  if (lane == 31) {
-#pragma unroll
-    for (int i = 0; i < P; i++) wsum[warp][i] = x[i];
+    g_done += (int)(tot & 0xFFFFu);
+    e_done += (int)(tot >> 16);
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive scan of the kWarps warp sums; gsum = per-group block totals
-    uint32_t y[P], z[P];
-#pragma unroll
-    for (int i = 0; i < P; i++) z[i] = y[i] = lane < kWarps ? wsum[lane][i] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-      for (int i = 0; i < P; i++) {
-        const uint32_t n = __shfl_up_sync(kFull, z[i], o);
-        if (lane >= o) z[i] += n;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < P; i++) {
-      if (lane < kWarps) wsum[lane][i] = z[i] - y[i];
-      if (lane == kWarps - 1) gsum[i] = z[i];
-    }
-  }
-  __syncthreads();
-  int base = 0;
-#pragma unroll
-  for (int i = 0; i < P; i++) {
-    const uint32_t pre = x[i] - v[i] + wsum[warp][i];  // within-group exclusive prefix, packed
-    const uint32_t tot = gsum[i];
-    off[2 * i] = base + (int)(pre & 0xFFFFu);
-    base += (int)(tot & 0xFFFFu);
-    off[2 * i + 1] = base + (int)(pre >> 16);
-    base += (int)(tot >> 16);
-  }
-  __syncthreads();  // wsum / gsum may be reused
-  return base;
+  const int got = min(g_done + min(e_done, take_total), k);  // equal to k whenever L > k
+  for (int i = tid; i < k; i += kThreads) o[i] = i < got ? stage[i] : -1;
 }
 
-// One CTA per row.  cand_key/cand_pos + row * cstride: the row's region of the workspace,
-// used when its candidates do not fit in shared memory.
-__global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __restrict__ logits, int64_t stride,
-                                                               const int32_t* __restrict__ context_lens,
-                                                               int32_t max_context, int32_t k, uint32_t* cand_key,
-                                                               uint16_t* cand_pos, int64_t cstride,
-                                                               int32_t* __restrict__ out, int32_t* status) {
-  extern __shared__ __align__(16) uint32_t dyn[];  // ckey[kCapB], cpos[kCapB] (uint16), stage[k]
+// One CTA per row.  keys[0..res) of the row stay in shared memory (res a multiple of 4);
+// spill + row * sstride holds the keys of positions res and up (sstride a multiple of 4).
+__global__ void __launch_bounds__(kThreads, 1)
+    topk_row_kernel(const float* __restrict__ logits, int64_t stride, const int32_t* __restrict__ context_lens,
+                    int32_t max_context, int32_t k, int32_t res, uint32_t* spill, int64_t sstride,
+                    int32_t* __restrict__ out, int32_t* status) {
+  extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Shared sh;
+  int* const hist = reinterpret_cast<int*>(dyn);
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
   int32_t L = __ldg(context_lens + row);
@@ -478,158 +269,77 @@ __global__ void __launch_bounds__(kThreads, 1) topk_row_kernel(const float* __re
     return;
   }
   const float* lg = logits + row * stride;
-  int32_t* const stage = reinterpret_cast<int32_t*>(dyn + kCapB + kCapB / 2);  // after ckey and cpos
+  const bool vec = (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
+  const int ng = (L + 3) >> 2;
+  const RowKeys keys{dyn + kHist, spill + row * sstride, res};
 
-  // ---- 1. threshold from the row's fixed sample: 128 runs of 8 adjacent logits starting
-  // at floor(r * L / 128) rounded down to 8 (single logits at floor(i * L / 1024) for
-  // rows shorter than 1024)
-  float sv[kSamplePer];
+  // ---- 1. keys and the top-bits histogram; the first loads are issued before the
+  // histogram is cleared
+  float4 r[kU];
 #pragma unroll
-  for (int j = 0; j < kSamplePer; j++) {
-    const int i = j * kThreads + tid;
-    const int sp = L >= kSample ? (((int)(((int64_t)(i >> 3) * L) / (kSample / 8)) & ~7) + (i & 7))
-                                : (int)(((int64_t)i * L) / kSample);
-    sv[j] = __ldg(lg + sp);
+  for (int u = 0; u < kU; u++) {
+    const int v = u * kThreads + tid;
+    if (v < ng) r[u] = load_group(lg, vec, v, L);
   }
-  float x[kPer];
-  load_block(lg, 0, L, x);  // issued before the threshold is known
-  if (tid < kSampleBins) sh.hist[tid] = 0;
-  uint32_t smin = 0xFFFFFFFFu, smax = 0u;
-#pragma unroll
-  for (int j = 0; j < kSamplePer; j++) {
-    smin = min(smin, order_key(sv[j]));
-    smax = max(smax, order_key(sv[j]));
-  }
-  block_minmax(smin, smax, sh.uscratch);  // its barriers also order the histogram clear
-  const float lo = key_value(smin);
-  const float sc = lin_scale(lo, key_value(smax)) * ((float)kSampleBins / (float)kBins);
-  auto sbucket = [&](float v) -> int {
-    const int b = lin_bucket(v, lo, sc);
-    return b >= kSampleBins ? kSampleBins - 1 : b;
-  };
-#pragma unroll
-  for (int j = 0; j < kSamplePer; j++) atomicAdd(&sh.hist[sbucket(sv[j])], 1);
+  for (int b = tid; b < kHist; b += kThreads) hist[b] = 0;
   __syncthreads();
-  // keep the sample's expected share of k plus four standard deviations
-  const float q = (float)k / (float)L;
-  const float mean = q * (float)kSample;
-  const int need = min(kSample, (int)ceilf(mean + 4.0f * sqrtf(mean * (1.0f - q)) + 8.0f));
-  const int mine = tid < kSampleBins ? sh.hist[kSampleBins - 1 - tid] : 0;
-  int tot;
-  const int above = block_excl_scan(mine, sh.scratch, tot);
-  if (tid < kSampleBins && above < need && need <= above + mine) sh.blo = kSampleBins - 1 - tid;
-  __syncthreads();
-  const int blo = sh.blo;
-  // the cut as a key: bucket blo starts at lo + blo / sc.  Any key threshold keeps the
-  // candidate set superset-closed, so the rounding of this edge cannot change the result.
-  const uint32_t kthr = (blo == 0 || !(sc > 0.0f)) ? 0u : order_key(lo + (float)blo / sc);
-
-  // ---- 2. order-preserving compaction of the candidates, block by block.  Candidate i
-  // lives in shared memory for i < kCapB and in the row's workspace region beyond.
-  uint32_t* const ckey_s = dyn;
-  uint16_t* const cpos_s = reinterpret_cast<uint16_t*>(dyn + kCapB);
-  uint32_t* const ckey_g = cand_key + row * cstride;
-  uint16_t* const cpos_g = cand_pos + row * cstride;
-  const int nblocks = (L + kBlockTokens - 1) / kBlockTokens;
-  int m = 0;
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int blk = 0; blk < nblocks; blk++) {
-    const int base = blk * kBlockTokens;
-    if (blk > 0) load_block(lg, base, L, x);
-    unsigned flags = 0;
-    int cnt[kGroups], off[kGroups];
+  for (int v0 = 0; v0 < ng; v0 += kU * kThreads) {
 #pragma unroll
-    for (int j = 0; j < kGroups; j++) {
-      const int p0 = elem_pos(base, j, 0);
-      cnt[j] = 0;
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        const bool in = p0 + e < L && order_key(x[4 * j + e]) >= kthr;
-        flags |= (unsigned)in << (4 * j + e);
-        cnt[j] += in;
+    for (int u = 0; u < kU; u++) {
+      const int v = v0 + u * kThreads + tid;
+      if (v < ng) {
+        const uint4 q = make_uint4(order_key(r[u].x), order_key(r[u].y), order_key(r[u].z), order_key(r[u].w));
+        keys.put(v, q);
+        const int i = 4 * v;
+        atomicAdd(&hist[q.x >> kLowBits], 1);
+        if (i + 1 < L) atomicAdd(&hist[q.y >> kLowBits], 1);
+        if (i + 2 < L) atomicAdd(&hist[q.z >> kLowBits], 1);
+        if (i + 3 < L) atomicAdd(&hist[q.w >> kLowBits], 1);
       }
     }
-    const int total = group_scan(cnt, off, sh.wsum, sh.gsum);
-    if (m + total <= kCapB) {  // the common case, uniform over the CTA: branch-free stores
+    const int vn = v0 + kU * kThreads;
+    if (vn < ng) {
 #pragma unroll
-      for (int j = 0; j < kGroups; j++) {
-        int w = m + off[j];
-        const int p0 = elem_pos(base, j, 0);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const bool in = (flags >> (4 * j + e)) & 1u;
-          const uint32_t u = order_key(x[4 * j + e]);
-          if (in) {
-            ckey_s[w] = u;
-            cpos_s[w] = (uint16_t)(p0 + e);  // positions < FP4IDX_MAX_CONTEXT = 65536
-          }
-          kmin = min(kmin, in ? u : 0xFFFFFFFFu);
-          kmax = max(kmax, in ? u : 0u);
-          w += in;
-        }
-      }
-    } else {  // candidates past kCapB go to the row's workspace region
-#pragma unroll
-      for (int j = 0; j < kGroups; j++) {
-        int w = m + off[j];
-        const int p0 = elem_pos(base, j, 0);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-          if (flags & (1u << (4 * j + e))) {
-            const uint32_t u = order_key(x[4 * j + e]);
-            if (w < kCapB) {
-              ckey_s[w] = u;
-              cpos_s[w] = (uint16_t)(p0 + e);
-            } else {
-              ckey_g[w] = u;
-              cpos_g[w] = (uint16_t)(p0 + e);
-            }
-            kmin = min(kmin, u);
-            kmax = max(kmax, u);
-            w++;
-          }
-        }
+      for (int u = 0; u < kU; u++) {
+        const int v = vn + u * kThreads + tid;
+        if (v < ng) r[u] = load_group(lg, vec, v, L);
       }
     }
-    m += total;
   }
-  if (m < k) {  // the threshold was too high for this row: exact path over the whole row
-    select_whole_row(lg, L, k, o, sh, stage);
-    return;
-  }
-
-  // ---- 3. selection among the candidates (m >= k)
-  for (int b = tid; b < kBins; b += kThreads) sh.hist[b] = 0;
-  if (tid == 0) sh.gcount = 0;
-  block_minmax(kmin, kmax, sh.uscratch);  // its barriers also publish the candidates
-  const float lo1 = key_value(kmin), sc1 = lin_scale(lo1, key_value(kmax));
-  auto ck = [&](int i) -> uint32_t { return i < kCapB ? ckey_s[i] : __ldcg(ckey_g + i); };
-  auto cpos = [&](int i) -> int { return i < kCapB ? (int)cpos_s[i] : (int)__ldcg(cpos_g + i); };
-  for (int i = tid; i < m; i += kThreads) atomicAdd(&sh.hist[lin_bucket(key_value(ck(i)), lo1, sc1)], 1);
   __syncthreads();
-  find_bin_from_top(sh.hist, k, sh.scratch, &sh.bin, &sh.rem);
-  const int b1 = sh.bin, rem = sh.rem, nb = sh.hist[b1];
-  __syncthreads();  // every thread has read nb before the radix path clears the histogram
-  auto in_b1 = [&](int i) -> bool { return lin_bucket(key_value(ck(i)), lo1, sc1) == b1; };
-  if (nb <= kGather) {
-    rank_bucket(m, ck, in_b1, nb, rem, sh);
-  } else {
-    radix_select(m, ck, in_b1, rem, sh.hist, sh.scratch, &sh.bin, &sh.rem, &sh.key, &sh.take);
-  }
-  emit_ordered(m, ck, cpos, sh.key, sh.take, o, k, sh.scratch64, stage);
+
+  // ---- 2. the bin holding the k-th largest key
+  find_bin_from_top<kHist / (32 * kWarps)>(hist, k, sh);
+  const uint32_t B = (uint32_t)sh.bin;
+  const int rem = sh.rem;
+
+  // ---- 3. two radix passes inside bin B
+  digit_pass(keys, L, ng, B, kLowBits, kDigitBits, rem, hist, sh);
+  const uint32_t d1 = (uint32_t)sh.bin;
+  const int rem1 = sh.rem;
+  const uint32_t hi22 = (B << kDigitBits) | d1;
+  digit_pass(keys, L, ng, hi22, kDigitBits, 0, rem1, hist, sh);
+  const uint32_t tau = (hi22 << kDigitBits) | (uint32_t)sh.bin;
+  const int take = sh.rem;
+
+  // ---- 4. ordered emit (the histogram's space becomes the output stage)
+  emit_ordered(keys, L, ng, tau, take, o, k, sh, hist);
 }
 
-inline int64_t cand_stride(int32_t max_context) { return ((int64_t)max(max_context, 1) + 7) / 8 * 8; }
+inline int64_t spill_stride(int32_t max_context) {
+  return max((int64_t)0, ((int64_t)max(max_context, 1) + 3) / 4 * 4 - kRes);
+}
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 std::atomic<bool> g_attr_done[64];
 
 }  // namespace
 
-// Workspace: per row, a spill region for its candidate keys (u32) and positions (u16).
+// Workspace: per row, the keys of positions past the kRes a CTA keeps in shared memory
+// (none when max_context <= kRes; the size is still at least 256 bytes).  Nothing in it
+// needs to be initialised.
 size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context) {
-  const size_t cells = (size_t)n_rows * (size_t)cand_stride(max_context);
-  return align256(cells * sizeof(uint32_t)) + align256(cells * sizeof(uint16_t));
+  return align256(max((size_t)1, (size_t)n_rows * (size_t)spill_stride(max_context) * sizeof(uint32_t)));
 }
 
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
@@ -640,15 +350,16 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !g_attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kFixedSmem + kRes * sizeof(uint32_t)));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) g_attr_done[dev].store(true);
   }
-  const size_t cells = (size_t)n_rows * (size_t)cand_stride(max_context);
-  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  topk_row_kernel<<<(unsigned)n_rows, kThreads, kDynSmem, stream>>>(
-      logits, stride, context_lens, max_context, k, reinterpret_cast<uint32_t*>(ws),
-      reinterpret_cast<uint16_t*>(ws + align256(cells * sizeof(uint32_t))), cand_stride(max_context), out, status);
+  const int32_t res = (int32_t)min((int64_t)kRes, ((int64_t)max(max_context, 1) + 3) / 4 * 4);
+  const size_t smem = kFixedSmem + (size_t)res * sizeof(uint32_t);
+  topk_row_kernel<<<(unsigned)n_rows, kThreads, smem, stream>>>(logits, stride, context_lens, max_context, k, res,
+                                                                reinterpret_cast<uint32_t*>(workspace),
+                                                                spill_stride(max_context), out, status);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// fp4idx_topk_noalloc: the top-k selection of fp4idx_topk with its candidate scratch in
+// fp4idx_topk_noalloc: the top-k selection of fp4idx_topk with its scratch in
 // a fixed array of this library's own device memory instead of a caller's workspace.
 //
 // It exists for callers that may not allocate device memory at the point where they
@@ -17,13 +17,13 @@
 // array's device address once (cudaGetSymbolAddress) and keeps it for later calls on the
 // same device; make that first call before any stream capture begins.
 //
-// Zero state: nothing in the array needs to start at zero.  A row's candidates go there
-// only when they do not fit in shared memory, and each call reads back only the
-// candidates it wrote itself.  So no call clears the array.
+// Zero state: nothing in the array needs to start at zero.  A row's sort keys go there
+// only for positions past what shared memory holds, and each call reads back only the
+// keys it wrote itself.  So no call clears the array.
 //
 // Every call on a device uses the same array.  Calls whose kernels may overlap (on
 // streams with no ordering between them, or from host threads at once) race on it and
-// corrupt each other's candidates; order such calls on one stream.
+// corrupt each other's keys; order such calls on one stream.
 #include <mutex>
 
 #include "fp4idx_internal.cuh"
