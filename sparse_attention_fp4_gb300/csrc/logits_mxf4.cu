@@ -208,6 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = ptx::smem_addr(smem);
+  // A kernel launched after this one as a programmatic dependent (the top-k) may be
+  // scheduled as soon as every CTA here has started; it waits for this grid's completion
+  // and memory flush itself before it reads anything, so its CTAs take each SM as these
+  // exit, with the launch latency already paid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // The schedule must describe exactly these rows and this grid.
   const SchedView sv = sched_view(const_cast<void*>(p.schedule), p.n_rows);

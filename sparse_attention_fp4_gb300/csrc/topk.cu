@@ -29,7 +29,10 @@
 namespace fp4idx {
 namespace {
 
-constexpr int kThreads = 1024;
+#ifndef FP4IDX_TOPK_THREADS
+#define FP4IDX_TOPK_THREADS 1024
+#endif
+constexpr int kThreads = FP4IDX_TOPK_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRes = 32768;    // keys a CTA keeps in shared memory
 constexpr int kHistBits = 12;  // top bits of the key counted by the first histogram
@@ -37,9 +40,11 @@ constexpr int kHist = 1 << kHistBits;
 constexpr int kLowBits = 32 - kHistBits;  // bits the radix passes resolve inside bin B
 constexpr int kDigitBits = kLowBits / 2;
 constexpr int kDigits = 1 << kDigitBits;
-constexpr int kU = 8;                 // 16-byte loads in flight per thread
-constexpr int kEmitGroups = 8192;     // groups of four positions per emit block (<= 36 mask bits a thread)
-static_assert(kWarps == 32 && kHist % (32 * kWarps) == 0 && kDigits == kThreads, "layout");
+constexpr int kU = 8192 / kThreads;   // 16-byte loads in flight per thread (128 KB per CTA)
+constexpr int kEmitGroups = 8 * kThreads;  // groups of four positions per emit block
+constexpr int kRunMax = ((kEmitGroups + kThreads - 1) / kThreads) | 1;  // groups a thread owns in a block
+static_assert(4 * kRunMax <= 64, "a run fits one 64-bit mask");
+static_assert(kWarps <= 32 && kHist % (4 * kThreads) == 0 && kDigits % kThreads == 0, "layout");
 static_assert(kLowBits == 2 * kDigitBits, "two digit passes");
 static_assert(kHist >= FP4IDX_MAX_TOPK, "the histogram doubles as the output stage");
 static_assert(4 * kEmitGroups <= 65535, "16-bit block counts in the emit scan");
@@ -72,14 +77,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratc
   }
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
-  uint32_t w = scratch[lane];  // kWarps == 32: every warp scans the warp sums itself
+  uint32_t w = lane < kWarps ? scratch[lane] : 0u;  // every warp scans the warp sums itself
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t n = __shfl_up_sync(kFull, w, o);
     if (lane >= o) w += n;
   }
   const uint32_t before = __shfl_sync(kFull, w, warp) - scratch[warp] + x - v;
-  total = __shfl_sync(kFull, w, 31);
+  total = __shfl_sync(kFull, w, kWarps - 1);
   __syncthreads();  // scratch may be reused
   return before;
 }
@@ -90,20 +95,24 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratc
 // the last one makes the result visible to the whole CTA.
 template <int kPerLane>
 __device__ __forceinline__ void find_bin_from_top(const int* counts, int rank, Shared& sh) {
-  static_assert(kPerLane == 1 || kPerLane == 4, "one or four bins a lane");
+  static_assert(kPerLane == 1 || kPerLane == 2 || kPerLane % 4 == 0, "bins a lane");
   constexpr int kPerWarp = kPerLane * 32;
   constexpr int kBins = kPerWarp * kWarps;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lo = kBins - warp * kPerWarp - (lane + 1) * kPerLane;  // this lane's lowest bin
   int c[kPerLane];
-  if constexpr (kPerLane == 4) {
-    const int4 v = *reinterpret_cast<const int4*>(counts + lo);
-    c[0] = v.x;
-    c[1] = v.y;
-    c[2] = v.z;
-    c[3] = v.w;
+  if constexpr (kPerLane % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < kPerLane; j += 4) {
+      const int4 v = *reinterpret_cast<const int4*>(counts + lo + j);
+      c[j] = v.x;
+      c[j + 1] = v.y;
+      c[j + 2] = v.z;
+      c[j + 3] = v.w;
+    }
   } else {
-    c[0] = counts[lo];
+#pragma unroll
+    for (int j = 0; j < kPerLane; j++) c[j] = counts[lo + j];
   }
   int s = 0;
 #pragma unroll
@@ -116,7 +125,7 @@ __device__ __forceinline__ void find_bin_from_top(const int* counts, int rank, S
   }
   if (lane == 31) sh.scratch[warp] = (uint32_t)x;
   __syncthreads();
-  const int ws = (int)sh.scratch[lane];
+  const int ws = lane < kWarps ? (int)sh.scratch[lane] : 0;
   int wx = ws;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -154,23 +163,38 @@ __device__ __forceinline__ float4 load_group(const float* lg, bool vec, int v, i
   return r;
 }
 
-// The row's keys: positions below res in shared memory, the rest in the row's spill
-// region of the workspace (res is a multiple of 4, so a group of four is in one place).
+// Dynamic shared memory of the top-k kernel (declared here so that helpers address it as
+// shared memory).
+extern __shared__ __align__(16) uint32_t topk_dyn[];
+
+// The row's keys: positions below res in shared memory (after the histogram), the rest in
+// the row's spill region of the workspace (res is a multiple of 4, so a group of four is
+// in one place).
 struct RowKeys {
-  uint32_t* sm;
   uint32_t* spill;
   int res;
   __device__ __forceinline__ uint4 get(int v) const {
     const int i = 4 * v;
-    if (i < res) return *reinterpret_cast<const uint4*>(sm + i);
+    if (i < res) return reinterpret_cast<const uint4*>(topk_dyn + kHist)[v];
     return __ldcg(reinterpret_cast<const uint4*>(spill + (i - res)));
   }
   __device__ __forceinline__ void put(int v, uint4 q) const {
     const int i = 4 * v;
-    if (i < res) *reinterpret_cast<uint4*>(sm + i) = q;
+    if (i < res) reinterpret_cast<uint4*>(topk_dyn + kHist)[v] = q;
     else *reinterpret_cast<uint4*>(spill + (i - res)) = q;
   }
 };
+
+// Nibble of the four keys of a group that satisfy pred (bit e = key e); keys at positions
+// 4v + e >= L (only in the row's last group) are left out.
+template <class Pred>
+__device__ __forceinline__ uint32_t group_mask(const uint4& q, int v, int L, Pred pred) {
+  uint32_t m = (uint32_t)pred(q.x) | ((uint32_t)pred(q.y) << 1) | ((uint32_t)pred(q.z) << 2) |
+               ((uint32_t)pred(q.w) << 3);
+  const int lim = L - 4 * v;  // >= 1 for every group of the row
+  if (lim < 4) m &= (1u << lim) - 1u;
+  return m;
+}
 
 __device__ __forceinline__ uint32_t lane_of(const uint4& q, int e) {
   return e == 0 ? q.x : (e == 1 ? q.y : (e == 2 ? q.z : q.w));
@@ -181,19 +205,25 @@ __device__ __forceinline__ uint32_t lane_of(const uint4& q, int e) {
 __device__ __forceinline__ void digit_pass(const RowKeys& keys, int L, int ng, uint32_t match, int match_shift,
                                            int shift, int rank, int* hist, Shared& sh) {
   const int tid = threadIdx.x;
-  hist[tid] = 0;  // kDigits == kThreads
+  for (int b = tid; b < kDigits; b += kThreads) hist[b] = 0;
   __syncthreads();
-#pragma unroll 4
-  for (int v = tid; v < ng; v += kThreads) {
-    const uint4 q = keys.get(v);
+  for (int v0 = 0; v0 < ng; v0 += kU * kThreads) {
 #pragma unroll
-    for (int e = 0; e < 4; e++) {
-      const uint32_t u = lane_of(q, e);
-      if ((u >> match_shift) == match && 4 * v + e < L) atomicAdd(&hist[(u >> shift) & (kDigits - 1)], 1);
+    for (int j = 0; j < kU; j++) {
+      const int v = v0 + j * kThreads + tid;
+      if (v < ng) {
+        const uint4 q = keys.get(v);
+        const uint32_t m = group_mask(q, v, L, [&](uint32_t u) { return (u >> match_shift) == match; });
+        if (m) {  // members are a few percent of the row
+#pragma unroll
+          for (int e = 0; e < 4; e++)
+            if ((m >> e) & 1u) atomicAdd(&hist[(lane_of(q, e) >> shift) & (kDigits - 1)], 1);
+        }
+      }
     }
   }
   __syncthreads();
-  find_bin_from_top<1>(hist, rank, sh);
+  find_bin_from_top<kDigits / (32 * kWarps)>(hist, rank, sh);
 }
 
 // Writes o[0..k): every position i < L whose key is above tau and the first take_total
@@ -209,18 +239,17 @@ __device__ void emit_ordered(const RowKeys& keys, int L, int ng, uint32_t tau, i
   int g_done = 0, e_done = 0;  // keys above / equal to tau in earlier blocks
   for (int b0 = 0; b0 < ng; b0 += kEmitGroups) {
     const int nbg = min(kEmitGroups, ng - b0);
-    const int run = ((nbg + kThreads - 1) / kThreads) | 1;
-    const int g0 = b0 + min(nbg, tid * run), g1 = b0 + min(nbg, tid * run + run);
+    const int run = ((nbg + kThreads - 1) / kThreads) | 1;  // at most kRunMax
+    const int g0 = b0 + min(nbg, tid * run);
+    const int mine = min(run, b0 + nbg - g0);
     uint64_t gtm = 0, eqm = 0;
-    for (int g = g0; g < g1; g++) {
-      const uint4 q = keys.get(g);
-      const int bit = 4 * (g - g0);
 #pragma unroll
-      for (int e = 0; e < 4; e++) {
-        const uint32_t u = lane_of(q, e);
-        const bool in = 4 * g + e < L;
-        gtm |= (uint64_t)(in && u > tau) << (bit + e);
-        eqm |= (uint64_t)(in && u == tau) << (bit + e);
+    for (int j = 0; j < kRunMax; j++) {
+      if (j < mine) {
+        const int g = g0 + j;
+        const uint4 q = keys.get(g);
+        gtm |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return u > tau; }) << (4 * j);
+        eqm |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return u == tau; }) << (4 * j);
       }
     }
     const int gt = __popcll(gtm), eq = __popcll(eqm);
@@ -253,11 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     topk_row_kernel(const float* __restrict__ logits, int64_t stride, const int32_t* __restrict__ context_lens,
                     int32_t max_context, int32_t k, int32_t res, uint32_t* spill, int64_t sstride,
                     int32_t* __restrict__ out, int32_t* status) {
-  extern __shared__ __align__(16) uint32_t dyn[];
   __shared__ Shared sh;
-  int* const hist = reinterpret_cast<int*>(dyn);
+  int* const hist = reinterpret_cast<int*>(topk_dyn);
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
+  // launched as a programmatic dependent of the kernel before it on the stream (the
+  // logits): wait until that grid has completed and its writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int32_t L = __ldg(context_lens + row);
   if (L < 0 || L > max_context) {
     if (tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
@@ -271,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* lg = logits + row * stride;
   const bool vec = (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
   const int ng = (L + 3) >> 2;
-  const RowKeys keys{dyn + kHist, spill + row * sstride, res};
+  const RowKeys keys{spill + row * sstride, res};
 
   // ---- 1. keys and the top-bits histogram; the first loads are issued before the
   // histogram is cleared
@@ -357,10 +388,22 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
   }
   const int32_t res = (int32_t)min((int64_t)kRes, ((int64_t)max(max_context, 1) + 3) / 4 * 4);
   const size_t smem = kFixedSmem + (size_t)res * sizeof(uint32_t);
-  topk_row_kernel<<<(unsigned)n_rows, kThreads, smem, stream>>>(logits, stride, context_lens, max_context, k, res,
-                                                                reinterpret_cast<uint32_t*>(workspace),
-                                                                spill_stride(max_context), out, status);
-  return cudaGetLastError();
+  // A programmatic dependent launch: the CTAs may become resident while the previous
+  // kernel on the stream is still running (as its CTAs exit), and wait in the kernel for
+  // its completion.  Without a trigger in the previous kernel this is an ordinary
+  // stream-ordered launch.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_row_kernel, logits, stride, context_lens, max_context, k, res,
+                            reinterpret_cast<uint32_t*>(workspace), spill_stride(max_context), out, status);
 }
 
 }  // namespace fp4idx
