@@ -24,7 +24,11 @@
 //      mask counts, then the set bits are written out.
 #include "fp4idx_internal.cuh"
 
+#include <cooperative_groups.h>
+
 #include <atomic>
+
+namespace cg = cooperative_groups;
 
 namespace fp4idx {
 namespace {
@@ -50,10 +54,6 @@ static_assert(kHist >= FP4IDX_MAX_TOPK, "the histogram doubles as the output sta
 static_assert(4 * kEmitGroups <= 65535, "16-bit block counts in the emit scan");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Dynamic shared memory: hist[kHist] (int; reused as the stage of the k outputs), then
-// keys[res].
-constexpr size_t kFixedSmem = kHist * sizeof(int);
-static_assert(kFixedSmem % 16 == 0, "keys start 16-byte aligned");
 
 // Order-preserving key; -0 maps to +0 so that equal values are equal keys.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -64,6 +64,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 struct Shared {
   uint32_t scratch[kWarps];
   int bin, rem;
+  uint32_t tot;  // a cluster CTA's packed emit totals, read by its peers
 };
 
 // Exclusive block scan of a uint32 (sums wrap modulo 2^32); `total` gets the block sum.
@@ -167,21 +168,22 @@ __device__ __forceinline__ float4 load_group(const float* lg, bool vec, int v, i
 // shared memory).
 extern __shared__ __align__(16) uint32_t topk_dyn[];
 
-// The row's keys: positions below res in shared memory (after the histogram), the rest in
-// the row's spill region of the workspace (res is a multiple of 4, so a group of four is
-// in one place).
+// The row's keys.  A CTA holds the keys of its slice of the row: groups v >= v0 with
+// 4 * (v - v0) < res in shared memory at topk_dyn + koff, the rest in the row's spill
+// region of the workspace (res is a multiple of 4, so a group of four is in one place;
+// distinct positions take distinct spill entries whichever CTA writes them).
 struct RowKeys {
   uint32_t* spill;
-  int res;
+  int res, v0, koff;
   __device__ __forceinline__ uint4 get(int v) const {
-    const int i = 4 * v;
-    if (i < res) return reinterpret_cast<const uint4*>(topk_dyn + kHist)[v];
-    return __ldcg(reinterpret_cast<const uint4*>(spill + (i - res)));
+    const int i = 4 * (v - v0);
+    if (i < res) return *reinterpret_cast<const uint4*>(topk_dyn + koff + i);
+    return __ldcg(reinterpret_cast<const uint4*>(spill + (4 * v - res)));
   }
   __device__ __forceinline__ void put(int v, uint4 q) const {
-    const int i = 4 * v;
-    if (i < res) reinterpret_cast<uint4*>(topk_dyn + kHist)[v] = q;
-    else *reinterpret_cast<uint4*>(spill + (i - res)) = q;
+    const int i = 4 * (v - v0);
+    if (i < res) *reinterpret_cast<uint4*>(topk_dyn + koff + i) = q;
+    else *reinterpret_cast<uint4*>(spill + (4 * v - res)) = q;
   }
 };
 
@@ -200,18 +202,19 @@ __device__ __forceinline__ uint32_t lane_of(const uint4& q, int e) {
   return e == 0 ? q.x : (e == 1 ? q.y : (e == 2 ? q.z : q.w));
 }
 
-// One radix pass: per digit (key >> shift) & (kDigits - 1), the number of the row's keys
-// whose bits from match_shift up equal `match`.  Ends with the digit picked for `rank`.
-__device__ __forceinline__ void digit_pass(const RowKeys& keys, int L, int ng, uint32_t match, int match_shift,
-                                           int shift, int rank, int* hist, Shared& sh) {
+// One radix pass over this CTA's groups [vs, ve): per digit (key >> shift) &
+// (kDigits - 1), the number of keys whose bits from match_shift up equal `match`, into
+// hist[0 .. kDigits).  Ends with a barrier.
+__device__ __forceinline__ void digit_count(const RowKeys& keys, int L, int vs, int ve, uint32_t match,
+                                            int match_shift, int shift, int* hist) {
   const int tid = threadIdx.x;
   for (int b = tid; b < kDigits; b += kThreads) hist[b] = 0;
   __syncthreads();
-  for (int v0 = 0; v0 < ng; v0 += kU * kThreads) {
+  for (int v0 = vs; v0 < ve; v0 += kU * kThreads) {
 #pragma unroll
     for (int j = 0; j < kU; j++) {
       const int v = v0 + j * kThreads + tid;
-      if (v < ng) {
+      if (v < ve) {
         const uint4 q = keys.get(v);
         const uint32_t m = group_mask(q, v, L, [&](uint32_t u) { return (u >> match_shift) == match; });
         if (m) {  // members are a few percent of the row
@@ -223,7 +226,6 @@ __device__ __forceinline__ void digit_pass(const RowKeys& keys, int L, int ng, u
     }
   }
   __syncthreads();
-  find_bin_from_top<kDigits / (32 * kWarps)>(hist, rank, sh);
 }
 
 // Writes o[0..k): every position i < L whose key is above tau and the first take_total
@@ -276,49 +278,131 @@ __device__ void emit_ordered(const RowKeys& keys, int L, int ng, uint32_t tau, i
   for (int i = tid; i < k; i += kThreads) o[i] = i < got ? stage[i] : -1;
 }
 
-// One CTA per row.  keys[0..res) of the row stay in shared memory (res a multiple of 4);
-// spill + row * sstride holds the keys of positions res and up (sstride a multiple of 4).
+// The emit of a row split over a cluster of kC CTAs: this CTA's groups [vs, ve) (at most
+// one emit block) in masks as in emit_ordered, one block scan for the offsets inside the
+// slice, then the totals of the lower-ranked CTAs (read from their shared memory) for the
+// slice's place in the output.  The caller's last cluster barrier keeps every CTA's
+// totals readable until its peers have read them.
+template <int kC>
+__device__ void emit_cluster(const RowKeys& keys, int L, int vs, int ve, uint32_t tau, int take_total, int32_t* o,
+                             int k, Shared& sh, int32_t* stage) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int tid = threadIdx.x;
+  const int nbg = ve - vs;  // <= kEmitGroups
+  const int run = ((nbg + kThreads - 1) / kThreads) | 1;
+  const int g0 = vs + min(nbg, tid * run);
+  const int mine = min(run, ve - g0);
+  uint64_t gtm = 0, eqm = 0;
+#pragma unroll
+  for (int j = 0; j < kRunMax; j++) {
+    if (j < mine) {
+      const int g = g0 + j;
+      const uint4 q = keys.get(g);
+      gtm |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return u > tau; }) << (4 * j);
+      eqm |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return u == tau; }) << (4 * j);
+    }
+  }
+  const int gt = __popcll(gtm), eq = __popcll(eqm);
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan((uint32_t)gt | ((uint32_t)eq << 16), sh.scratch, tot);
+  if (tid == 0) sh.tot = tot;
+  cl.sync();
+  const int rank = (int)cl.block_rank();
+  int Gb = 0, Eb = 0;  // keys above / equal to tau in the lower-ranked CTAs' slices
+  for (int q = 0; q < rank; q++) {
+    const uint32_t t = *cl.map_shared_rank(&sh.tot, q);
+    Gb += (int)(t & 0xFFFFu);
+    Eb += (int)(t >> 16);
+  }
+  const int G = Gb + (int)(pre & 0xFFFFu), E = Eb + (int)(pre >> 16);
+  const int take_eq = max(0, min(eq, take_total - E));
+  for (int drop = eq - take_eq; drop > 0; drop--) eqm &= ~(1ull << (63 - __clzll(eqm)));
+  uint64_t sel = gtm | eqm;
+  const int out0 = Gb + min(Eb, take_total);  // this slice's first output
+  const int out1 = Gb + (int)(tot & 0xFFFFu) + min(Eb + (int)(tot >> 16), take_total);
+  int w = G + min(E, take_total);
+  while (sel) {
+    const int b = __ffsll(sel) - 1;
+    sel &= sel - 1;
+    if (w < k) stage[w - out0] = 4 * g0 + b;
+    w++;
+  }
+  __syncthreads();
+  for (int i = out0 + tid; i < min(out1, k); i += kThreads) o[i] = stage[i - out0];
+  if (rank == kC - 1)  // past the selection (only rows with fewer than k keys in total)
+    for (int i = out1 + tid; i < k; i += kThreads) o[i] = -1;
+}
+
+// Sum of the kC CTAs' copies of counts[0 .. n) (n a multiple of 4) into merged[0 .. n).
+template <int kC, int n>
+__device__ __forceinline__ void merge_counts(int* counts, int* merged) {
+  cg::cluster_group cl = cg::this_cluster();
+  for (int i = 4 * (int)threadIdx.x; i < n; i += 4 * kThreads) {
+    int4 acc = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < kC; q++) {
+      const int4 v = *reinterpret_cast<const int4*>(cl.map_shared_rank(counts + i, q));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<int4*>(merged + i) = acc;
+  }
+  __syncthreads();
+}
+
+// kC CTAs (a cluster) per row; each owns a contiguous slice of the row's groups.  Shared
+// memory: hist[kHist] (also the output stage), for kC > 1 merged[kHist] and
+// dhist[kDigits], then the slice's keys[res] (res a multiple of 4).  spill + row * sstride
+// holds keys past res (sstride a multiple of 4).
+template <int kC>
 __global__ void __launch_bounds__(kThreads, 1)
     topk_row_kernel(const float* __restrict__ logits, int64_t stride, const int32_t* __restrict__ context_lens,
                     int32_t max_context, int32_t k, int32_t res, uint32_t* spill, int64_t sstride,
                     int32_t* __restrict__ out, int32_t* status) {
   __shared__ Shared sh;
   int* const hist = reinterpret_cast<int*>(topk_dyn);
-  const int64_t row = blockIdx.x;
+  int* const merged = kC > 1 ? hist + kHist : hist;
+  int* const dhist = kC > 1 ? hist + 2 * kHist : hist;
+  const int64_t row = blockIdx.x / kC;
+  const int rank = (int)(blockIdx.x % kC);
   const int tid = threadIdx.x;
   // launched as a programmatic dependent of the kernel before it on the stream (the
   // logits): wait until that grid has completed and its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   int32_t L = __ldg(context_lens + row);
   if (L < 0 || L > max_context) {
-    if (tid == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
+    if (tid == 0 && rank == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
     L = L < 0 ? 0 : max_context;
   }
   int32_t* o = out + row * k;
-  if (L <= k) {
-    for (int i = tid; i < k; i += kThreads) o[i] = i < L ? i : -1;
+  if (L <= k) {  // the same for every CTA of the row: none of them reaches a cluster barrier
+    for (int i = rank * kThreads + tid; i < k; i += kC * kThreads) o[i] = i < L ? i : -1;
     return;
   }
   const float* lg = logits + row * stride;
   const bool vec = (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
   const int ng = (L + 3) >> 2;
-  const RowKeys keys{spill + row * sstride, res};
+  const int per = (ng + kC - 1) / kC;
+  const int vs = min(ng, rank * per), ve = min(ng, vs + per);
+  const RowKeys keys{spill + row * sstride, res, vs, kC > 1 ? 2 * kHist + kDigits : kHist};
 
-  // ---- 1. keys and the top-bits histogram; the first loads are issued before the
-  // histogram is cleared
+  // ---- 1. keys of the slice and their top-bits histogram; the first loads are issued
+  // before the histogram is cleared
   float4 r[kU];
 #pragma unroll
   for (int u = 0; u < kU; u++) {
-    const int v = u * kThreads + tid;
-    if (v < ng) r[u] = load_group(lg, vec, v, L);
+    const int v = vs + u * kThreads + tid;
+    if (v < ve) r[u] = load_group(lg, vec, v, L);
   }
   for (int b = tid; b < kHist; b += kThreads) hist[b] = 0;
   __syncthreads();
-  for (int v0 = 0; v0 < ng; v0 += kU * kThreads) {
+  for (int v0 = vs; v0 < ve; v0 += kU * kThreads) {
 #pragma unroll
     for (int u = 0; u < kU; u++) {
       const int v = v0 + u * kThreads + tid;
-      if (v < ng) {
+      if (v < ve) {
         const uint4 q = make_uint4(order_key(r[u].x), order_key(r[u].y), order_key(r[u].z), order_key(r[u].w));
         keys.put(v, q);
         const int i = 4 * v;
@@ -329,32 +413,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const int vn = v0 + kU * kThreads;
-    if (vn < ng) {
+    if (vn < ve) {
 #pragma unroll
       for (int u = 0; u < kU; u++) {
         const int v = vn + u * kThreads + tid;
-        if (v < ng) r[u] = load_group(lg, vec, v, L);
+        if (v < ve) r[u] = load_group(lg, vec, v, L);
       }
     }
   }
-  __syncthreads();
+  if constexpr (kC > 1) {
+    cg::this_cluster().sync();
+    merge_counts<kC, kHist>(hist, merged);  // peers read this CTA's hist until the next cluster barrier
+  } else {
+    __syncthreads();
+  }
 
   // ---- 2. the bin holding the k-th largest key
-  find_bin_from_top<kHist / (32 * kWarps)>(hist, k, sh);
+  find_bin_from_top<kHist / (32 * kWarps)>(merged, k, sh);
   const uint32_t B = (uint32_t)sh.bin;
   const int rem = sh.rem;
 
   // ---- 3. two radix passes inside bin B
-  digit_pass(keys, L, ng, B, kLowBits, kDigitBits, rem, hist, sh);
+  digit_count(keys, L, vs, ve, B, kLowBits, kDigitBits, dhist);
+  if constexpr (kC > 1) {
+    cg::this_cluster().sync();  // also: every peer is done with this CTA's hist
+    merge_counts<kC, kDigits>(dhist, merged);
+  }
+  find_bin_from_top<kDigits / (32 * kWarps)>(merged, rem, sh);
   const uint32_t d1 = (uint32_t)sh.bin;
   const int rem1 = sh.rem;
   const uint32_t hi22 = (B << kDigitBits) | d1;
-  digit_pass(keys, L, ng, hi22, kDigitBits, 0, rem1, hist, sh);
+  digit_count(keys, L, vs, ve, hi22, kDigitBits, 0, hist);
+  if constexpr (kC > 1) {
+    cg::this_cluster().sync();
+    merge_counts<kC, kDigits>(hist, merged);
+  }
+  find_bin_from_top<kDigits / (32 * kWarps)>(merged, rem1, sh);
   const uint32_t tau = (hi22 << kDigitBits) | (uint32_t)sh.bin;
   const int take = sh.rem;
 
   // ---- 4. ordered emit (the histogram's space becomes the output stage)
-  emit_ordered(keys, L, ng, tau, take, o, k, sh, hist);
+  if constexpr (kC > 1) {
+    emit_cluster<kC>(keys, L, vs, ve, tau, take, o, k, sh, hist);
+    cg::this_cluster().sync();  // no CTA leaves while a peer may still read its shared memory
+  } else {
+    emit_ordered(keys, L, ng, tau, take, o, k, sh, hist);
+  }
 }
 
 inline int64_t spill_stride(int32_t max_context) {
@@ -362,7 +466,49 @@ inline int64_t spill_stride(int32_t max_context) {
 }
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-std::atomic<bool> g_attr_done[64];
+std::atomic<bool> g_attr_done[2][64];
+std::atomic<int> g_sms[64];
+
+// Shared memory of a kC-CTA launch with `res` keys a CTA.
+template <int kC>
+constexpr size_t smem_bytes(int32_t res) {
+  return (kC > 1 ? 2 * kHist + kDigits : kHist) * sizeof(int) + (size_t)res * sizeof(uint32_t);
+}
+
+template <int kC>
+cudaError_t launch_rows(int dev, const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
+                        int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,
+                        cudaStream_t stream) {
+  if (dev < 0 || dev >= 64 || !g_attr_done[kC - 1][dev].load()) {
+    const cudaError_t e = cudaFuncSetAttribute(topk_row_kernel<kC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem_bytes<kC>(kRes));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) g_attr_done[kC - 1][dev].store(true);
+  }
+  // keys a CTA holds: its slice of the longest row, rounded to groups of four
+  const int64_t groups = ((int64_t)max(max_context, 1) + 3) / 4;
+  const int32_t res = (int32_t)min((int64_t)kRes, 4 * ((groups + kC - 1) / kC));
+  // A programmatic dependent launch: the CTAs may become resident while the previous
+  // kernel on the stream is still running (as its CTAs exit), and wait in the kernel for
+  // its completion.  Without a trigger in the previous kernel this is an ordinary
+  // stream-ordered launch.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_rows * kC);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<kC>(res);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kC;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kC > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, topk_row_kernel<kC>, logits, stride, context_lens, max_context, k, res,
+                            reinterpret_cast<uint32_t*>(workspace), spill_stride(max_context), out, status);
+}
 
 }  // namespace
 
@@ -380,30 +526,17 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !g_attr_done[dev].load()) {
-    e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kFixedSmem + kRes * sizeof(uint32_t)));
+  int sms = dev >= 0 && dev < 64 ? g_sms[dev].load() : 0;
+  if (sms <= 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) g_attr_done[dev].store(true);
+    if (dev >= 0 && dev < 64) g_sms[dev].store(sms);
   }
-  const int32_t res = (int32_t)min((int64_t)kRes, ((int64_t)max(max_context, 1) + 3) / 4 * 4);
-  const size_t smem = kFixedSmem + (size_t)res * sizeof(uint32_t);
-  // A programmatic dependent launch: the CTAs may become resident while the previous
-  // kernel on the stream is still running (as its CTAs exit), and wait in the kernel for
-  // its completion.  Without a trigger in the previous kernel this is an ordinary
-  // stream-ordered launch.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)n_rows);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_row_kernel, logits, stride, context_lens, max_context, k, res,
-                            reinterpret_cast<uint32_t*>(workspace), spill_stride(max_context), out, status);
+  // Few rows leave most SMs idle: then each row goes to a pair of CTAs (a cluster), which
+  // halves the passes over its keys.
+  if (2 * (int64_t)n_rows <= sms)
+    return launch_rows<2>(dev, logits, stride, context_lens, n_rows, max_context, k, workspace, out, status, stream);
+  return launch_rows<1>(dev, logits, stride, context_lens, n_rows, max_context, k, workspace, out, status, stream);
 }
 
 }  // namespace fp4idx
