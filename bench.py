@@ -300,10 +300,10 @@ class DecodeStep:
             fn()
 
     def launch_user(self):
-        """The step as a caller issues it, in order on one stream: K store, Q quant,
-        schedule, then the fused logits + top-k call."""
+        """The step as a caller issues it, in order on one stream: schedule, K store, Q
+        quant, then the fused logits + top-k call."""
         calls = dict(self.calls())
-        for name in ("store_k", "quant_q", "build_schedule"):
+        for name in ("build_schedule", "store_k", "quant_q"):
             calls[name]()
         self.logits_topk()
 
@@ -320,7 +320,8 @@ class DecodeStep:
         start = torch.cuda.Event()
         start.record(cur)
         done = []
-        for name, st in zip(("store_k", "quant_q", "build_schedule"), side_streams):
+        # the longest branch first: a graph starts its root branches one after another
+        for name, st in zip(("build_schedule", "store_k", "quant_q"), side_streams):
             st.wait_event(start)
             with torch.cuda.stream(st):
                 calls[name]()

@@ -22,6 +22,8 @@
 //     the sign of zero taken from the input.
 #include "fp4idx_internal.cuh"
 
+#include <atomic>
+
 namespace fp4idx {
 namespace {
 
@@ -283,6 +285,21 @@ __global__ void __launch_bounds__(256) quant_q_kernel(
 
 inline unsigned grid_for(int64_t rows) { return (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock); }
 
+// These kernels need no shared memory, but they run just before the logits kernel, which
+// needs nearly all of it: asking for the largest shared-memory carveout keeps the SMs in
+// that configuration, so the logits CTAs launch without a carveout change.
+template <class K>
+cudaError_t prefer_max_shared(K kernel, std::atomic<bool>* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev].load()) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true);
+  return e;
+}
+std::atomic<bool> g_carve_store[64], g_carve_store_fp8[64], g_carve_quant[64];
+
 }  // namespace
 
 cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
@@ -290,6 +307,8 @@ cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* pos
                            uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status,
                            cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
+  cudaError_t e = prefer_max_shared(store_k_kernel, g_carve_store);
+  if (e != cudaSuccess) return e;
   store_k_kernel<<<grid_for(n_rows), 256, 0, stream>>>(k, n_rows, positions, slots, norm_w, eps, cos_sin,
                                                         max_pos, payload, scale, num_pages, status);
   return cudaGetLastError();
@@ -299,6 +318,8 @@ cudaError_t launch_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t*
                                const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
                                uint8_t* pages, int64_t num_pages, int32_t* status, cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
+  cudaError_t e = prefer_max_shared(store_k_fp8_kernel, g_carve_store_fp8);
+  if (e != cudaSuccess) return e;
   store_k_fp8_kernel<<<grid_for(n_rows), 256, 0, stream>>>(k, n_rows, positions, slots, norm_w, eps, cos_sin,
                                                             max_pos, pages, num_pages, status);
   return cudaGetLastError();
@@ -308,6 +329,8 @@ cudaError_t launch_quant_q(const uint16_t* q, int64_t n_rows, const int32_t* q_p
                            int32_t max_pos, uint8_t* q_payload, uint8_t* q_scale, int32_t* status,
                            cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
+  cudaError_t e = prefer_max_shared(quant_q_kernel, g_carve_quant);
+  if (e != cudaSuccess) return e;
   quant_q_kernel<<<grid_for(n_rows * kHeads), 256, 0, stream>>>(q, n_rows, q_positions, cos_sin, max_pos,
                                                                  q_payload, q_scale, status);
   return cudaGetLastError();
