@@ -56,8 +56,16 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
                                                                   const int32_t* __restrict__ row_seq,
                                                                   int32_t n_rows, int32_t num_ctas, void* ws) {
   __shared__ int64_t scratch[kWarps];
+  // Shared copies for the common case of at most kThreads rows (one chunk): the group
+  // starts, the cost prefix and the rows' context lengths, so that phases B and C wait on
+  // no global reads.  Larger inputs read the global arrays past the first chunk.
+  __shared__ int32_t row0_s[kThreads + 1];
+  __shared__ int64_t prefix_s[kThreads + 1];
+  __shared__ int32_t len_s[kThreads];
   SchedView s = sched_view(ws, n_rows);
   const int tid = threadIdx.x;
+  // the first chunk's context lengths: in flight while phase A scans
+  const int32_t len0 = tid < n_rows ? context_lens[tid] : 0;
 
   // Phase A: group starts.  run_start(t) = last t' <= t where row_seq changes; a group
   // starts where (t - run_start) is a multiple of kGroupMax.
@@ -71,25 +79,40 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
     const int64_t run = block_scan<true>(seg ? (int64_t)t : carry_run, scratch, run_tot);
     const bool gstart = valid && ((t - run) % kGroupMax == 0);
     const int64_t cnt = block_scan<false>(gstart ? 1 : 0, scratch, tot);
-    if (gstart) s.row0[carry_groups + cnt - 1] = t;
+    if (gstart) {
+      const int64_t gi = carry_groups + cnt - 1;
+      s.row0[gi] = t;
+      if (gi <= kThreads) row0_s[gi] = t;
+    }
     carry_groups += tot;
     carry_run = run_tot;
   }
   const int32_t n_groups = (int32_t)carry_groups;
-  if (tid == 0) s.row0[n_groups] = n_rows;
+  if (tid == 0) {
+    s.row0[n_groups] = n_rows;
+    if (n_groups <= kThreads) row0_s[n_groups] = n_rows;
+  }
+  len_s[tid] = len0;
   __syncthreads();
 
   // Phase B: per-group longest (clamped) context and cost prefix.
   int64_t carry_cost = 0;
-  if (tid == 0) s.prefix[0] = 0;
+  if (tid == 0) s.prefix[0] = prefix_s[0] = 0;
   for (int32_t base = 0; base < n_groups; base += kThreads) {
     const int32_t g = base + tid;
     int64_t cost = 0;
     if (g < n_groups) {
-      const int32_t r0 = s.row0[g], r1 = s.row0[g + 1];
+      int32_t r0, r1;
+      if (g < kThreads) {
+        r0 = row0_s[g];
+        r1 = row0_s[g + 1];
+      } else {
+        r0 = s.row0[g];
+        r1 = s.row0[g + 1];
+      }
       int32_t mx = 0;
       for (int32_t r = r0; r < r1; r++) {
-        int32_t L = context_lens[r];
+        int32_t L = r < kThreads ? len_s[r] : context_lens[r];
         L = L < 0 ? 0 : (L > FP4IDX_MAX_CONTEXT ? FP4IDX_MAX_CONTEXT : L);
         mx = L > mx ? L : mx;
       }
@@ -99,13 +122,19 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
     }
     int64_t tot;
     int64_t inc = block_scan<false>(cost, scratch, tot);
-    if (g < n_groups) s.prefix[g + 1] = carry_cost + inc;
+    if (g < n_groups) {
+      s.prefix[g + 1] = carry_cost + inc;
+      if (g < kThreads) prefix_s[g + 1] = carry_cost + inc;
+    }
     carry_cost += tot;
   }
   __syncthreads();
   // Phase C: each logits CTA's first group, so the kernel starts without a search.
-  for (int32_t c = tid; c < num_ctas; c += kThreads)
-    s.cta_g0[c] = first_group_after(s.prefix, n_groups, carry_cost * c / num_ctas);
+  for (int32_t c = tid; c < num_ctas; c += kThreads) {
+    const int64_t lo = carry_cost * c / num_ctas;
+    s.cta_g0[c] = n_groups <= kThreads ? first_group_after(prefix_s, n_groups, lo)
+                                       : first_group_after(s.prefix, n_groups, lo);
+  }
   if (tid == 0) {
     s.hdr->magic = kSchedMagic;
     s.hdr->n_rows = n_rows;
