@@ -199,6 +199,22 @@ __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, in
       : "memory");
 }
 
+// Lane l's share of the 32 page ids starting at logical page 2 * tile0 of the item's
+// sequence: the physical page, or -2 where the page lies past the item's longest context
+// or the sequence is out of range.
+__device__ __forceinline__ int32_t page_ids(const LogitsParams& p, const Item& it, int32_t tile0, int lane) {
+  const bool seq_ok = it.seq >= 0 && (int64_t)it.seq < p.num_seqs;
+  const int64_t span = min((int64_t)min(it.maxlen, p.max_context), (int64_t)p.max_pages * kPage);
+  const int64_t npages = (span + kPage - 1) / kPage;
+  const int64_t lp = 2 * (int64_t)tile0 + lane;
+  if (!seq_ok || lp < 0 || lp >= npages) return -2;
+  return __ldg(p.page_table + (int64_t)it.seq * p.max_pages + lp);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
 // Stage bookkeeping shared by all roles: tile pairs [i, i+1] of an item, in order.
 __device__ __forceinline__ int stage_tiles(int32_t i, int32_t t1) { return min(kTilesPerStage, t1 - i); }
 
@@ -208,19 +224,31 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = ptx::smem_addr(smem);
-  // A kernel launched after this one as a programmatic dependent (the top-k) may be
-  // scheduled as soon as every CTA here has started; it waits for this grid's completion
-  // and memory flush itself before it reads anything, so its CTAs take each SM as these
-  // exit, with the launch latency already paid.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // The schedule must describe exactly these rows and this grid.
+  // The schedule must describe exactly these rows and this grid.  The CTA's start record
+  // (inside the workspace the host checked against this grid) loads with the header.
   const SchedView sv = sched_view(const_cast<void*>(p.schedule), p.n_rows);
   const SchedHeader hdr = *sv.hdr;
+  const CtaStart cs = sv.cta[blockIdx.x];
   if (hdr.magic != kSchedMagic || hdr.n_rows != p.n_rows || hdr.num_ctas != (int32_t)gridDim.x ||
       hdr.group_max != kGroupMax) {
     if (threadIdx.x == 0) record_error(p.status, FP4IDX_ERR_SCHEDULE);
     return;
+  }
+  ItemIter items;
+  items.init(sv, cs);
+  // The producers request their first item's page ids before the prologue barrier, so the
+  // page-table read overlaps barrier set-up and the tensor-memory allocation.
+  const bool is_producer = warp >= kWarpProducer && warp < kWarpEpi0;
+  Item it;
+  bool have = false;
+  int32_t pid_cur = -2, pid_next = -2;
+  if (is_producer) {
+    have = items.next(it);
+    if (have) {
+      pid_cur = page_ids(p, it, it.t0, lane);
+      pid_next = page_ids(p, it, it.t0 + 16, lane);
+    }
   }
 
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + OFF_MISC + 4);
@@ -251,22 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.status};
 
-  ItemIter items;
-  items.init(sv, blockIdx.x, gridDim.x);
-  int32_t g, t0, t1;
-
-  if (warp >= kWarpProducer && warp < kWarpEpi0) {
+  if (is_producer) {
     // ------------------------------------------------------------ producers
     const int pw = warp - kWarpProducer;  // issues the stages with kctr % kProducers == pw
     uint32_t kctr = 0, ictr = 0;
     bool ok = true;
-    while (ok && items.next(g, t0, t1)) {
-      const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
-      const int32_t seq = sv.seq[g];  // row_seq of the group's rows, copied by the schedule
-      const bool seq_ok = seq >= 0 && (int64_t)seq < p.num_seqs;
-      int32_t maxlen = sv.maxlen[g];
-      maxlen = min(maxlen, min(p.max_context, p.max_pages * kPage));
-      const int32_t npages = (maxlen + kPage - 1) / kPage;
+    while (ok && have) {
+      const int32_t r0 = it.r0, rows = it.rows;
+      const bool seq_ok = it.seq >= 0 && (int64_t)it.seq < p.num_seqs;
       const int qb = ictr & 1;
       if (pw == 0) {
         ok = wait_lane0(bar_qempty(sb, qb), ((ictr >> 1) & 1) ^ 1, ctl);
@@ -279,28 +299,41 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           if (!seq_ok) record_error(p.status, FP4IDX_ERR_BAD_PAGE);
         }
       }
-      const int32_t* pt = p.page_table + (int64_t)(seq_ok ? seq : 0) * p.max_pages;
-      // lane l holds the physical page of logical page 2*chunk + l (16 tiles per chunk);
-      // a page that is not needed or not valid reads page 0 (status recorded if needed).
-      auto fetch = [&](int32_t tile0) -> int32_t {
-        const int32_t lp = 2 * tile0 + lane;
-        if (!seq_ok || lp >= npages) return -2;
-        return __ldg(pt + lp);
+      // The next item is looked up, and its first page ids requested, once this warp has
+      // filled its share of the ring (or at the end of a shorter item), so that a CTA
+      // whose range spans two groups does not stall on that chain at the switch.  Warp 0
+      // also warms the next item's query rows, head weights and lengths in L2.
+      Item nx;
+      bool have_nx = false, looked = false;
+      int32_t nx_cur = -2, nx_next = -2;
+      auto look_ahead = [&]() {
+        looked = true;
+        have_nx = items.next(nx);
+        if (!have_nx) return;
+        nx_cur = page_ids(p, nx, nx.t0, lane);
+        nx_next = page_ids(p, nx, nx.t0 + 16, lane);
+        if (pw == 0) {
+          for (int j = lane; j < nx.rows * 32; j += 32) prefetch_l2(p.q_payload + (int64_t)nx.r0 * 4096 + j * 128);
+          if (lane < 2 * nx.rows) {
+            prefetch_l2(p.q_scale + (int64_t)nx.r0 * 256 + lane * 128);
+            prefetch_l2(reinterpret_cast<const uint8_t*>(p.w + (int64_t)nx.r0 * 64) + lane * 128);
+          }
+          if (lane == 0) prefetch_l2(p.context_lens + nx.r0);
+        }
       };
-      int32_t chunk = t0;
-      int32_t pid_cur = fetch(chunk);
-      int32_t pid_next = fetch(chunk + 16);
-      for (int32_t i = t0; i < t1; i += kTilesPerStage, kctr++) {
+      int own = 0;
+      int32_t chunk = it.t0;
+      for (int32_t i = it.t0; i < it.t1; i += kTilesPerStage, kctr++) {
         if (i - chunk >= 16) {
           chunk += 16;
           pid_cur = pid_next;
-          pid_next = fetch(chunk + 16);
+          pid_next = page_ids(p, it, chunk + 16, lane);
         }
         if ((int)(kctr % kProducers) != pw) continue;
         const int s = kctr % kStages;
         ok = wait_lane0(bar_kempty(sb, s), ((kctr / kStages) & 1) ^ 1, ctl);
         if (!ok) break;
-        const int tiles = stage_tiles(i, t1);
+        const int tiles = stage_tiles(i, it.t1);
         // pages of this stage in lanes 0..3 (tile a: pages 2a, 2a+1)
         int32_t pg = __shfl_sync(kFull, pid_cur, (2 * (i - chunk) + (lane & 3)) & 31);
         const bool needed = (lane & 3) < 2 * tiles && pg != -2;
@@ -324,8 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           gather4(sb + OFF_KSC + s * kKScBytes, &sc_map, q0, q1, q2, q3, kbar);
         }
         __syncwarp();
+        if (!looked && ++own == kStages / kProducers) look_ahead();
       }
       ictr++;  // also after a failed stage wait: this item's query copies were issued
+      if (!ok) break;
+      if (!looked) look_ahead();
+      it = nx;
+      have = have_nx;
+      pid_cur = nx_cur;
+      pid_next = nx_next;
     }
     // Tail: every copy a warp issued must land, and (when not aborting) every stage must
     // be released by the MMAs that read it, before the CTA may exit.  kctr stops at the
@@ -349,11 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       bool ok = true;
       constexpr uint32_t kIdesc0 = ptx::idesc_mxf4(64, 0, 0);
       constexpr uint32_t kIdesc1 = ptx::idesc_mxf4(64, 2, 2);
-      while (ok && items.next(g, t0, t1)) {
-        const int32_t rows = sv.row0[g + 1] - sv.row0[g];
+      Item it;
+      while (ok && items.next(it)) {
+        const int32_t rows = it.rows;
         const int qb = ictr & 1;
         bool q_ready = false;
-        for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage, kctr++, ucnt += rows) {
+        for (int32_t i = it.t0; i < it.t1 && ok; i += kTilesPerStage, kctr++, ucnt += rows) {
           if ((int)(kctr % kMmaWarps) != mw) continue;
           if (!q_ready) {
             // query rows landed and their scales are in tensor memory
@@ -363,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
             q_ready = true;
           }
           const int s = kctr % kStages;
-          const int tiles = stage_tiles(i, t1);
+          const int tiles = stage_tiles(i, it.t1);
           // the stage's tiles landed with their scales in tensor memory (every scale
           // writer done with this use of the buffer), and each row's accumulator slot
           // is free (every epilogue warp released its previous use)
@@ -405,8 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     uint32_t kctr = 0, ictr = 0;
     bool ok = true;
-    while (ok && items.next(g, t0, t1)) {
-      const int32_t rows = sv.row0[g + 1] - sv.row0[g];
+    Item it;
+    while (ok && items.next(it)) {
+      const int32_t rows = it.rows;
       const int qb = ictr & 1;
       ok = wait_warp(bar_qfull(sb, qb), (ictr >> 1) & 1, ctl);
       if (!ok) break;
@@ -422,9 +464,9 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_qsf(sb, qb));
-      for (int32_t i = t0; i < t1; i += kTilesPerStage) {
+      for (int32_t i = it.t0; i < it.t1; i += kTilesPerStage) {
         const int s = kctr % kStages;
-        const int tiles = stage_tiles(i, t1);
+        const int tiles = stage_tiles(i, it.t1);
         ok = wait_warp(bar_kfull(sb, s), (kctr / kStages) & 1, ctl);
         if (!ok) break;
         for (int a = 0; a < tiles; a++) {
@@ -452,8 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
     float* wsm = reinterpret_cast<float*>(smem + OFF_WEPI) + ew * kGroupMax * 64;  // this warp's copy
     uint32_t ucnt = 0;
     bool ok = true;
-    while (ok && items.next(g, t0, t1)) {
-      const int32_t r0 = sv.row0[g], rows = sv.row0[g + 1] - r0;
+    Item it;
+    while (ok && items.next(it)) {
+      const int32_t r0 = it.r0, rows = it.rows;
       __syncwarp();
       if (lane < rows) {
         int32_t L = __ldg(p.context_lens + r0 + lane);
@@ -468,8 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       for (int j = lane; j < rows * 16; j += 32)
         reinterpret_cast<float4*>(wsm)[j] = __ldg(reinterpret_cast<const float4*>(p.w + (int64_t)r0 * 64) + j);
       __syncwarp();
-      for (int32_t i = t0; i < t1 && ok; i += kTilesPerStage) {
-        const int tiles = stage_tiles(i, t1);
+      for (int32_t i = it.t0; i < it.t1 && ok; i += kTilesPerStage) {
+        const int tiles = stage_tiles(i, it.t1);
         for (int r = 0; r < rows && ok; r++) {
           const float* wr = wsm + r * 64;  // same address in every lane: shared-memory broadcast
           const int32_t L = lsm[r];

@@ -129,11 +129,54 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
     carry_cost += tot;
   }
   __syncthreads();
-  // Phase C: each logits CTA's first group, so the kernel starts without a search.
-  for (int32_t c = tid; c < num_ctas; c += kThreads) {
-    const int64_t lo = carry_cost * c / num_ctas;
-    s.cta_g0[c] = n_groups <= kThreads ? first_group_after(prefix_s, n_groups, lo)
-                                       : first_group_after(s.prefix, n_groups, lo);
+  // Phase C: each logits CTA's cost range and first work item, so that the kernel starts
+  // its page-table reads without walking the schedule.
+  // (up to kThreads groups from the shared copies, more from the global arrays)
+  const bool small_cost = carry_cost * (int64_t)num_ctas < ((int64_t)1 << 31);
+  auto write_start = [&](int32_t c, auto row0_at, auto maxlen_at, auto seq_at, auto prefix_at, const int64_t* pre) {
+    CtaStart cs;
+    if (small_cost) {  // 32-bit division when every product fits
+      cs.lo = (int64_t)((uint32_t)carry_cost * (uint32_t)c / (uint32_t)num_ctas);
+      cs.hi = (int64_t)((uint32_t)carry_cost * (uint32_t)(c + 1) / (uint32_t)num_ctas);
+    } else {
+      cs.lo = carry_cost * c / num_ctas;
+      cs.hi = carry_cost * (c + 1) / num_ctas;
+    }
+    cs.n_groups = n_groups;
+    int32_t g = first_group_after(pre, n_groups, cs.lo);
+    Item it;
+    if (next_item(row0_at, maxlen_at, seq_at, prefix_at, n_groups, cs.lo, cs.hi, g, it)) {
+      cs.g = it.g;
+      cs.t0 = it.t0;
+      cs.t1 = it.t1;
+      cs.r0 = it.r0;
+      cs.rows = it.rows;
+      cs.seq = it.seq;
+      cs.maxlen = it.maxlen;
+    } else {
+      cs.g = n_groups;
+      cs.t0 = cs.t1 = cs.r0 = cs.rows = cs.seq = cs.maxlen = 0;
+    }
+    s.cta[c] = cs;
+  };
+  if (n_groups <= kThreads) {
+    // a group's longest clamped context, recomputed from its rows' lengths as in phase B
+    auto maxlen_at = [&](int32_t i) {
+      int32_t mx = 0;
+      for (int32_t r = row0_s[i]; r < row0_s[i + 1]; r++) {
+        int32_t L = r < kThreads ? len_s[r] : context_lens[r];
+        L = L < 0 ? 0 : (L > FP4IDX_MAX_CONTEXT ? FP4IDX_MAX_CONTEXT : L);
+        mx = L > mx ? L : mx;
+      }
+      return mx;
+    };
+    for (int32_t c = tid; c < num_ctas; c += kThreads)
+      write_start(c, [&](int32_t i) { return row0_s[i]; }, maxlen_at, [&](int32_t i) { return row_seq[row0_s[i]]; },
+                  [&](int32_t i) { return prefix_s[i]; }, prefix_s);
+  } else {
+    for (int32_t c = tid; c < num_ctas; c += kThreads)
+      write_start(c, [&](int32_t i) { return s.row0[i]; }, [&](int32_t i) { return s.maxlen[i]; },
+                  [&](int32_t i) { return s.seq[i]; }, [&](int32_t i) { return s.prefix[i]; }, s.prefix);
   }
   if (tid == 0) {
     s.hdr->magic = kSchedMagic;

@@ -29,6 +29,18 @@ struct SchedHeader {
   int32_t reserved;
 };
 
+// The first work item of one logits CTA, resolved by the schedule builder, so that the
+// kernel's first page-table read waits on one load of this record and nothing else.
+struct alignas(16) CtaStart {
+  int64_t lo, hi;       // the CTA's cost range [lo, hi)
+  int32_t g;            // group of the first item; n_groups when the range holds no item
+  int32_t t0, t1;       // its tile range
+  int32_t r0, rows;     // the group's first row and row count
+  int32_t seq, maxlen;  // the group's sequence and longest clamped context
+  int32_t n_groups;
+};
+static_assert(sizeof(CtaStart) == 48, "CtaStart layout");
+
 struct SchedView {
   SchedHeader* hdr;
   int32_t* row0;     // [n_rows + 1] first row of each group (entry n_groups = n_rows)
@@ -36,7 +48,7 @@ struct SchedView {
   int32_t* seq;      // [n_rows] the group's sequence (row_seq of its rows), so that a work
                      // item's first page-table read need not wait on a row_seq load
   int64_t* prefix;   // [n_rows + 1] exclusive prefix of group costs
-  int32_t* cta_g0;   // [num_ctas] first group whose cost interval ends after the CTA's range start
+  CtaStart* cta;     // [num_ctas] each logits CTA's cost range and first item
 };
 
 __host__ __device__ inline size_t sched_align16(size_t x) { return (x + 15) & ~(size_t)15; }
@@ -47,7 +59,7 @@ __host__ __device__ inline size_t sched_bytes(int64_t n_rows, int64_t num_ctas) 
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
-  b += sched_align16(sizeof(int32_t) * (size_t)num_ctas);
+  b += sizeof(CtaStart) * (size_t)num_ctas;
   return b;
 }
 
@@ -64,7 +76,7 @@ __host__ __device__ inline SchedView sched_view(void* base, int64_t n_rows) {
   p += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   v.prefix = reinterpret_cast<int64_t*>(p);
   p += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
-  v.cta_g0 = reinterpret_cast<int32_t*>(p);
+  v.cta = reinterpret_cast<CtaStart*>(p);
   return v;
 }
 
@@ -81,45 +93,97 @@ __host__ __device__ inline int32_t first_group_after(const int64_t* prefix, int3
   return a;
 }
 
-// Iterates the (group, tile range) items of one CTA in a fixed order.
+// One work item: tiles [t0, t1) of group g.
+struct Item {
+  int32_t g, t0, t1;
+  int32_t r0, rows;     // the group's rows
+  int32_t seq, maxlen;  // its sequence and longest clamped context
+};
+
+// Tile range [i0, i1) of a group whose cost interval starts at `base`, costs u per tile
+// and has ntiles tiles, cut to the cost range [lo, hi).  The differences are clamped to
+// the group's cost first, so the divisions are 32-bit.
+__host__ __device__ __forceinline__ void item_tiles(int64_t lo, int64_t hi, int64_t base, int32_t u, int32_t ntiles,
+                                           int32_t& i0, int32_t& i1) {
+  const int64_t span = (int64_t)ntiles * u;
+  const int32_t dl = (int32_t)(lo > base ? (lo - base < span ? lo - base : span) : 0);
+  const int32_t dh = (int32_t)(hi > base ? (hi - base < span ? hi - base : span) : 0);
+  i0 = (dl + u - 1) / u;
+  i1 = (dh + u - 1) / u;
+}
+
+// First non-empty item of the cost range [lo, hi) at or after group g (advanced past
+// it); false when there is none.  Accessors give a group's first row (row0(n_groups) =
+// the row count), longest clamped context, sequence and cost-prefix entry.
+template <class Row0, class MaxLen, class Seq, class Prefix>
+__host__ __device__ __forceinline__ bool next_item(Row0 row0, MaxLen maxlen, Seq seq, Prefix prefix, int32_t n_groups,
+                                          int64_t lo, int64_t hi, int32_t& g, Item& it) {
+  while (g < n_groups && prefix(g) < hi) {
+    const int32_t gg = g++;
+    const int32_t r0 = row0(gg), rows = row0(gg + 1) - r0;
+    const int32_t mx = maxlen(gg);
+    const int32_t ntiles = (mx + kTileTokens - 1) / kTileTokens;
+    int32_t i0, i1;
+    item_tiles(lo, hi, prefix(gg), kTileCost + rows, ntiles, i0, i1);
+    if (i0 < i1) {
+      it.g = gg;
+      it.t0 = i0;
+      it.t1 = i1;
+      it.r0 = r0;
+      it.rows = rows;
+      it.seq = seq(gg);
+      it.maxlen = mx;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Iterates the items of one CTA in a fixed order: the first from the CTA's start record,
+// the rest from the group arrays.
 struct ItemIter {
   const int32_t* row0;
   const int32_t* maxlen;
+  const int32_t* seq;
   const int64_t* prefix;
   int32_t n_groups;
   int64_t lo, hi;
   int32_t g;
+  Item first;
+  bool first_pending;
 
-  __device__ void init(const SchedView& s, int cta, int num_ctas) {
+  __device__ void init(const SchedView& s, const CtaStart& c) {
     row0 = s.row0;
     maxlen = s.maxlen;
+    seq = s.seq;
     prefix = s.prefix;
-    n_groups = s.hdr->n_groups;
-    const int64_t W = s.hdr->total_cost;
-    lo = W * cta / num_ctas;
-    hi = W * (cta + 1) / num_ctas;
-    g = s.cta_g0[cta];  // precomputed by the schedule kernel
+    n_groups = c.n_groups;
+    lo = c.lo;
+    hi = c.hi;
+    first_pending = c.g < c.n_groups;
+    g = first_pending ? c.g + 1 : c.n_groups;
+    first.g = c.g;
+    first.t0 = c.t0;
+    first.t1 = c.t1;
+    first.r0 = c.r0;
+    first.rows = c.rows;
+    first.seq = c.seq;
+    first.maxlen = c.maxlen;
   }
 
   // Next non-empty item; false when this CTA's range is exhausted.
-  __device__ bool next(int32_t& grp, int32_t& t0, int32_t& t1) {
-    while (g < n_groups && prefix[g] < hi) {
-      const int32_t gg = g++;
-      const int32_t rows = row0[gg + 1] - row0[gg];
-      const int64_t u = kTileCost + rows;
-      const int64_t ntiles = ceil_div64(maxlen[gg], kTileTokens);
-      const int64_t base = prefix[gg];
-      int64_t i0 = lo > base ? ceil_div64(lo - base, u) : 0;
-      int64_t i1 = hi > base ? ceil_div64(hi - base, u) : 0;
-      if (i1 > ntiles) i1 = ntiles;
-      if (i0 < i1) {
-        grp = gg;
-        t0 = (int32_t)i0;
-        t1 = (int32_t)i1;
-        return true;
-      }
+  __device__ bool next(Item& it) {
+    if (first_pending) {
+      first_pending = false;
+      it = first;
+      return true;
     }
-    return false;
+    const int32_t* r = row0;
+    const int32_t* m = maxlen;
+    const int32_t* q = seq;
+    const int64_t* x = prefix;
+    return next_item([r](int32_t i) { return r[i]; }, [m](int32_t i) { return m[i]; },
+                     [q](int32_t i) { return q[i]; }, [x](int32_t i) { return x[i]; }, n_groups, lo, hi, g, it);
   }
 };
 

@@ -18,10 +18,12 @@
 //      key and how many of B's keys the selection still needs;
 //   3. two radix passes over the keys, each counting only the keys still in the running
 //      (10 + 10 low bits), resolve the k-th key tau and how many keys equal to tau are
-//      taken;
+//      taken; the second is skipped when the first one's boundary sub-bin is taken
+//      whole (then the selection is every key from that sub-bin up, with no ties);
 //   4. one ordered pass emits every key above tau and the lowest-positioned keys equal to
 //      it: per thread a bit mask over a contiguous run of positions, one block scan of the
-//      mask counts, then the set bits are written out.
+//      mask counts, then the set bits are written out (straight to the output when there
+//      are no ties, else through a shared-memory stage).
 #include "fp4idx_internal.cuh"
 
 #include <cooperative_groups.h>
@@ -333,6 +335,44 @@ __device__ void emit_cluster(const RowKeys& keys, int L, int vs, int ve, uint32_
     for (int i = out1 + tid; i < k; i += kThreads) o[i] = -1;
 }
 
+// The emit when the selection is exactly the keys above tau (no ties to resolve): this
+// CTA's keys above tau, in position order, written straight to the output.  In a pair
+// (kC = 2, one emit block a CTA) the lower CTA fills the output from its start and the
+// upper one from its end: a row longer than k has exactly k keys above tau, so the two
+// exchange no counts.  One CTA (kC = 1) walks its emit blocks in order.
+template <int kC>
+__device__ void emit_above(const RowKeys& keys, int L, int vs, int ve, uint32_t tau, int32_t* o, int k,
+                           Shared& sh) {
+  static_assert(kC == 1 || kC == 2, "one CTA or a pair per row");
+  const int tid = threadIdx.x;
+  const int rank = kC > 1 ? (int)(blockIdx.x % kC) : 0;
+  int done = 0;  // keys above tau in this slice's earlier emit blocks
+  for (int b0 = vs; b0 < ve; b0 += kEmitGroups) {
+    const int nbg = min(kEmitGroups, ve - b0);
+    const int run = ((nbg + kThreads - 1) / kThreads) | 1;  // at most kRunMax
+    const int g0 = b0 + min(nbg, tid * run);
+    const int mine = min(run, b0 + nbg - g0);
+    uint64_t gtm = 0;
+#pragma unroll
+    for (int j = 0; j < kRunMax; j++) {
+      if (j < mine) {
+        const int g = g0 + j;
+        gtm |= (uint64_t)group_mask(keys.get(g), g, L, [&](uint32_t u) { return u > tau; }) << (4 * j);
+      }
+    }
+    uint32_t tot;
+    const uint32_t pre = block_excl_scan((uint32_t)__popcll(gtm), sh.scratch, tot);
+    int w = (rank == 1 ? k - (int)tot : done) + (int)pre;
+    while (gtm) {
+      const int b = __ffsll(gtm) - 1;
+      gtm &= gtm - 1;
+      if (w >= 0 && w < k) o[w] = 4 * g0 + b;
+      w++;
+    }
+    done += (int)tot;
+  }
+}
+
 // Sum of the kC CTAs' copies of counts[0 .. n) (n a multiple of 4) into merged[0 .. n).
 template <int kC, int n>
 __device__ __forceinline__ void merge_counts(int* counts, int* merged) {
@@ -368,9 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row = blockIdx.x / kC;
   const int rank = (int)(blockIdx.x % kC);
   const int tid = threadIdx.x;
-  // launched as a programmatic dependent of the kernel before it on the stream (the
-  // logits): wait until that grid has completed and its writes are visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   int32_t L = __ldg(context_lens + row);
   if (L < 0 || L > max_context) {
     if (tid == 0 && rank == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
@@ -443,6 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t d1 = (uint32_t)sh.bin;
   const int rem1 = sh.rem;
   const uint32_t hi22 = (B << kDigitBits) | d1;
+  if (merged[d1] == rem1 && hi22 != 0u) {
+    // Every key of the boundary sub-bin is taken (usually it holds a single key): the
+    // selection is every key whose top 22 bits are at least hi22, i.e. every key above
+    // the sub-bin's lowest value minus one, with no ties to resolve.  The same counts give
+    // every CTA of a pair the same decision.  The pair's last reads of each other's shared
+    // memory (the merge above) are done: arrive now, wait only before leaving.
+    if constexpr (kC > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    emit_above<kC>(keys, L, vs, ve, (hi22 << kDigitBits) - 1u, o, k, sh);
+    if constexpr (kC > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return;
+  }
   digit_count(keys, L, vs, ve, hi22, kDigitBits, 0, hist);
   if constexpr (kC > 1) {
     cg::this_cluster().sync();
@@ -488,24 +536,18 @@ cudaError_t launch_rows(int dev, const float* logits, int64_t stride, const int3
   // keys a CTA holds: its slice of the longest row, rounded to groups of four
   const int64_t groups = ((int64_t)max(max_context, 1) + 3) / 4;
   const int32_t res = (int32_t)min((int64_t)kRes, 4 * ((groups + kC - 1) / kC));
-  // A programmatic dependent launch: the CTAs may become resident while the previous
-  // kernel on the stream is still running (as its CTAs exit), and wait in the kernel for
-  // its completion.  Without a trigger in the previous kernel this is an ordinary
-  // stream-ordered launch.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_rows * kC);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem_bytes<kC>(res);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kC;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = kC > 1 ? 2 : 1;
+  cfg.numAttrs = kC > 1 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, topk_row_kernel<kC>, logits, stride, context_lens, max_context, k, res,
                             reinterpret_cast<uint32_t*>(workspace), spill_stride(max_context), out, status);
 }

@@ -121,3 +121,27 @@ def test_topk_rows_that_mislead_the_sample():
     got = run(rows, lens, 2048)
     for t, L in enumerate(lens):
         assert np.array_equal(got[t], expected(rows[t], L, 2048)), t
+
+
+def _boundary_row(rng, L, k, n_band, band):
+    """k - 2 keys at 10, n_band keys whose values share the top 22 key bits (the values in
+    `band`), the rest at 1; shuffled.  With n_band == 2 the boundary sub-bin is taken whole;
+    with n_band == 3 one of its keys must be left out (the higher position)."""
+    x = np.full(L, 1.0, np.float32)
+    pos = rng.permutation(L)
+    x[pos[:k - 2]] = 10.0
+    x[pos[k - 2:k - 2 + n_band]] = np.asarray(band[:n_band], np.float32)
+    return x
+
+
+@pytest.mark.parametrize("n_rows", [8, 100])  # a CTA pair per row, and one CTA per row
+@pytest.mark.parametrize("n_band,band", [(2, [5.0, 5.0]), (2, [5.0, 5.0000005]), (3, [5.0, 5.0, 5.0]),
+                                         (3, [5.0000005, 5.0, 5.0000005])])
+def test_topk_boundary_sub_bin(n_rows, n_band, band):
+    rng = np.random.default_rng(21 + n_band)
+    L, k = 4096, 2048
+    lens = [L] * n_rows
+    rows = [_boundary_row(rng, L, k, n_band, band) for _ in range(n_rows)]
+    got = run(rows, lens, k)
+    for t in range(n_rows):
+        assert np.array_equal(got[t], expected(rows[t], L, k)), (n_rows, n_band, t)
