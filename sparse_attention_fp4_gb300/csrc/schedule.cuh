@@ -4,10 +4,12 @@
 // row_seq, split every kGroupMax rows.  A group's rows share every K tile (all draft
 // rows of a sequence, or a block of prefill rows), so one tile load serves them all.
 // Group g covers tiles [0, ntiles) of 128 tokens, ntiles = ceil(max context / 128), and
-// costs ntiles * (kTileCost + rows) units: one unit per row for the epilogue plus a
-// fixed charge for streaming the tile.  The logits grid splits the total cost into
-// num_ctas equal ranges; CTA c takes every tile whose cost interval starts in its range.
-// The split decides only which CTA computes a logit, never its value.
+// costs kItemStartCost + ntiles * (kTileCost + rows) units (nothing when ntiles = 0): one
+// unit per row and tile for the epilogue, a fixed charge per tile for streaming it, and a
+// charge at the group's start for the CTA that switches to it mid-stream (its queries,
+// head weights and lengths, about two pipeline stages of time).  The logits grid splits
+// the total cost into num_ctas equal ranges; CTA c takes every tile whose cost interval
+// starts in its range.  The split decides only which CTA computes a logit, never its value.
 #pragma once
 
 #include <stdint.h>
@@ -17,6 +19,7 @@ namespace fp4idx {
 constexpr int kGroupMax = 6;  // six draft rows of a sequence share one group
 constexpr int kTileTokens = 128;
 constexpr int kTileCost = 2;
+constexpr int kItemStartCost = 10;
 constexpr int32_t kSchedMagic = 0x46344944;  // "F4ID"
 
 struct SchedHeader {
@@ -124,7 +127,7 @@ __host__ __device__ __forceinline__ bool next_item(Row0 row0, MaxLen maxlen, Seq
     const int32_t mx = maxlen(gg);
     const int32_t ntiles = (mx + kTileTokens - 1) / kTileTokens;
     int32_t i0, i1;
-    item_tiles(lo, hi, prefix(gg), kTileCost + rows, ntiles, i0, i1);
+    item_tiles(lo, hi, prefix(gg) + kItemStartCost, kTileCost + rows, ntiles, i0, i1);
     if (i0 < i1) {
       it.g = gg;
       it.t0 = i0;

@@ -18,8 +18,9 @@
 //      key and how many of B's keys the selection still needs;
 //   3. two radix passes over the keys, each counting only the keys still in the running
 //      (10 + 10 low bits), resolve the k-th key tau and how many keys equal to tau are
-//      taken; the second is skipped when the first one's boundary sub-bin is taken
-//      whole (then the selection is every key from that sub-bin up, with no ties);
+//      taken.  The second pass is skipped when the first one's boundary sub-bin is taken
+//      whole (then the selection is every key from that sub-bin up, with no ties), or
+//      holds at most kListMax keys (then those keys are ranked directly in the emit);
 //   4. one ordered pass emits every key above tau and the lowest-positioned keys equal to
 //      it: per thread a bit mask over a contiguous run of positions, one block scan of the
 //      mask counts, then the set bits are written out (straight to the output when there
@@ -55,6 +56,7 @@ static_assert(kLowBits == 2 * kDigitBits, "two digit passes");
 static_assert(kHist >= FP4IDX_MAX_TOPK, "the histogram doubles as the output stage");
 static_assert(4 * kEmitGroups <= 65535, "16-bit block counts in the emit scan");
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kListMax = 64;  // boundary sub-bin keys of a row ranked directly (all CTAs of a row)
 
 
 // Order-preserving key; -0 maps to +0 so that equal values are equal keys.
@@ -67,6 +69,7 @@ struct Shared {
   uint32_t scratch[kWarps];
   int bin, rem;
   uint32_t tot;  // a cluster CTA's packed emit totals, read by its peers
+  int nlist;     // entries in this CTA's list of boundary sub-bin keys, read by its peers
 };
 
 // Exclusive block scan of a uint32 (sums wrap modulo 2^32); `total` gets the block sum.
@@ -335,6 +338,90 @@ __device__ void emit_cluster(const RowKeys& keys, int L, int vs, int ve, uint32_
     for (int i = out1 + tid; i < k; i += kThreads) o[i] = -1;
 }
 
+// The emit when the boundary sub-bin (keys whose top 22 bits equal hi22) holds at most
+// kListMax keys in the row: every key above the sub-bin is taken, and of the sub-bin's keys
+// the rem1 largest, equal keys by position.  The sub-bin's keys are collected as (key,
+// position) pairs, the CTAs of a pair read each other's, and each key is taken when fewer
+// than rem1 of the row's sub-bin keys come before it; this replaces a second radix pass.
+// Exactly k keys are taken, so a pair fills the output from both ends as in emit_above.
+// `list` holds 2 * kListMax pairs (this CTA's, then the row's) and must not overlap the
+// first kDigits counts.  One emit block a CTA.
+template <int kC>
+__device__ void emit_ranked(const RowKeys& keys, int L, int vs, int ve, uint32_t hi22, int rem1, int32_t* o, int k,
+                            Shared& sh, uint32_t* list) {
+  static_assert(kC == 1 || kC == 2, "one CTA or a pair per row");
+  const int tid = threadIdx.x;
+  const int rank = kC > 1 ? (int)(blockIdx.x % kC) : 0;
+  const int nbg = ve - vs;  // <= kEmitGroups
+  const int run = ((nbg + kThreads - 1) / kThreads) | 1;
+  const int g0 = vs + min(nbg, tid * run);
+  const int mine = min(run, ve - g0);
+  uint64_t sel = 0, mem = 0;
+#pragma unroll
+  for (int j = 0; j < kRunMax; j++) {
+    if (j < mine) {
+      const int g = g0 + j;
+      const uint4 q = keys.get(g);
+      sel |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return (u >> kDigitBits) > hi22; }) << (4 * j);
+      const uint32_t m = group_mask(q, g, L, [&](uint32_t u) { return (u >> kDigitBits) == hi22; });
+      if (m) {  // a few keys in the whole row
+        mem |= (uint64_t)m << (4 * j);
+        for (int e = 0; e < 4; e++)
+          if ((m >> e) & 1u) {
+            const int i = atomicAdd(&sh.nlist, 1);
+            if (i < kListMax) {
+              list[2 * i] = lane_of(q, e);
+              list[2 * i + 1] = (uint32_t)(4 * g + e);
+            }
+          }
+      }
+    }
+  }
+  uint32_t* all = list + 2 * kListMax;
+  int n_all;
+  if constexpr (kC > 1) {
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();  // every CTA's list is complete
+    const int n_own = min(sh.nlist, kListMax);
+    const int n_peer = min(*cl.map_shared_rank(&sh.nlist, rank ^ 1), kListMax);
+    const uint32_t* plist = cl.map_shared_rank(list, rank ^ 1);
+    // the row's list in position order of the slices: the lower CTA's pairs first
+    const int off_own = rank == 0 ? 0 : n_peer, off_peer = rank == 0 ? n_own : 0;
+    if (tid < 2 * n_own) all[2 * off_own + tid] = list[tid];
+    if (tid < 2 * n_peer) all[2 * off_peer + tid] = plist[tid];
+    n_all = n_own + n_peer;
+    __syncthreads();
+    // this CTA's reads of its peer's shared memory are done; wait only before leaving
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  } else {
+    __syncthreads();
+    n_all = min(sh.nlist, kListMax);
+    all = list;
+  }
+  for (uint64_t mm = mem; mm;) {
+    const int b = __ffsll(mm) - 1;
+    mm &= mm - 1;
+    const uint32_t key = lane_of(keys.get(g0 + (b >> 2)), b & 3);
+    const uint32_t pos = (uint32_t)(4 * g0 + b);
+    int before = 0;
+    for (int i = 0; i < n_all; i++) {
+      const uint32_t kk = all[2 * i], pp = all[2 * i + 1];
+      before += (kk > key || (kk == key && pp < pos)) ? 1 : 0;
+    }
+    if (before < rem1) sel |= 1ull << b;
+  }
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan((uint32_t)__popcll(sel), sh.scratch, tot);
+  int w = (rank == 1 ? k - (int)tot : 0) + (int)pre;
+  while (sel) {
+    const int b = __ffsll(sel) - 1;
+    sel &= sel - 1;
+    if (w >= 0 && w < k) o[w] = 4 * g0 + b;
+    w++;
+  }
+  if constexpr (kC > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The emit when the selection is exactly the keys above tau (no ties to resolve): this
 // CTA's keys above tau, in position order, written straight to the output.  In a pair
 // (kC = 2, one emit block a CTA) the lower CTA fills the output from its start and the
@@ -408,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row = blockIdx.x / kC;
   const int rank = (int)(blockIdx.x % kC);
   const int tid = threadIdx.x;
+  if (tid == 0) sh.nlist = 0;  // many barriers pass before its first use
   int32_t L = __ldg(context_lens + row);
   if (L < 0 || L > max_context) {
     if (tid == 0 && rank == 0) record_error(status, FP4IDX_ERR_BAD_LENGTH);
@@ -480,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t d1 = (uint32_t)sh.bin;
   const int rem1 = sh.rem;
   const uint32_t hi22 = (B << kDigitBits) | d1;
-  if (merged[d1] == rem1 && hi22 != 0u) {
+  const int nd1 = merged[d1];  // keys of the row in the boundary sub-bin
+  if (nd1 == rem1 && hi22 != 0u) {
     // Every key of the boundary sub-bin is taken (usually it holds a single key): the
     // selection is every key whose top 22 bits are at least hi22, i.e. every key above
     // the sub-bin's lowest value minus one, with no ties to resolve.  The same counts give
@@ -489,6 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kC > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     emit_above<kC>(keys, L, vs, ve, (hi22 << kDigitBits) - 1u, o, k, sh);
     if constexpr (kC > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    return;
+  }
+  if (nd1 <= kListMax && (kC > 1 || ng <= kEmitGroups)) {
+    // a few keys in the boundary sub-bin: rank them directly instead of a second pass (the
+    // list sits past the first kDigits counts, which hold the sub-bin counts when kC = 1)
+    emit_ranked<kC>(keys, L, vs, ve, hi22, rem1, o, k, sh, reinterpret_cast<uint32_t*>(hist) + kDigits);
     return;
   }
   digit_count(keys, L, vs, ve, hi22, kDigitBits, 0, hist);
