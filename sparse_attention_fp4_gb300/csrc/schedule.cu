@@ -118,8 +118,7 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
       }
       s.maxlen[g] = mx;
       s.seq[g] = row_seq[r0];
-      const int64_t ntiles = ceil_div64(mx, kTileTokens);
-      cost = ntiles > 0 ? kItemStartCost + ntiles * (int64_t)(kTileCost + (r1 - r0)) : 0;
+      cost = group_cost(mx, r1 - r0);
     }
     int64_t tot;
     int64_t inc = block_scan<false>(cost, scratch, tot);

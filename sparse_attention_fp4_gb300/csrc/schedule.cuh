@@ -12,6 +12,7 @@
 // starts in its range.  The split decides only which CTA computes a logit, never its value.
 #pragma once
 
+#include <stddef.h>
 #include <stdint.h>
 
 namespace fp4idx {
@@ -84,6 +85,12 @@ __host__ __device__ inline SchedView sched_view(void* base, int64_t n_rows) {
 }
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Cost of a group of `rows` rows whose longest clamped context is maxlen.
+__host__ __device__ inline int64_t group_cost(int32_t maxlen, int32_t rows) {
+  const int64_t ntiles = ceil_div64(maxlen, kTileTokens);
+  return ntiles > 0 ? kItemStartCost + ntiles * (int64_t)(kTileCost + rows) : 0;
+}
 
 // First group whose cost interval [prefix[g], prefix[g+1]) ends after `lo`.
 __host__ __device__ inline int32_t first_group_after(const int64_t* prefix, int32_t n_groups, int64_t lo) {
