@@ -215,6 +215,34 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
 int fp4idx_topk_noalloc(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
                         int32_t max_context, int32_t k, int32_t* topk_idx, int32_t* status_dev, void* stream);
 
+/*
+ * Whole pages of the split cache -- [P1] Summary (dequantize_k_cache_paged serves the
+ * V4.1 layouts) and [P2] Device memory and sizing / HiCache integration (page-row views
+ * of the separately allocated payload and scale buffers; FP4 indexer rows move to and
+ * from host memory as whole pages, payload and scale as separate regions).
+ *   page_ids  [n_pages] int32  pages to process; an id < 0 is padding (skipped, its
+ *                              output untouched); an id >= num_pages records BAD_PAGE
+ *                              in status_dev and is skipped.
+ * fp4idx_dequant_pages: out [n_pages,64,128] fp32 (written), out[i][j][d] = the
+ *   e2m1 value of element d of token j of page page_ids[i] times 2^(scale byte - 127),
+ *   exact in fp32 (values past the fp32 range, possible only for scale bytes >= 253,
+ *   become +-inf).
+ * fp4idx_export_pages: rows_payload [n_pages,4096] uint8 and rows_scale [n_pages,256]
+ *   uint8 (written) = the payload and scale bytes of page page_ids[i], unchanged: page
+ *   rows ready for one host copy each region.
+ * fp4idx_import_pages: the reverse, writing page page_ids[i] of payload/scale from row
+ *   i.  The ids of one call must be distinct (two rows into one page race).
+ * rows_* and out are 16-byte aligned device buffers owned by the caller.
+ */
+int fp4idx_dequant_pages(const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_ids,
+                         int64_t n_pages, float* out, int32_t* status_dev, void* stream);
+int fp4idx_export_pages(const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_ids,
+                        int64_t n_pages, uint8_t* rows_payload, uint8_t* rows_scale, int32_t* status_dev,
+                        void* stream);
+int fp4idx_import_pages(const uint8_t* rows_payload, const uint8_t* rows_scale, const int32_t* page_ids,
+                        int64_t n_pages, uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status_dev,
+                        void* stream);
+
 /* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
  * a test/diagnostic helper, not for the hot path. */
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream);

@@ -233,6 +233,49 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
                                        topk_idx, status_dev, s));
 }
 
+namespace {
+
+int check_page_args(const void* payload, const void* scale, int64_t num_pages, const int32_t* page_ids,
+                    int64_t n_pages, const void* rows_a, const void* rows_b, int32_t* status_dev) {
+  if (num_pages < 0 || n_pages < 0 || n_pages > INT32_MAX) return FP4IDX_ERR_INVALID_ARG;
+  if (n_pages == 0) return FP4IDX_OK;
+  if (!payload || !scale || !page_ids || !rows_a || !rows_b) return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(payload) || !aligned16(scale) || !aligned4(page_ids) || !aligned16(rows_a) || !aligned16(rows_b))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return FP4IDX_OK;
+}
+
+}  // namespace
+
+int fp4idx_dequant_pages(const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_ids,
+                         int64_t n_pages, float* out, int32_t* status_dev, void* stream) {
+  const int st = check_page_args(payload, scale, num_pages, page_ids, n_pages, out, out, status_dev);
+  if (st != FP4IDX_OK || n_pages == 0) return st;
+  return from_cuda(fp4idx::launch_dequant_pages(payload, scale, num_pages, page_ids, n_pages, out, status_dev,
+                                                as_stream(stream)));
+}
+
+int fp4idx_export_pages(const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_ids,
+                        int64_t n_pages, uint8_t* rows_payload, uint8_t* rows_scale, int32_t* status_dev,
+                        void* stream) {
+  const int st = check_page_args(payload, scale, num_pages, page_ids, n_pages, rows_payload, rows_scale, status_dev);
+  if (st != FP4IDX_OK || n_pages == 0) return st;
+  return from_cuda(fp4idx::launch_copy_pages(const_cast<uint8_t*>(payload), const_cast<uint8_t*>(scale), num_pages,
+                                             page_ids, n_pages, rows_payload, rows_scale, true, status_dev,
+                                             as_stream(stream)));
+}
+
+int fp4idx_import_pages(const uint8_t* rows_payload, const uint8_t* rows_scale, const int32_t* page_ids,
+                        int64_t n_pages, uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status_dev,
+                        void* stream) {
+  const int st = check_page_args(payload, scale, num_pages, page_ids, n_pages, rows_payload, rows_scale, status_dev);
+  if (st != FP4IDX_OK || n_pages == 0) return st;
+  return from_cuda(fp4idx::launch_copy_pages(payload, scale, num_pages, page_ids, n_pages,
+                                             const_cast<uint8_t*>(rows_payload), const_cast<uint8_t*>(rows_scale),
+                                             false, status_dev, as_stream(stream)));
+}
+
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream) {
   if (!status_dev || !host_out) return FP4IDX_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);

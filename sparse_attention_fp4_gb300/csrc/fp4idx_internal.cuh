@@ -38,6 +38,12 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
                                const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
                                const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
                                int32_t* status, cudaStream_t stream);
+cudaError_t launch_dequant_pages(const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                                 const int32_t* page_ids, int64_t n_pages, float* out, int32_t* status,
+                                 cudaStream_t stream);
+cudaError_t launch_copy_pages(uint8_t* payload, uint8_t* scale, int64_t num_pages, const int32_t* page_ids,
+                              int64_t n_pages, uint8_t* rows_payload, uint8_t* rows_scale, bool to_rows,
+                              int32_t* status, cudaStream_t stream);
 size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context);
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,

@@ -66,6 +66,9 @@ _SIGS = {
     "fp4idx_topk_workspace_bytes": (_sz, [_i64, _i32]),
     "fp4idx_topk": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
     "fp4idx_topk_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _vp]),
+    "fp4idx_dequant_pages": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
+    "fp4idx_export_pages": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "fp4idx_import_pages": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
 }
 
@@ -240,6 +243,42 @@ def topk_noalloc(logits_buf, context_lens, max_context, k, topk_idx, status=None
                                   _ptr(topk_idx, "topk_idx", _I32, T * int(k)),
                                   _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_topk_noalloc", rc)
+
+
+def dequant_pages(payload, scale, page_ids, out, status=None, stream=None):
+    """out[i] = the fp32 values of page page_ids[i] of the split cache ([n, 64, 128])."""
+    n = page_ids.numel()
+    num_pages = payload.shape[0]
+    rc = _lib.fp4idx_dequant_pages(_ptr(payload, "payload", _U8, num_pages * 4096),
+                                   _ptr(scale, "scale", _U8, num_pages * 256), num_pages,
+                                   _ptr(page_ids, "page_ids", _I32, n), n, _ptr(out, "out", _F32, n * 64 * 128),
+                                   _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_dequant_pages", rc)
+
+
+def export_pages(payload, scale, page_ids, rows_payload, rows_scale, status=None, stream=None):
+    """Page rows of the listed pages: rows_payload [n, 4096] and rows_scale [n, 256] uint8."""
+    n = page_ids.numel()
+    num_pages = payload.shape[0]
+    rc = _lib.fp4idx_export_pages(_ptr(payload, "payload", _U8, num_pages * 4096),
+                                  _ptr(scale, "scale", _U8, num_pages * 256), num_pages,
+                                  _ptr(page_ids, "page_ids", _I32, n), n,
+                                  _ptr(rows_payload, "rows_payload", _U8, n * 4096),
+                                  _ptr(rows_scale, "rows_scale", _U8, n * 256),
+                                  _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_export_pages", rc)
+
+
+def import_pages(rows_payload, rows_scale, page_ids, payload, scale, status=None, stream=None):
+    """Writes page page_ids[i] of the split cache from page row i (ids distinct)."""
+    n = page_ids.numel()
+    num_pages = payload.shape[0]
+    rc = _lib.fp4idx_import_pages(_ptr(rows_payload, "rows_payload", _U8, n * 4096),
+                                  _ptr(rows_scale, "rows_scale", _U8, n * 256), _ptr(page_ids, "page_ids", _I32, n),
+                                  n, _ptr(payload, "payload", _U8, num_pages * 4096),
+                                  _ptr(scale, "scale", _U8, num_pages * 256), num_pages,
+                                  _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_import_pages", rc)
 
 
 def read_status(status, stream=None) -> int:
