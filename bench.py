@@ -776,13 +776,75 @@ def run_pages(args):
                       "export": res["export"], "import": res["import"], "dequant": res["dequant"]}), flush=True)
 
 
+def run_cp_merge(args):
+    """The exchange step of a context-parallel indexer on one GPU: 64 rows of the decode
+    shape (contexts U[8192, 32768] compressed tokens), each split over 4 shards of equal
+    token ranges; per shard the top-2048 (value, global position) candidates, chosen on
+    the host from N(0,1) logits; fp4idx_topk_merge selects each row's top-2048 from the
+    8,192 candidates.  Timed as a captured graph with the L2 flushed before each launch."""
+    import torch
+    from sparse_attention_fp4_gb300 import fp4idx
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    rng = np.random.default_rng(1006)
+    T, S, k, span = 64, 4, 2048, 32768
+    lens = rng.integers(8192, 32769, size=T)
+    width = span // S
+    cv = np.zeros((T, S, k), np.float32)
+    ci = np.full((T, S, k), -1, np.int32)
+    for t in range(T):
+        row = rng.standard_normal(int(lens[t])).astype(np.float32)
+        for s in range(S):
+            lo = s * width
+            part = row[lo:lo + width]
+            if part.size == 0:
+                continue
+            order = np.lexsort((np.arange(part.size), -part.astype(np.float64)))[:k]
+            sel = np.sort(order)
+            ci[t, s, :sel.size] = sel + lo
+            cv[t, s, :sel.size] = part[sel]
+    d_cv = torch.from_numpy(cv).to(device)
+    d_ci = torch.from_numpy(ci).to(device)
+    out = torch.empty((T, k), dtype=torch.int32, device=device)
+    ws = torch.empty(fp4idx.topk_merge_workspace_bytes(T, S, k), dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    fn = lambda: fp4idx.topk_merge(d_cv, d_ci, ws, out, status=status)
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    ts = []
+    for _ in range(min(args.steps, 500)):
+        flush.zero_()
+        torch.cuda._sleep(200000)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    us = statistics.median(ts)
+    assert fp4idx.read_status(status) == 0
+    print(json.dumps({"metric": "context-parallel top-k merge, query rows/s (4 shards x 2,048 candidates)",
+                      "value": round(T / (us * 1e-6), 1), "unit": "query rows/s", "n_gpus": 1,
+                      "higher_is_better": True, "data": "synthetic",
+                      "config": {"workload": "cp_merge_64x4x2048", "rows": T, "shards": S, "topk": k,
+                                 "l2": "flushed before every launch"},
+                      "merge_us": round(us, 2),
+                      "candidate_bytes": int(T * S * k * 8)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["fp4idx", "reference"], default="fp4idx")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["kstore", "pages"], default="decode_b64")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["kstore", "pages", "cp_merge"], default="decode_b64")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -795,6 +857,8 @@ def main(argv=None):
         run_kstore(args)
     elif args.workload == "pages":
         run_pages(args)
+    elif args.workload == "cp_merge":
+        run_cp_merge(args)
     else:
         run_gpu(args)
 

@@ -243,6 +243,31 @@ int fp4idx_import_pages(const uint8_t* rows_payload, const uint8_t* rows_scale, 
                         int64_t n_pages, uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status_dev,
                         void* stream);
 
+/*
+ * Context-parallel top-k -- [P3] the context-parallel runs (one long sequence's
+ * compressed tokens sharded over GPUs): each shard scores its own token range and keeps
+ * its top-k; the row's selection is the top-k of the gathered (value, index)
+ * candidates.  The merge is exact: every token of the row's top-k is in its shard's
+ * top-k, ties included (both sides give equal values to the lower position).
+ * fp4idx_topk_values: values[t][i] = logits[t][topk_idx[t][i]] (the values of a
+ *   selection made by fp4idx_topk on the same buffer); -inf where topk_idx is -1.
+ *   n_rows <= 65535.
+ * fp4idx_topk_merge: cand_values/cand_idx [n_rows, n_shards, k] fp32/int32: per row and
+ *   shard, the shard's selection as GLOBAL positions (ascending, -1 padding at the end)
+ *   with their values; shards in ascending position order (every position of shard s
+ *   below every position of shard s+1).  topk_idx [n_rows, k] (written): the k largest
+ *   candidates of the row, equal values to the lower position, ascending, -1 padding --
+ *   the same selection fp4idx_topk makes on the whole row.  n_shards * k <=
+ *   FP4IDX_MAX_CONTEXT, n_shards <= 1024, n_rows <= 65535; workspace of at least
+ *   fp4idx_topk_merge_workspace_bytes(n_rows, n_shards, k) bytes, 16-byte aligned,
+ *   nothing in it needs to be initialised.  Device errors as fp4idx_topk.
+ */
+size_t fp4idx_topk_merge_workspace_bytes(int64_t max_rows, int32_t n_shards, int32_t k);
+int fp4idx_topk_values(const float* logits, int64_t logits_stride, const int32_t* topk_idx, int64_t n_rows, int32_t k,
+                       float* values, void* stream);
+int fp4idx_topk_merge(const float* cand_values, const int32_t* cand_idx, int64_t n_rows, int32_t n_shards, int32_t k,
+                      void* workspace, size_t workspace_bytes, int32_t* topk_idx, int32_t* status_dev, void* stream);
+
 /* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
  * a test/diagnostic helper, not for the hot path. */
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream);

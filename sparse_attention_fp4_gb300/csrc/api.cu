@@ -276,6 +276,36 @@ int fp4idx_import_pages(const uint8_t* rows_payload, const uint8_t* rows_scale, 
                                              false, status_dev, as_stream(stream)));
 }
 
+size_t fp4idx_topk_merge_workspace_bytes(int64_t max_rows, int32_t n_shards, int32_t k) {
+  if (max_rows < 0 || n_shards < 1 || k < 1 || (int64_t)n_shards * k > FP4IDX_MAX_CONTEXT) return 0;
+  return fp4idx::merge_workspace_bytes(max_rows, n_shards, k);
+}
+
+int fp4idx_topk_values(const float* logits, int64_t logits_stride, const int32_t* topk_idx, int64_t n_rows, int32_t k,
+                       float* values, void* stream) {
+  if (n_rows < 0 || n_rows > 65535 || k < 1 || k > FP4IDX_MAX_TOPK || logits_stride < 1) return FP4IDX_ERR_INVALID_ARG;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!logits || !topk_idx || !values || !aligned4(logits) || !aligned4(topk_idx) || !aligned4(values))
+    return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_gather_values(logits, logits_stride, topk_idx, (int32_t)n_rows, k, values,
+                                                as_stream(stream)));
+}
+
+int fp4idx_topk_merge(const float* cand_values, const int32_t* cand_idx, int64_t n_rows, int32_t n_shards, int32_t k,
+                      void* workspace, size_t workspace_bytes, int32_t* topk_idx, int32_t* status_dev, void* stream) {
+  if (n_rows < 0 || n_rows > 65535 || k < 1 || k > FP4IDX_MAX_TOPK || n_shards < 1 || n_shards > 1024 ||
+      (int64_t)n_shards * k > FP4IDX_MAX_CONTEXT)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!cand_values || !cand_idx || !topk_idx || !workspace || !aligned4(cand_values) || !aligned4(cand_idx) ||
+      !aligned4(topk_idx) || !aligned16(workspace))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  if (workspace_bytes < fp4idx::merge_workspace_bytes(n_rows, n_shards, k)) return FP4IDX_ERR_WORKSPACE;
+  return from_cuda(fp4idx::launch_topk_merge(cand_values, cand_idx, (int32_t)n_rows, n_shards, k, workspace,
+                                             topk_idx, status_dev, as_stream(stream)));
+}
+
 int fp4idx_read_status(const int32_t* status_dev, int32_t* host_out, void* stream) {
   if (!status_dev || !host_out) return FP4IDX_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);

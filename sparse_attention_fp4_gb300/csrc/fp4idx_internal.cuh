@@ -44,6 +44,11 @@ cudaError_t launch_dequant_pages(const uint8_t* payload, const uint8_t* scale, i
 cudaError_t launch_copy_pages(uint8_t* payload, uint8_t* scale, int64_t num_pages, const int32_t* page_ids,
                               int64_t n_pages, uint8_t* rows_payload, uint8_t* rows_scale, bool to_rows,
                               int32_t* status, cudaStream_t stream);
+size_t merge_workspace_bytes(int64_t n_rows, int32_t n_shards, int32_t k);
+cudaError_t launch_gather_values(const float* logits, int64_t stride, const int32_t* idx, int32_t n_rows, int32_t k,
+                                 float* values, cudaStream_t stream);
+cudaError_t launch_topk_merge(const float* cand_values, const int32_t* cand_idx, int32_t n_rows, int32_t n_shards,
+                              int32_t k, void* workspace, int32_t* topk_idx, int32_t* status, cudaStream_t stream);
 size_t topk_workspace_bytes(int64_t n_rows, int32_t max_context);
 cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,

@@ -69,6 +69,9 @@ _SIGS = {
     "fp4idx_dequant_pages": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp]),
     "fp4idx_export_pages": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _vp]),
     "fp4idx_import_pages": (ctypes.c_int, [_vp, _vp, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "fp4idx_topk_merge_workspace_bytes": (_sz, [_i64, _i32, _i32]),
+    "fp4idx_topk_values": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _vp, _vp]),
+    "fp4idx_topk_merge": (ctypes.c_int, [_vp, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
     "fp4idx_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
 }
 
@@ -279,6 +282,31 @@ def import_pages(rows_payload, rows_scale, page_ids, payload, scale, status=None
                                   _ptr(scale, "scale", _U8, num_pages * 256), num_pages,
                                   _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_import_pages", rc)
+
+
+def topk_values(logits_buf, topk_idx, values, stream=None):
+    """values[t][i] = logits_buf[t][topk_idx[t][i]] (-inf for -1 padding)."""
+    T, k = topk_idx.shape
+    rc = _lib.fp4idx_topk_values(_ptr(logits_buf, "logits", _F32), logits_buf.shape[1],
+                                 _ptr(topk_idx, "topk_idx", _I32, T * k), T, k, _ptr(values, "values", _F32, T * k),
+                                 _stream_ptr(stream))
+    _check("fp4idx_topk_values", rc)
+
+
+def topk_merge_workspace_bytes(max_rows, n_shards, k) -> int:
+    return int(_lib.fp4idx_topk_merge_workspace_bytes(int(max_rows), int(n_shards), int(k)))
+
+
+def topk_merge(cand_values, cand_idx, workspace, topk_idx, status=None, stream=None):
+    """Row top-k from per-shard candidates [T, n_shards, k] (global positions, shards in
+    position order)."""
+    T, S, k = cand_idx.shape
+    rc = _lib.fp4idx_topk_merge(_ptr(cand_values, "cand_values", _F32, T * S * k),
+                                _ptr(cand_idx, "cand_idx", _I32, T * S * k), T, S, k,
+                                _ptr(workspace, "workspace", _U8), workspace.numel(),
+                                _ptr(topk_idx, "topk_idx", _I32, T * k), _ptr(status, "status", _I32, 1, nullable=True),
+                                _stream_ptr(stream))
+    _check("fp4idx_topk_merge", rc)
 
 
 def read_status(status, stream=None) -> int:
