@@ -42,11 +42,17 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
 }
 
 // out[i][j][32c + e] = e2m1(element 32c + e of token j) * 2^(scale[c][j] - 127), fp32.
+// A page's 32 KB of output is staged in shared memory (rows padded to 132 floats, so
+// the 16-byte stores of a quarter warp fall in distinct banks) and written out as one
+// contiguous run of 16-byte stores.
+constexpr int kOutPitch = 128 + 4;
+
 __global__ void __launch_bounds__(kPageThreads) dequant_pages_kernel(const uint8_t* __restrict__ payload,
                                                                      const uint8_t* __restrict__ scale,
                                                                      int64_t num_pages,
                                                                      const int32_t* __restrict__ page_ids,
                                                                      float* __restrict__ out, int32_t* status) {
+  __shared__ __align__(16) float tile[64 * kOutPitch];
   const int64_t i = blockIdx.x;
   const int64_t p = page_of(page_ids, i, num_pages, status);
   if (p < 0) return;
@@ -55,14 +61,22 @@ __global__ void __launch_bounds__(kPageThreads) dequant_pages_kernel(const uint8
   const int e = (int)__ldg(scale + p * kPageScale + c * 64 + j) - 127;
   const float s = ldexpf(1.0f, e);  // exact power of two (subnormal below 2^-126)
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float4* dst = reinterpret_cast<float4*>(out + (i * 64 + j) * 128 + 32 * c);
+  float4* st = reinterpret_cast<float4*>(tile + j * kOutPitch + 32 * c);
 #pragma unroll
   for (int b = 0; b < 4; b++) {
     float v[8];
 #pragma unroll
     for (int n = 0; n < 8; n++) v[n] = e2m1_value((w[b] >> (4 * n)) & 0xFu) * s;
-    dst[2 * b] = make_float4(v[0], v[1], v[2], v[3]);
-    dst[2 * b + 1] = make_float4(v[4], v[5], v[6], v[7]);
+    st[2 * b] = make_float4(v[0], v[1], v[2], v[3]);
+    st[2 * b + 1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  __syncthreads();
+  float4* dst = reinterpret_cast<float4*>(out + i * 64 * 128);
+#pragma unroll
+  for (int r = 0; r < 8; r++) {
+    const int f = r * kPageThreads + t;  // float4 index in the page's [64][128] output
+    const int row = f >> 5, col = f & 31;
+    dst[f] = *reinterpret_cast<const float4*>(tile + row * kOutPitch + 4 * col);
   }
 }
 
