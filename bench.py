@@ -838,13 +838,72 @@ def run_cp_merge(args):
                       "candidate_bytes": int(T * S * k * 8)}), flush=True)
 
 
+def run_qpack(args):
+    """Q pack + head weights in one launch for the decode batch (64 rows, 64 heads x 128) with
+    a hidden size of 7,168 (a reading: the pages give none), against the Q quant alone;
+    graph replays with the L2 flushed before each launch.  Bytes counted: Q in (16 KB/row),
+    packed Q out (4,352 B/row), hidden in (14 KB/row), the projection (917 KB, once), head
+    weights out (256 B/row)."""
+    import torch
+    from sparse_attention_fp4_gb300 import fp4idx
+    from sparse_attention_fp4_gb300 import workloads as wl
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    rng = np.random.default_rng(1007)
+    T, D = 64, 7168
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    q = bf(wl.f32_to_bf16_bits(rng.standard_normal((T, 64, 128)).astype(np.float32)))
+    qpos = torch.from_numpy(rng.integers(0, 131072, size=T).astype(np.int32)).to(device)
+    hidden = bf(wl.f32_to_bf16_bits(rng.standard_normal((T, D)).astype(np.float32)))
+    w_proj = bf(wl.f32_to_bf16_bits((rng.standard_normal((64, D)) / np.sqrt(D)).astype(np.float32)))
+    cs = bf(wl.rope_cos_sin_table())
+    qp, qs = fp4idx.alloc_query(T)
+    w_out = torch.empty((T, 64), dtype=torch.float32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    calls = {"quant_q_w": (lambda: fp4idx.quant_q_w(q, qpos, cs, hidden, w_proj, 0.125, qp, qs, w_out,
+                                                    status=status),
+                           T * (16384 + 4352 + 2 * D + 256) + 64 * D * 2),
+             "quant_q": (lambda: fp4idx.quant_q(q, qpos, cs, qp, qs, status=status), T * (16384 + 4352))}
+    peak, _ = measured_peaks()
+    res = {}
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ts = []
+        for _ in range(min(args.steps, 500)):
+            flush.zero_()
+            torch.cuda._sleep(200000)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(ts)
+        res[name] = {"us": round(us, 2), "algorithmic_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac_of_measured_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+    assert fp4idx.read_status(status) == 0
+    print(json.dumps({"metric": "Q pack + head weights, query rows/s (64 rows, hidden 7,168)",
+                      "value": round(T / (res["quant_q_w"]["us"] * 1e-6), 1), "unit": "query rows/s", "n_gpus": 1,
+                      "higher_is_better": True, "data": "synthetic",
+                      "config": {"workload": "qpack_64x7168", "rows": T, "hidden_dim": D,
+                                 "l2": "flushed before every launch"},
+                      "quant_q_w": res["quant_q_w"], "quant_q_alone": res["quant_q"]}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["fp4idx", "reference"], default="fp4idx")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["kstore", "pages", "cp_merge"], default="decode_b64")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["kstore", "pages", "cp_merge", "qpack"], default="decode_b64")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -859,6 +918,8 @@ def main(argv=None):
         run_pages(args)
     elif args.workload == "cp_merge":
         run_cp_merge(args)
+    elif args.workload == "qpack":
+        run_qpack(args)
     else:
         run_gpu(args)
 

@@ -56,6 +56,7 @@ extern "C" {
 #define FP4IDX_FP8_PAGE_BYTES (64 * 128 + 64 * 4)
 #define FP4IDX_MAX_TOPK 4096
 #define FP4IDX_MAX_CONTEXT 65536
+#define FP4IDX_MAX_HIDDEN 16384 /* hidden size limit of fp4idx_quant_q_w */
 #define FP4IDX_TOPK_NOALLOC_MAX_BYTES (16u * 1024u * 1024u) /* fixed scratch of fp4idx_topk_noalloc */
 
 typedef enum {
@@ -118,6 +119,29 @@ int fp4idx_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t* positio
 int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
                    const uint16_t* cos_sin, int32_t max_pos, uint8_t* q_payload, uint8_t* q_scale,
                    int32_t* status_dev, void* stream);
+
+/*
+ * Q quant and head weights in one launch -- [P1] Summary: "a one-launch index-Q pack +
+ * head weights", where indexer_head_weights runs a batch-invariant split-K bf16 GEMV whose
+ * result stays in fp32.  The queries are packed exactly as fp4idx_quant_q packs them
+ * (same arguments, same bytes); beside them
+ *   w_out[t][h] = w_scale * sum_d hidden[t][d] * w_proj[h][d]      (fp32, [n_rows, 64])
+ *   hidden [n_rows, hidden_dim] bf16; w_proj [64, hidden_dim] bf16 (row h: head h)
+ *   hidden_dim a multiple of 256, at most FP4IDX_MAX_HIDDEN (UNSUPPORTED otherwise)
+ * The pages give neither the hidden size nor a scale: any constant factor goes into
+ * w_scale.  Order of the sum (the same for every batch, so a row's weights do not depend
+ * on the rows beside it): the hidden dimension is cut into M = hidden_dim/256 chunks of
+ * 256 and the chunks into 8 runs [wM/8, (w+1)M/8); in run w, lane l of 32 adds the products
+ * d = 256m + 8l + i, m then i ascending, one fp32 rounding per addition (bf16 products are
+ * exact in fp32); then the 32 lane sums pairwise at lane distances 16, 8, 4, 2, 1; then the
+ * 8 run sums in run order; then one rounding for w_scale.  A product meets at most
+ * 8*ceil(M/8) + 12 <= hidden_dim/256 + 19 roundings, so the result is within
+ * (hidden_dim/256 + 20) * 2^-24 * |w_scale| * sum_d |hidden*w_proj| of the exact value.
+ */
+int fp4idx_quant_q_w(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
+                     const uint16_t* cos_sin, int32_t max_pos, const uint16_t* hidden, int32_t hidden_dim,
+                     const uint16_t* w_proj, float w_scale, uint8_t* q_payload, uint8_t* q_scale, float* w_out,
+                     int32_t* status_dev, void* stream);
 
 /*
  * Schedule -- the length-balanced split of the logits work over the GPU

@@ -289,3 +289,23 @@ def run_indexer(batch, cos_sin, rows=None):
         if len(rows) else np.zeros((0, batch.topk), np.int32)
     return dict(payload=payload, scale=scale, q_payload=qp, q_scale=qs, logits=lg, bound=bnd,
                 topk=tk, rows=np.asarray(rows))
+
+
+# ------------------------------------------------------------------ head weights
+def bf16_values(bits) -> np.ndarray:
+    """bf16 bit patterns -> their exact values in binary64 (a bf16 is the top half of a
+    float32)."""
+    b = np.ascontiguousarray(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def head_weights(hidden, w_proj, w_scale):
+    """[P1] Summary ("a one-launch index-Q pack + head weights"; indexer_head_weights runs a
+    bf16 GEMV whose result stays in fp32): w[t,h] = w_scale * sum_d hidden[t,d] *
+    w_proj[h,d] in binary64 (bf16 products are exact there), and the bound
+    |w_scale| * sum_d |hidden[t,d] * w_proj[h,d]| that device rounding is measured against.
+    hidden [T, D] and w_proj [H, D] are bf16 bit patterns; w_scale is taken as an fp32."""
+    h = bf16_values(hidden)
+    w = bf16_values(w_proj)
+    s = float(np.float32(w_scale))
+    return s * (h @ w.T), abs(s) * (np.abs(h) @ np.abs(w).T)

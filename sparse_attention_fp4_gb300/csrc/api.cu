@@ -93,6 +93,25 @@ int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int
                                           as_stream(stream)));
 }
 
+int fp4idx_quant_q_w(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
+                     const uint16_t* cos_sin, int32_t max_pos, const uint16_t* hidden, int32_t hidden_dim,
+                     const uint16_t* w_proj, float w_scale, uint8_t* q_payload, uint8_t* q_scale, float* w_out,
+                     int32_t* status_dev, void* stream) {
+  if (n_rows < 0 || max_pos <= 0 || hidden_dim <= 0) return FP4IDX_ERR_INVALID_ARG;
+  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
+  if (hidden_dim % 256 != 0 || hidden_dim > FP4IDX_MAX_HIDDEN) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows > (int64_t)INT32_MAX / 12) return FP4IDX_ERR_UNSUPPORTED;  // 4 quant blocks and 8 weight blocks a row
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!q || !q_positions || !cos_sin || !q_payload || !q_scale || !hidden || !w_proj || !w_out)
+    return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(cos_sin) || !aligned16(q_payload) || !aligned4(q_positions) || !aligned16(hidden) ||
+      !aligned16(w_proj) || !aligned4(w_out))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_quant_q_w(q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, hidden,
+                                            hidden_dim, w_proj, w_scale, w_out, status_dev, as_stream(stream)));
+}
+
 size_t fp4idx_schedule_workspace_bytes(int64_t max_rows, int32_t num_ctas) {
   if (max_rows < 0 || max_rows > INT32_MAX - 1 || num_ctas < 0) return 0;
   if (num_ctas == 0 && device_sms(&num_ctas) != FP4IDX_OK) return 0;

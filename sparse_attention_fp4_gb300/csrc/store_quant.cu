@@ -247,13 +247,15 @@ __global__ void __launch_bounds__(256) store_k_fp8_kernel(
   }
 }
 
-__global__ void __launch_bounds__(256) quant_q_kernel(
-    const uint16_t* __restrict__ q, int64_t n_rows, const int32_t* __restrict__ q_positions,
-    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ q_payload,
-    uint8_t* __restrict__ q_scale, int32_t* status) {
+// Q quant of the 16 (row, head) vectors of block `block`.
+__device__ __forceinline__ void quant_q_block(int64_t block, const uint16_t* __restrict__ q, int64_t n_rows,
+                                              const int32_t* __restrict__ q_positions,
+                                              const uint16_t* __restrict__ cos_sin, int32_t max_pos,
+                                              uint8_t* __restrict__ q_payload, uint8_t* __restrict__ q_scale,
+                                              int32_t* status) {
   // one "row" per (query row t, head h); 64 heads
   const int lh = threadIdx.x & 15;
-  const int64_t th = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4);
+  const int64_t th = block * kRowsPerBlock + (threadIdx.x >> 4);
   const int64_t total = n_rows * kHeads;
   const bool in_range = th < total;
   const int64_t t = th >> 6;
@@ -283,6 +285,88 @@ __global__ void __launch_bounds__(256) quant_q_kernel(
   }
 }
 
+__global__ void __launch_bounds__(256) quant_q_kernel(
+    const uint16_t* __restrict__ q, int64_t n_rows, const int32_t* __restrict__ q_positions,
+    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ q_payload,
+    uint8_t* __restrict__ q_scale, int32_t* status) {
+  quant_q_block(blockIdx.x, q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, status);
+}
+
+// Head weights of query row t: w[t][h] = w_scale * sum_d hidden[t][d] * w_proj[h][d], bf16
+// inputs, fp32 accumulation ([P1] Summary: indexer_head_weights runs a batch-invariant
+// split-K bf16 GEMV whose result stays in fp32).  A CTA takes row t and heads 8g .. 8g+7;
+// its 8 warps split the hidden dimension: with M = hidden_dim / 256 chunks, warp w takes
+// chunks [w M / 8, (w + 1) M / 8).  Fixed order, whatever the batch: lane l of warp w adds
+// the products d = 256 m + 8 l + i of its chunks, m then i ascending (every bf16 product is
+// exact in fp32, one rounding per addition); then the 32 lanes pairwise at distances 16, 8,
+// 4, 2, 1; then the 8 warp sums in warp order; then one rounding for the scale.  Each warp
+// keeps four heads' sums side by side, so that their weight loads are in flight together.
+__device__ __forceinline__ void head_weights_part(int64_t t, int g, const uint16_t* __restrict__ hidden, int32_t dim,
+                                                  const uint16_t* __restrict__ w_proj, float w_scale,
+                                                  float* __restrict__ w_out, uint16_t* hs, float* part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4* src = reinterpret_cast<const uint4*>(hidden + t * dim);
+  for (int i = threadIdx.x; i < dim / 8; i += 256) reinterpret_cast<uint4*>(hs)[i] = __ldg(src + i);
+  __syncthreads();
+  const int M = dim / 256;
+  const int m0 = warp * M / 8, m1 = (warp + 1) * M / 8;
+  float acc[8];
+#pragma unroll
+  for (int hp = 0; hp < 2; hp++) {
+    const uint16_t* wr = w_proj + (int64_t)(8 * g + 4 * hp) * dim;
+    float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+    for (int m = m0; m < m1; m++) {
+      const int d = 256 * m + 8 * lane;
+      uint4 wv[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) wv[j] = ldg16(wr + (int64_t)j * dim + d);
+      float a[8];
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(hs + d), a);
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        float b[8];
+        unpack_bf16x8(wv[j], b);
+#pragma unroll
+        for (int i = 0; i < 8; i++) a4[j] = __fadd_rn(a4[j], __fmul_rn(a[i], b[i]));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; j++) acc[4 * hp + j] = a4[j];
+  }
+#pragma unroll
+  for (int j = 0; j < 8; j++) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(0xFFFFFFFFu, acc[j], o));
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 8; j++) part[warp * 8 + j] = acc[j];
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    float sum = part[threadIdx.x];
+    for (int w = 1; w < 8; w++) sum = __fadd_rn(sum, part[w * 8 + threadIdx.x]);
+    w_out[t * kHeads + 8 * g + threadIdx.x] = __fmul_rn(sum, w_scale);
+  }
+}
+
+// One launch: blocks [0, q_blocks) quantise the queries, blocks q_blocks + 8t + g compute
+// row t's head weights 8g .. 8g + 7.
+__global__ void __launch_bounds__(256) quant_q_w_kernel(
+    const uint16_t* __restrict__ q, int64_t n_rows, const int32_t* __restrict__ q_positions,
+    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ q_payload,
+    uint8_t* __restrict__ q_scale, int64_t q_blocks, const uint16_t* __restrict__ hidden, int32_t dim,
+    const uint16_t* __restrict__ w_proj, float w_scale, float* __restrict__ w_out, int32_t* status) {
+  extern __shared__ __align__(16) uint16_t hidden_row[];
+  __shared__ float part[64];
+  if ((int64_t)blockIdx.x < q_blocks)
+    quant_q_block(blockIdx.x, q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, status);
+  else
+    head_weights_part(((int64_t)blockIdx.x - q_blocks) >> 3, (int)(((int64_t)blockIdx.x - q_blocks) & 7), hidden, dim,
+                      w_proj, w_scale, w_out, hidden_row, part);
+}
+
 inline unsigned grid_for(int64_t rows) { return (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock); }
 
 // These kernels need no shared memory, but they run just before the logits kernel, which
@@ -298,7 +382,7 @@ cudaError_t prefer_max_shared(K kernel, std::atomic<bool>* done) {
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true);
   return e;
 }
-std::atomic<bool> g_carve_store[64], g_carve_store_fp8[64], g_carve_quant[64];
+std::atomic<bool> g_carve_store[64], g_carve_store_fp8[64], g_carve_quant[64], g_carve_quant_w[64];
 
 }  // namespace
 
@@ -333,6 +417,20 @@ cudaError_t launch_quant_q(const uint16_t* q, int64_t n_rows, const int32_t* q_p
   if (e != cudaSuccess) return e;
   quant_q_kernel<<<grid_for(n_rows * kHeads), 256, 0, stream>>>(q, n_rows, q_positions, cos_sin, max_pos,
                                                                  q_payload, q_scale, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_q_w(const uint16_t* q, int64_t n_rows, const int32_t* q_positions, const uint16_t* cos_sin,
+                             int32_t max_pos, uint8_t* q_payload, uint8_t* q_scale, const uint16_t* hidden,
+                             int32_t dim, const uint16_t* w_proj, float w_scale, float* w_out, int32_t* status,
+                             cudaStream_t stream) {
+  if (n_rows == 0) return cudaSuccess;
+  cudaError_t e = prefer_max_shared(quant_q_w_kernel, g_carve_quant_w);
+  if (e != cudaSuccess) return e;
+  const int64_t q_blocks = grid_for(n_rows * kHeads);
+  quant_q_w_kernel<<<(unsigned)(q_blocks + 8 * n_rows), 256, (size_t)dim * sizeof(uint16_t), stream>>>(
+      q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, q_blocks, hidden, dim, w_proj, w_scale, w_out,
+      status);
   return cudaGetLastError();
 }
 

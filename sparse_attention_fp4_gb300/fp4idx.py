@@ -56,6 +56,8 @@ _SIGS = {
     "fp4idx_store_k": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_store_k_fp8": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _i64, _vp, _vp]),
     "fp4idx_quant_q": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "fp4idx_quant_q_w": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _f32, _vp, _vp, _vp, _vp,
+                                        _vp]),
     "fp4idx_schedule_workspace_bytes": (_sz, [_i64, _i32]),
     "fp4idx_build_schedule": (ctypes.c_int, [_vp, _vp, _i64, _i32, _vp, _sz, _vp]),
     "fp4idx_logits_workspace_bytes": (_sz, [_i64, _i32, _i32]),
@@ -170,6 +172,20 @@ def quant_q(q, q_positions, cos_sin, q_payload, q_scale, status=None, stream=Non
         cos_sin.shape[0], _ptr(q_payload, "q_payload", _U8, T * 4096), _ptr(q_scale, "q_scale", _U8, T * 256),
         _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_quant_q", rc)
+
+
+def quant_q_w(q, q_positions, cos_sin, hidden, w_proj, w_scale, q_payload, q_scale, w_out, status=None,
+              stream=None):
+    """fp4idx_quant_q and the head weights w_out = w_scale * hidden @ w_proj^T in one launch."""
+    T, H, D = q.shape
+    dim = hidden.shape[1]
+    rc = _lib.fp4idx_quant_q_w(_ptr(q, "q", _BF16, T * H * D), T, H, _ptr(q_positions, "q_positions", _I32, T),
+                               _ptr(cos_sin, "cos_sin", _BF16), cos_sin.shape[0],
+                               _ptr(hidden, "hidden", _BF16, T * dim), dim, _ptr(w_proj, "w_proj", _BF16, NUM_HEADS * dim),
+                               float(w_scale), _ptr(q_payload, "q_payload", _U8, T * 4096),
+                               _ptr(q_scale, "q_scale", _U8, T * 256), _ptr(w_out, "w_out", _F32, T * NUM_HEADS),
+                               _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_quant_q_w", rc)
 
 
 def schedule_workspace_bytes(max_rows, num_ctas=0) -> int:
