@@ -147,7 +147,7 @@ void ref_hadamard128(float u[D]) {
 }
 
 /* ------------------------------------------------------------------ UE8M0 block scale
- * the benchmark spec / P2 Motivation: one UE8M0 scale byte per 32 elements.
+ * [P2] Motivation: one UE8M0 scale byte per 32 elements.
  * Reading (rounding rule): the block exponent e is the smallest integer with
  * 6 * 2^e >= amax (6 = largest e2m1 magnitude), so no element saturates;
  * clamped to [-127, 127]; amax = 0 gives -127.  Stored byte = e + 127. */
@@ -395,7 +395,8 @@ void ref_dequant_q(const uint8_t* q_payload, const uint8_t* q_scale, int32_t H, 
 
 /* ------------------------------------------------------------------ paged-MQA logits
  * [P2] Modifications: decode and prefill "FP4 paged-MQA logits" read the split
- * payload/scale cache through the page table; the benchmark spec fixes the formula
+ * payload/scale cache through the page table.  The pages do not write the formula;
+ * this library reads it as (ReLU, head weights, no softmax or 1/sqrt(d))
  *   logits[t,s] = sum_h w[t,h] * ReLU(q_hat[t,h] . k_hat[s]),  s < context_lens[t],
  * with q_hat, k_hat the dequantised FP4 operands.  Token s of row t lives at
  * physical page page_table[row_seq[t]][s / 64], slot s % 64.
@@ -451,7 +452,7 @@ int ref_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w,
 }
 
 /* ------------------------------------------------------------------ top-k
- * the benchmark spec: per query row, the k largest logits among s < L; [P3] Changes and
+ * Per query row, the k largest logits among s < L; [P3] Changes and
  * Historical results: the selection is sorted and "ordered by position, not KV
  * slot".  Candidates ordered by (logit descending, index ascending); the first
  * min(k, L) are kept and emitted in ascending index order; the rest is -1. */
