@@ -705,12 +705,28 @@ def run_kstore(args):
         res[name] = {"us": round(us, 2), "rows_per_s": round(len(ks.positions) / (us * 1e-6), 1),
                      "algorithmic_gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bytes_per_token": out_b}
     assert fp4idx.read_status(status) == 0
+    cpu = None
+    if not args.no_cpu_baseline:
+        # the oracle's K store on a bounded slice of the same rows (host cores)
+        import dataclasses
+        import oracle
+        cs_np = wl.rope_cos_sin_table()
+        n, secs, done = 4096, 0.0, 0
+        while secs < args.cpu_seconds and done < len(ks.positions):
+            sub = dataclasses.replace(ks, k_rows=ks.k_rows[done:done + n], positions=ks.positions[done:done + n],
+                                      slots=ks.slots[done:done + n])
+            t0 = time.perf_counter()
+            oracle.store_k(sub, cs_np)
+            secs += time.perf_counter() - t0
+            done += len(sub.positions)
+        cpu = {"value": round(done / secs, 1), "unit": "rows/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": "%d rows of the same workload in slices of %d; %.1f s" % (done, n, secs)}
     peak, _ = measured_peaks()
     print(json.dumps({"metric": "K store rows/s (65,536 rows, split FP4 cache)", "value": res["fp4"]["rows_per_s"],
                       "unit": "rows/s", "n_gpus": 1, "higher_is_better": True, "data": "synthetic",
                       "config": {"workload": "kstore_65536", "rows": len(ks.positions), "cache_pages": ks.num_pages,
                                  "l2": "flushed before every launch"},
-                      "fp4": res["fp4"], "fp8_132B": res["fp8"],
+                      "fp4": res["fp4"], "fp8_132B": res["fp8"], "cpu_baseline": cpu,
                       "frac_of_measured_hbm": round(res["fp4"]["algorithmic_gbs"] / peak, 4)}), flush=True)
 
 
