@@ -451,6 +451,104 @@ int ref_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float* w,
   return status;
 }
 
+/* ------------------------------------------------------------------ FP8 comparison path
+ * [P2] Device memory and sizing: the FP8 indexer entry that the FP4 entry replaces, 132 B
+ * per token (128 e4m3 values and one fp32 scale).  Page layout as ref_store_k_fp8 writes it:
+ * bytes [j*128, j*128+128) = token j's e4m3 values, bytes [8192 + 4j, 8192 + 4j + 4) = its
+ * fp32 scale.  The query side follows the K side's rule (a reading: the pages give only the
+ * K entry): after RoPE and the Hadamard, one fp32 scale s = amax/448 per (row, head), 1 when
+ * amax = 0, and e4m3 = RNE-satfinite(z / s).  Query layout (this library's own):
+ * q8[t][c][h][16] for the 8 chunks c of 16 values, q8_scale[t][h] fp32. */
+int ref_quant_q_fp8(const uint16_t* q, int64_t T, int32_t H, const int32_t* q_positions, const uint16_t* cos_sin,
+                    int32_t max_pos, uint8_t* q8, float* q8_scale) {
+  int status = REF_OK;
+#pragma omp parallel for schedule(static)
+  for (int64_t th = 0; th < T * H; th++) {
+    int64_t t = th / H;
+    int32_t h = (int32_t)(th % H), pos = q_positions[t];
+    if (pos < 0 || pos >= max_pos) {
+#pragma omp critical
+      status = REF_ERR_ARG;
+      continue;
+    }
+    float z[D];
+    ref_q_chain(q + (size_t)th * D, pos, cos_sin, 3, z);
+    float amax = 0.0f;
+    for (int i = 0; i < D; i++) {
+      float a = fabsf(z[i]);
+      if (a > amax) amax = a;
+    }
+    float sc = (amax > 0.0f) ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < D; i++)
+      q8[((size_t)(t * 8 + i / 16) * H + h) * 16 + (i % 16)] = (uint8_t)ref_e4m3_code(z[i] / sc);
+    q8_scale[t * H + h] = sc;
+  }
+  return status;
+}
+
+/* dequantised K of one token of an FP8 page */
+void ref_dequant_k_fp8_token(const uint8_t* pages, int64_t page, int32_t j, double out[D]) {
+  const uint8_t* base = pages + (size_t)page * PAGE * (D + 4);
+  float sc;
+  memcpy(&sc, base + (size_t)PAGE * D + (size_t)j * 4, 4);
+  for (int i = 0; i < D; i++) out[i] = ref_e4m3_value(base[(size_t)j * D + i]) * (double)sc;
+}
+
+/* dequantised FP8 Q of one (row, head) */
+void ref_dequant_q_fp8(const uint8_t* q8, const float* q8_scale, int32_t H, int64_t t, int32_t h, double out[D]) {
+  double sc = (double)q8_scale[t * H + h];
+  for (int i = 0; i < D; i++) out[i] = ref_e4m3_value(q8[((size_t)(t * 8 + i / 16) * H + h) * 16 + (i % 16)]) * sc;
+}
+
+/* logits[t,s] = sum_h w[t,h] * ReLU(q_hat[t,h] . k_hat[s]) over the FP8 operands, binary64,
+ * with the same paging, masking and bound as ref_logits. */
+int ref_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t T, int32_t H,
+                   const uint8_t* pages, int64_t num_pages, const int32_t* page_table, int32_t max_pages,
+                   const int32_t* row_seq, const int32_t* context_lens, const int64_t* rows, int64_t n_req,
+                   int64_t L_stride, double* logits, double* bound) {
+  int status = REF_OK;
+  for (int64_t r = 0; r < n_req; r++) {
+    int64_t t = rows[r];
+    if (t < 0 || t >= T) return REF_ERR_ARG;
+    int32_t L = context_lens[t];
+    if (L > L_stride) return REF_ERR_ARG;
+    double* qh = (double*)malloc(sizeof(double) * (size_t)H * D);
+    for (int32_t h = 0; h < H; h++) ref_dequant_q_fp8(q8, q8_scale, H, t, h, qh + (size_t)h * D);
+    const int32_t* pt = page_table + (size_t)row_seq[t] * max_pages;
+#pragma omp parallel for schedule(static)
+    for (int32_t s = 0; s < L; s++) {
+      int32_t lp = s / PAGE;
+      int64_t page = (lp < max_pages) ? pt[lp] : -1;
+      if (page < 0 || page >= num_pages) {
+#pragma omp critical
+        status = REF_ERR_BAD_PAGE;
+        logits[r * L_stride + s] = NAN;
+        if (bound) bound[r * L_stride + s] = NAN;
+        continue;
+      }
+      double kh[D];
+      ref_dequant_k_fp8_token(pages, page, s % PAGE, kh);
+      double acc = 0.0, accb = 0.0;
+      for (int32_t h = 0; h < H; h++) {
+        const double* qv = qh + (size_t)h * D;
+        double dot = 0.0, adot = 0.0;
+        for (int i = 0; i < D; i++) {
+          double p = qv[i] * kh[i];
+          dot += p;
+          adot += fabs(p);
+        }
+        double wh = (double)w[t * H + h];
+        acc += wh * (dot > 0.0 ? dot : 0.0);
+        accb += fabs(wh) * adot;
+      }
+      logits[r * L_stride + s] = acc;
+      if (bound) bound[r * L_stride + s] = accb;
+    }
+    free(qh);
+  }
+  return status;
+}
+
 /* ------------------------------------------------------------------ top-k
  * Per query row, the k largest logits among s < L; [P3] Changes and
  * Historical results: the selection is sorted and "ordered by position, not KV

@@ -57,6 +57,11 @@ def lib():
             "ref_quant_q": (ctypes.c_int, [_u16p, _i64, _i32, _i32p, _u16p, _i32, _u8p, _u8p]),
             "ref_dequant_k_token": (None, [_u8p, _u8p, _i64, _i32, _f64p]),
             "ref_dequant_q": (None, [_u8p, _u8p, _i32, _i64, _i32, _f64p]),
+            "ref_quant_q_fp8": (ctypes.c_int, [_u16p, _i64, _i32, _i32p, _u16p, _i32, _u8p, _f32p]),
+            "ref_dequant_k_fp8_token": (None, [_u8p, _i64, _i32, _f64p]),
+            "ref_dequant_q_fp8": (None, [_u8p, _f32p, _i32, _i64, _i32, _f64p]),
+            "ref_logits_fp8": (ctypes.c_int, [_u8p, _f32p, _f32p, _i64, _i32, _u8p, _i64, _i32p, _i32, _i32p,
+                                              _i32p, _i64p, _i64, _i64, _f64p, _f64p]),
             "ref_logits": (ctypes.c_int, [_u8p, _u8p, _f32p, _i64, _i32, _u8p, _u8p, _i64, _i32p, _i32,
                                           _i32p, _i32p, _i64p, _i64, _i64, _f64p, _f64p]),
             "ref_topk": (ctypes.c_int, [_f64p, _i64, _i32, _i32p]),
@@ -262,6 +267,59 @@ def logits(q_payload, q_scale, w, payload, scale, page_table, row_seq, context_l
                           pl.shape[0], _p(pt, _i32p), pt.shape[1], _p(rs, _i32p), _p(cl, _i32p),
                           _p(rows, _i64p), rows.shape[0], Lmax, _p(out, _f64p),
                           _p(bnd, _f64p) if bnd is not None else None)
+    return out, bnd, int(st)
+
+
+def quant_q_fp8(q, q_positions, cos_sin):
+    """FP8 query pack: (q8 [T,8,H,16] u8, q8_scale [T,H] f32, status); the K side's FP8 rule
+    per (row, head) after RoPE and the Hadamard."""
+    q = _c(q, np.uint16)
+    T, H, Dd = q.shape
+    assert Dd == HEAD_DIM
+    pos = _c(q_positions, np.int32)
+    cs = _c(cos_sin, np.uint16)
+    q8 = np.zeros((T, 8, H, 16), np.uint8)
+    s8 = np.zeros((T, H), np.float32)
+    st = lib().ref_quant_q_fp8(_p(q, _u16p), T, H, _p(pos, _i32p), _p(cs, _u16p), cs.shape[0], _p(q8, _u8p),
+                               _p(s8, _f32p))
+    return q8, s8, int(st)
+
+
+def dequant_k_fp8_token(pages, page, j) -> np.ndarray:
+    out = np.empty(HEAD_DIM, np.float64)
+    pages = _c(pages, np.uint8)
+    lib().ref_dequant_k_fp8_token(_p(pages, _u8p), int(page), int(j), _p(out, _f64p))
+    return out
+
+
+def dequant_q_fp8(q8, q8_scale, t, h) -> np.ndarray:
+    q8 = _c(q8, np.uint8)
+    s8 = _c(q8_scale, np.float32)
+    out = np.empty(HEAD_DIM, np.float64)
+    lib().ref_dequant_q_fp8(_p(q8, _u8p), _p(s8, _f32p), q8.shape[2], int(t), int(h), _p(out, _f64p))
+    return out
+
+
+def logits_fp8(q8, q8_scale, w, pages, page_table, row_seq, context_lens, rows=None, with_bound=True):
+    """Binary64 logits over the FP8 operands (the 132 B/token pages of store_k_fp8 and the FP8
+    query pack): (logits [n, Lmax], bound or None, status); NaN at s >= L_t."""
+    q8 = _c(q8, np.uint8)
+    s8 = _c(q8_scale, np.float32)
+    w = _c(w, np.float32)
+    pg = _c(pages, np.uint8)
+    pt = _c(page_table, np.int32)
+    rs = _c(row_seq, np.int32)
+    cl = _c(context_lens, np.int32)
+    T, _, H, _ = q8.shape
+    if rows is None:
+        rows = np.arange(T, dtype=np.int64)
+    rows = _c(rows, np.int64)
+    Lmax = int(max(1, cl[rows].max() if rows.size else 1))
+    out = np.full((rows.shape[0], Lmax), np.nan, np.float64)
+    bnd = np.full((rows.shape[0], Lmax), np.nan, np.float64) if with_bound else None
+    st = lib().ref_logits_fp8(_p(q8, _u8p), _p(s8, _f32p), _p(w, _f32p), T, H, _p(pg, _u8p), pg.shape[0],
+                              _p(pt, _i32p), pt.shape[1], _p(rs, _i32p), _p(cl, _i32p), _p(rows, _i64p),
+                              rows.shape[0], Lmax, _p(out, _f64p), _p(bnd, _f64p) if bnd is not None else None)
     return out, bnd, int(st)
 
 
