@@ -121,6 +121,20 @@ int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int
                    int32_t* status_dev, void* stream);
 
 /*
+ * FP8 query pack -- the query side of the FP8 comparison path ([P2] Device memory and
+ * sizing: the 132 B/token FP8 entry the FP4 entry replaces).  RoPE and the Hadamard as in
+ * fp4idx_quant_q, then the K side's FP8 rule per (row, head): s = amax/448 (1 if amax = 0),
+ * e4m3 = RNE-satfinite(x / s).  The pages give only the K entry; this rule for the query is
+ * a reading.
+ *   q8 [n_rows,8,64,16] uint8: q8[t][c][h][i] = element 16c + i of head h (written)
+ *   q8_scale [n_rows,64] fp32 (written)
+ * n_heads must be 64.  Device error: BAD_POSITION.
+ */
+int fp4idx_quant_q_fp8(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
+                       const uint16_t* cos_sin, int32_t max_pos, uint8_t* q8, float* q8_scale, int32_t* status_dev,
+                       void* stream);
+
+/*
  * Q quant and head weights in one launch -- [P1] Summary: "a one-launch index-Q pack +
  * head weights", where indexer_head_weights runs a batch-invariant split-K bf16 GEMV whose
  * result stays in fp32.  The queries are packed exactly as fp4idx_quant_q packs them

@@ -2,7 +2,7 @@
 // stream.  No allocation, no synchronisation (except fp4idx_read_status).
 #include <cstdio>
 
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 #include "schedule.cuh"
 
 namespace {
@@ -91,6 +91,20 @@ int fp4idx_quant_q(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int
   if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
   return from_cuda(fp4idx::launch_quant_q(q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, status_dev,
                                           as_stream(stream)));
+}
+
+int fp4idx_quant_q_fp8(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,
+                       const uint16_t* cos_sin, int32_t max_pos, uint8_t* q8, float* q8_scale, int32_t* status_dev,
+                       void* stream) {
+  if (n_rows < 0 || max_pos <= 0) return FP4IDX_ERR_INVALID_ARG;
+  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (!q || !q_positions || !cos_sin || !q8 || !q8_scale) return FP4IDX_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(cos_sin) || !aligned16(q8) || !aligned4(q_positions) || !aligned4(q8_scale))
+    return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  return from_cuda(fp4idx::launch_quant_q_fp8(q, n_rows, q_positions, cos_sin, max_pos, q8, q8_scale, status_dev,
+                                              as_stream(stream)));
 }
 
 int fp4idx_quant_q_w(const uint16_t* q, int64_t n_rows, int32_t n_heads, const int32_t* q_positions,

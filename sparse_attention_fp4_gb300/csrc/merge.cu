@@ -14,7 +14,7 @@
 // global position order -- selects the k largest values of the compacted row with the
 // top-k kernel (ties to the lower slot, i.e. the lower position), and maps the selected
 // slots back to global indices, ascending.
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 
 namespace fp4idx {
 namespace {

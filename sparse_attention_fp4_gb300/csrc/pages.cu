@@ -13,7 +13,7 @@
 // (c, j) = (t / 64, t % 64) of the payload and, for t < 16, a 16-byte piece of the
 // scales, so every global access is a coalesced 16-byte access.  Page ids < 0 are
 // padding and skipped; ids >= num_pages record FP4IDX_ERR_BAD_PAGE and are skipped.
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 
 namespace fp4idx {
 namespace {

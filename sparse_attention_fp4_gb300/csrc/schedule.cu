@@ -10,7 +10,7 @@
 // Here: one CTA of 1024 threads walks the rows in chunks of 1024 with carried block
 // scans (registers fixed, any row count), entirely on the device: capturable, no host
 // synchronisation, a pure function of its inputs.
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 #include "schedule.cuh"
 
 #include <atomic>

@@ -20,7 +20,7 @@
 //   * UE8M0 per 32-element block (4 lanes): smallest e with 6*2^e >= amax, from the
 //     exponent/mantissa bits of amax; e2m1 by the hardware RNE-satfinite convert,
 //     the sign of zero taken from the input.
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 
 #include <atomic>
 
@@ -292,6 +292,50 @@ __global__ void __launch_bounds__(256) quant_q_kernel(
   quant_q_block(blockIdx.x, q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, status);
 }
 
+// FP8 query pack (the comparison path of the 132 B/token layout): per (row t, head h), RoPE
+// and the Hadamard as for the FP4 pack, then the K side's FP8 rule -- one fp32 scale
+// s = amax / 448 (1 when amax = 0) and e4m3 = RNE-satfinite(x / s).  Layout q8[t][c][h][16]
+// (chunk c = elements 16c .. 16c + 15), q8_scale[t][h].
+__global__ void __launch_bounds__(256) quant_q_fp8_kernel(
+    const uint16_t* __restrict__ q, int64_t n_rows, const int32_t* __restrict__ q_positions,
+    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ q8, float* __restrict__ q8_scale,
+    int32_t* status) {
+  const int lh = threadIdx.x & 15;
+  const int64_t th = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4);
+  const bool in_range = th < n_rows * kHeads;
+  const int64_t t = th >> 6;
+  const int h = (int)(th & 63);
+  int32_t pos = in_range ? __ldg(q_positions + t) : 0;
+  bool store = in_range;
+  if (in_range && (pos < 0 || pos >= max_pos)) {
+    if (lh == 0 && h == 0) record_error(status, FP4IDX_ERR_BAD_POSITION);
+    store = false;
+    pos = 0;
+  }
+  float v[8];
+  if (in_range) unpack_bf16x8(ldg16(q + th * kHeadDim + 8 * lh), v);
+  else {
+#pragma unroll
+    for (int e = 0; e < 8; e++) v[e] = 0.0f;
+  }
+  rope_row(v, cos_sin + (int64_t)pos * kRope, lh);
+  hadamard_row(v, lh);
+  float amax = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; e++) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint2 out;
+  out.x = e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) | (e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
+  out.y = e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) | (e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
+  if (store) {
+    // elements 8 lh .. 8 lh + 7: chunk lh / 2, bytes 8 (lh & 1) .. of that chunk's 16
+    *reinterpret_cast<uint2*>(q8 + ((t * 8 + (lh >> 1)) * kHeads + h) * 16 + 8 * (lh & 1)) = out;
+    if (lh == 0) q8_scale[t * kHeads + h] = s;
+  }
+}
+
 // Head weights of query row t: w[t][h] = w_scale * sum_d hidden[t][d] * w_proj[h][d], bf16
 // inputs, fp32 accumulation ([P1] Summary: indexer_head_weights runs a batch-invariant
 // split-K bf16 GEMV whose result stays in fp32).  A CTA takes row t and heads 8g .. 8g+7;
@@ -417,6 +461,14 @@ cudaError_t launch_quant_q(const uint16_t* q, int64_t n_rows, const int32_t* q_p
   if (e != cudaSuccess) return e;
   quant_q_kernel<<<grid_for(n_rows * kHeads), 256, 0, stream>>>(q, n_rows, q_positions, cos_sin, max_pos,
                                                                  q_payload, q_scale, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_q_fp8(const uint16_t* q, int64_t n_rows, const int32_t* q_positions, const uint16_t* cos_sin,
+                               int32_t max_pos, uint8_t* q8, float* q8_scale, int32_t* status, cudaStream_t stream) {
+  if (n_rows == 0) return cudaSuccess;
+  quant_q_fp8_kernel<<<grid_for(n_rows * kHeads), 256, 0, stream>>>(q, n_rows, q_positions, cos_sin, max_pos, q8,
+                                                                   q8_scale, status);
   return cudaGetLastError();
 }
 

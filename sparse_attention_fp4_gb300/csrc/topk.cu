@@ -25,7 +25,7 @@
 //      it: per thread a bit mask over a contiguous run of positions, one block scan of the
 //      mask counts, then the set bits are written out (straight to the output when there
 //      are no ties, else through a shared-memory stage).
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 
 #include <cooperative_groups.h>
 

@@ -26,7 +26,7 @@
 // corrupt each other's keys; order such calls on one stream.
 #include <mutex>
 
-#include "fp4idx_internal.cuh"
+#include "launchers.cuh"
 
 static __device__ __align__(256) unsigned char g_topk_noalloc_scratch[FP4IDX_TOPK_NOALLOC_MAX_BYTES];
 

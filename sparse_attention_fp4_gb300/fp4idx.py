@@ -56,6 +56,7 @@ _SIGS = {
     "fp4idx_store_k": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_store_k_fp8": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _f32, _vp, _i32, _vp, _i64, _vp, _vp]),
     "fp4idx_quant_q": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "fp4idx_quant_q_fp8": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "fp4idx_quant_q_w": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _f32, _vp, _vp, _vp, _vp,
                                         _vp]),
     "fp4idx_schedule_workspace_bytes": (_sz, [_i64, _i32]),
@@ -172,6 +173,16 @@ def quant_q(q, q_positions, cos_sin, q_payload, q_scale, status=None, stream=Non
         cos_sin.shape[0], _ptr(q_payload, "q_payload", _U8, T * 4096), _ptr(q_scale, "q_scale", _U8, T * 256),
         _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_quant_q", rc)
+
+
+def quant_q_fp8(q, q_positions, cos_sin, q8, q8_scale, status=None, stream=None):
+    """FP8 query pack: q8 [T, 8, 64, 16] uint8 and q8_scale [T, 64] fp32."""
+    T, H, D = q.shape
+    rc = _lib.fp4idx_quant_q_fp8(_ptr(q, "q", _BF16, T * H * D), T, H, _ptr(q_positions, "q_positions", _I32, T),
+                                 _ptr(cos_sin, "cos_sin", _BF16), cos_sin.shape[0], _ptr(q8, "q8", _U8, T * 8192),
+                                 _ptr(q8_scale, "q8_scale", _F32, T * NUM_HEADS),
+                                 _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_quant_q_fp8", rc)
 
 
 def quant_q_w(q, q_positions, cos_sin, hidden, w_proj, w_scale, q_payload, q_scale, w_out, status=None,
