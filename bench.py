@@ -913,13 +913,88 @@ def run_qpack(args):
                       "quant_q_w": res["quant_q_w"], "quant_q_alone": res["quant_q"]}), flush=True)
 
 
+def run_fp8_compare(args):
+    """The same-box FP4/FP8 comparison on the decode batch (64 rows, contexts 8k-32k tokens):
+    the logits launch over the split FP4 cache (68 B/token) and over the fused FP8 cache
+    (132 B/token), each captured alone in a graph and replayed with the L2 flushed before
+    every launch.  Bytes counted per launch: the K cache of every visible token once per
+    sequence, the packed queries (FP4 4,352 B/row; FP8 8,192 B + 256 B of scales), head
+    weights, page ids and row metadata."""
+    import torch
+    from sparse_attention_fp4_gb300 import fp4idx
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    b = make_batch("decode_b64")
+    st = DecodeStep(b, device)
+    ks = b.kstore
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    pages = torch.zeros((b.num_pages, fp4idx.FP8_PAGE_BYTES), dtype=torch.uint8, device=device)
+    chunk = 1 << 20
+    for r0 in range(0, ks.n_rows, chunk):
+        r1 = min(ks.n_rows, r0 + chunk)
+        fp4idx.store_k_fp8(bf(ks.k_rows[r0:r1]), torch.from_numpy(ks.positions[r0:r1]).to(device),
+                           torch.from_numpy(ks.slots[r0:r1]).to(device), st.norm_w, ks.eps, st.cs, pages,
+                           status=st.status)
+    T = st.T
+    q8 = torch.empty((T, 8, 64, 16), dtype=torch.uint8, device=device)
+    s8 = torch.empty((T, 64), dtype=torch.float32, device=device)
+    st.launch()  # FP4 queries and the schedule
+    fp4idx.quant_q_fp8(st.q, st.qpos, st.cs, q8, s8, status=st.status)
+    lg8 = torch.empty_like(st.logits)
+    calls = dict(st.calls())
+    L = b.context_lens.astype(np.int64)
+    seq_max = np.zeros(int(b.row_seq.max()) + 1, np.int64)
+    np.maximum.at(seq_max, b.row_seq.astype(np.int64), L)
+    meta = 256.0 * T + 4.0 * np.ceil(seq_max / 64.0).sum() + 8.0 * T
+    runs = {"fp4": (calls["logits"], 68.0 * seq_max.sum() + 4352.0 * T + meta, 68.0 * seq_max.sum()),
+            "fp8": (lambda: fp4idx.logits_fp8(q8, s8, st.w, pages, st.pt, st.rs, st.cl, st.max_ctx, st.sched, lg8,
+                                              status=st.status),
+                    132.0 * seq_max.sum() + 8448.0 * T + meta, 132.0 * seq_max.sum())}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    peak, peak_kind = measured_peaks()
+    res = {}
+    for name, (fn, nbytes, kbytes) in runs.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ts = []
+        for _ in range(min(args.steps, 500)):
+            flush.zero_()
+            torch.cuda._sleep(200000)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(ts)
+        res[name] = {"us": round(us, 2), "query_rows_per_s": round(T / (us * 1e-6), 1),
+                     "kcache_gbs": round(kbytes / (us * 1e-6) / 1e9, 1),
+                     "algorithmic_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac_of_%s_hbm" % peak_kind: round(nbytes / (us * 1e-6) / 1e9 / peak, 4),
+                     "algorithmic_bytes": nbytes}
+    assert fp4idx.read_status(st.status) == 0
+    print(json.dumps({"metric": "paged logits, FP8 132 B/token vs FP4 68 B/token cache, query rows/s",
+                      "value": res["fp8"]["query_rows_per_s"], "unit": "query rows/s", "n_gpus": 1,
+                      "higher_is_better": True, "dtype": "e4m3->f32 (fp8) / e2m1,ue8m0->f32 (fp4)",
+                      "data": "synthetic",
+                      "config": {"workload": b.name, "rows": T, "context_tokens": int(L.sum()),
+                                 "l2": "flushed before every launch", "timing": "median of graph replays"},
+                      "fp8": res["fp8"], "fp4": res["fp4"],
+                      "fp8_over_fp4_time": round(res["fp8"]["us"] / res["fp4"]["us"], 3)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["fp4idx", "reference"], default="fp4idx")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["kstore", "pages", "cp_merge", "qpack"], default="decode_b64")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["kstore", "pages", "cp_merge", "qpack", "fp8_compare"], default="decode_b64")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -936,6 +1011,8 @@ def main(argv=None):
         run_cp_merge(args)
     elif args.workload == "qpack":
         run_qpack(args)
+    elif args.workload == "fp8_compare":
+        run_fp8_compare(args)
     else:
         run_gpu(args)
 

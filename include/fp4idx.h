@@ -228,6 +228,29 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
                 int32_t* status_dev, void* stream);
 
 /*
+ * FP8 logits -- the read side of the FP8 comparison path ([P2] Device memory and sizing:
+ * the fused 132 B/token FP8 entry that the 68 B FP4 entry replaces), over the pages of
+ * fp4idx_store_k_fp8 and the queries of fp4idx_quant_q_fp8:
+ *   logits[t,s] = sum_h w[t,h] * ReLU(q[t,h] . k[s]),  s < context_lens[t],
+ * with q = e4m3(q8[t,.,h,.]) * q8_scale[t,h] and k = e4m3(token s's 128 bytes) * its fp32
+ * scale.  Tensor-core kernel (e4m3 x e4m3 -> f32); the two scales are applied in fp32
+ * after the dot products.
+ *   q8 [n_rows,8,64,16] uint8, q8_scale [n_rows,64] fp32, w [n_rows,64] fp32
+ *   fp8_pages [num_pages, 8448] uint8 (1 <= num_pages <= INT32_MAX)
+ *   page_table, row_seq, context_lens, max_context, schedule: as fp4idx_logits (the same
+ *   schedule serves both formats)
+ *   logits_out [n_rows, logits_stride] fp32: written for s < context_lens[t], NaN where
+ *   the token's page id is out of range; the rest of each row is not written.
+ * All pointers 16-byte aligned except page_table, row_seq, context_lens, logits_out and
+ * status_dev (4-byte).  Device errors: BAD_PAGE, BAD_LENGTH, TIMEOUT, SCHEDULE.
+ */
+int fp4idx_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t n_rows, int32_t n_heads,
+                      const uint8_t* fp8_pages, int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                      int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
+                      const void* schedule, size_t schedule_bytes, float* logits_out, int64_t logits_stride,
+                      int32_t* status_dev, void* stream);
+
+/*
  * fp4idx_topk_noalloc -- fp4idx_topk for callers that may not allocate device memory.
  * The pages this library follows have no counterpart: it is an interface addition.
  * A serving runtime that gives all of its memory to its own pool at start-up, or a

@@ -216,6 +216,26 @@ int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float*
                                status_dev, as_stream(stream));
 }
 
+int fp4idx_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t n_rows, int32_t n_heads,
+                      const uint8_t* fp8_pages, int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                      int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
+                      const void* schedule, size_t schedule_bytes, float* logits_out, int64_t logits_stride,
+                      int32_t* status_dev, void* stream) {
+  // the FP8 operands take the places of the FP4 ones in the common checks (all 16-byte aligned)
+  int st = check_logits_args(q8, reinterpret_cast<const uint8_t*>(q8_scale), w, n_rows, n_heads, fp8_pages, fp8_pages,
+                             num_pages, page_table, num_seqs, max_pages, row_seq, context_lens, max_context, schedule,
+                             schedule_bytes, status_dev);
+  if (st != FP4IDX_OK || n_rows == 0) return st;
+  if (!logits_out || !aligned4(logits_out) || logits_stride < max_context) return FP4IDX_ERR_INVALID_ARG;
+  if (num_pages < 1 || num_pages > INT32_MAX) return FP4IDX_ERR_INVALID_ARG;
+  int32_t grid = 0;
+  st = device_sms(&grid);
+  if (st != FP4IDX_OK) return st;
+  return from_cuda(fp4idx::launch_logits_fp8(q8, q8_scale, w, (int32_t)n_rows, fp8_pages, num_pages, page_table,
+                                             num_seqs, max_pages, context_lens, max_context, schedule, grid,
+                                             logits_out, logits_stride, status_dev, as_stream(stream)));
+}
+
 int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* context_lens, int64_t n_rows,
                 int32_t max_context, int32_t k, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                 int32_t* status_dev, void* stream) {

@@ -33,6 +33,11 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
                                const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
                                const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
                                int32_t* status, cudaStream_t stream);
+cudaError_t launch_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int32_t n_rows,
+                              const uint8_t* pages, int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                              int32_t max_pages, const int32_t* context_lens, int32_t max_context,
+                              const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
+                              int32_t* status, cudaStream_t stream);
 cudaError_t launch_dequant_pages(const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
                                  const int32_t* page_ids, int64_t n_pages, float* out, int32_t* status,
                                  cudaStream_t stream);

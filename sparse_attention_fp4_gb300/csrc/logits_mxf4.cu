@@ -431,12 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
           ptx::mma_commit(bar_kempty(sb, s));
         }
         if (!ok) break;
-        // this issuer is done with the item's queries: once its MMAs have read them, or at
-        // once when it issued none for this item
-        if (q_ready)
+        // this issuer is done with the item's queries: once its MMAs have read them, or, when
+        // it issued none for this item, once the item's rows are in place.  An arrival made
+        // before that would count toward the buffer's previous use, which the other issuer
+        // may still be reading, and let the producer overwrite it.
+        if (q_ready) {
           ptx::mma_commit(bar_qempty(sb, qb));
-        else
+        } else {
+          ok = poll(bar_qsf(sb, qb), (ictr >> 1) & 1, ctl, true);
+          if (!ok) break;
           ptx::mbar_arrive(bar_qempty(sb, qb));
+        }
         ictr++;
       }
     }

@@ -66,6 +66,8 @@ _SIGS = {
                                           _i32, _i32, _vp, _sz, _vp, _sz, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_logits": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
                                      _vp, _sz, _vp, _i64, _vp, _vp]),
+    "fp4idx_logits_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
+                                         _vp, _sz, _vp, _i64, _vp, _vp]),
     "fp4idx_topk_workspace_bytes": (_sz, [_i64, _i32]),
     "fp4idx_topk": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
     "fp4idx_topk_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _vp]),
@@ -246,6 +248,23 @@ def logits(q_payload, q_scale, w, payload, scale, page_table, row_seq, context_l
         _ptr(schedule, "schedule", _U8), schedule.numel(), _ptr(logits_out, "logits_out", _F32),
         logits_out.shape[1], _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_logits", rc)
+
+
+def logits_fp8(q8, q8_scale, w, fp8_pages, page_table, row_seq, context_lens, max_context, schedule, logits_out,
+               status=None, stream=None):
+    """Paged-MQA logits over the FP8 comparison cache (fp8_pages [P, 8448] u8) and the FP8
+    query pack (q8 [T, 8, 64, 16] u8, q8_scale [T, 64] f32)."""
+    T = q8.shape[0]
+    num_pages = fp8_pages.shape[0]
+    S, max_pages = page_table.shape
+    rc = _lib.fp4idx_logits_fp8(
+        _ptr(q8, "q8", _U8, T * 8192), _ptr(q8_scale, "q8_scale", _F32, T * NUM_HEADS),
+        _ptr(w, "w", _F32, T * NUM_HEADS), T, NUM_HEADS, _ptr(fp8_pages, "fp8_pages", _U8, num_pages * FP8_PAGE_BYTES),
+        num_pages, _ptr(page_table, "page_table", _I32), S, max_pages, _ptr(row_seq, "row_seq", _I32, T),
+        _ptr(context_lens, "context_lens", _I32, T), int(max_context), _ptr(schedule, "schedule", _U8),
+        schedule.numel(), _ptr(logits_out, "logits_out", _F32), logits_out.shape[1],
+        _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_logits_fp8", rc)
 
 
 def topk_workspace_bytes(max_rows, max_context) -> int:
