@@ -29,6 +29,7 @@ def lib():
         "fp4idx_dequant_pages": [V, V, I64, V, I64, V, V, V],
         "fp4idx_export_pages": [V, V, I64, V, I64, V, V, V, V],
         "fp4idx_import_pages": [V, V, V, I64, V, V, I64, V, V],
+        "fp4idx_logits_fp8": [V, V, V, I64, I32, V, I64, V, I64, I32, V, V, I32, V, SZ, V, I64, V, V],
         "fp4idx_read_status": [V, V, V],
     }
     for name, args in sig.items():
@@ -127,3 +128,21 @@ def test_status_strings(lib):
     assert len(set(names)) == 11 and "unknown status" not in names
     assert lib.fp4idx_status_string(99).decode() == "unknown status"
     assert lib.fp4idx_read_status(None, None, None) == INVALID
+
+
+def test_logits_fp8(lib):
+    f = lib.fp4idx_logits_fp8
+
+    def call(q8=A, s8=A, w=A, n=4, heads=64, pages=A, P=8, pt=A, rs=A, cl=A, max_ctx=256, sched=A, status=None):
+        return f(q8, s8, w, n, heads, pages, P, pt, 2, 4, rs, cl, max_ctx, sched, 1 << 20, A, 256, status, None)
+
+    assert call(n=-1) == INVALID
+    assert call(heads=32) == UNSUPPORTED
+    assert call(max_ctx=(1 << 30)) == UNSUPPORTED
+    assert call(n=0, q8=None, pages=None) == OK  # nothing to do
+    assert call(q8=None) == INVALID
+    assert call(pages=None) == INVALID
+    assert call(s8=M4) == INVALID      # q8_scale must be 16-byte aligned
+    assert call(pages=M4) == INVALID   # the tensor map wants a 16-byte aligned base
+    assert call(cl=M1) == INVALID
+    assert call(status=M1) == INVALID
