@@ -251,6 +251,20 @@ int fp4idx_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, 
                       int32_t* status_dev, void* stream);
 
 /*
+ * FP8 logits + top-k in one call: fp4idx_logits_fp8 into a logits buffer, then the
+ * selection of fp4idx_topk.  Workspace, k, topk_idx and logits_out (nullable) as in
+ * fp4idx_logits_topk; the other arguments as in fp4idx_logits_fp8.  A token on an
+ * out-of-range page has a NaN logit (status BAD_PAGE), and its place in the selection is
+ * then unspecified.
+ */
+int fp4idx_logits_topk_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t n_rows, int32_t n_heads,
+                           const uint8_t* fp8_pages, int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                           int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
+                           int32_t max_context, int32_t k, const void* schedule, size_t schedule_bytes,
+                           void* workspace, size_t workspace_bytes, int32_t* topk_idx, float* logits_out,
+                           int64_t logits_stride, int32_t* status_dev, void* stream);
+
+/*
  * fp4idx_topk_noalloc -- fp4idx_topk for callers that may not allocate device memory.
  * The pages this library follows have no counterpart: it is an interface addition.
  * A serving runtime that gives all of its memory to its own pool at start-up, or a

@@ -286,6 +286,45 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
                                        topk_idx, status_dev, s));
 }
 
+int fp4idx_logits_topk_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t n_rows, int32_t n_heads,
+                           const uint8_t* fp8_pages, int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
+                           int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
+                           int32_t max_context, int32_t k, const void* schedule, size_t schedule_bytes,
+                           void* workspace, size_t workspace_bytes, int32_t* topk_idx, float* logits_out,
+                           int64_t logits_stride, int32_t* status_dev, void* stream) {
+  int st = check_logits_args(q8, reinterpret_cast<const uint8_t*>(q8_scale), w, n_rows, n_heads, fp8_pages, fp8_pages,
+                             num_pages, page_table, num_seqs, max_pages, row_seq, context_lens, max_context, schedule,
+                             schedule_bytes, status_dev);
+  if (st != FP4IDX_OK) return st;
+  if (k < 1 || k > FP4IDX_MAX_TOPK) return FP4IDX_ERR_INVALID_ARG;
+  if (n_rows == 0) return FP4IDX_OK;
+  if (num_pages < 1 || num_pages > INT32_MAX) return FP4IDX_ERR_INVALID_ARG;
+  if (!topk_idx || !aligned4(topk_idx)) return FP4IDX_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return FP4IDX_ERR_INVALID_ARG;
+  if (workspace_bytes < fp4idx_logits_workspace_bytes(n_rows, max_context, k)) return FP4IDX_ERR_WORKSPACE;
+  float* buf;
+  int64_t stride;
+  if (logits_out) {
+    if (logits_stride < max_context || !aligned4(logits_out)) return FP4IDX_ERR_INVALID_ARG;
+    buf = logits_out;
+    stride = logits_stride;
+  } else {
+    stride = logits_row_stride(max_context);
+    buf = reinterpret_cast<float*>(workspace);
+  }
+  void* topk_ws = reinterpret_cast<uint8_t*>(workspace) + logits_region_bytes(n_rows, max_context);
+  cudaStream_t s = as_stream(stream);
+  int32_t grid = 0;
+  st = device_sms(&grid);
+  if (st != FP4IDX_OK) return st;
+  st = from_cuda(fp4idx::launch_logits_fp8(q8, q8_scale, w, (int32_t)n_rows, fp8_pages, num_pages, page_table,
+                                           num_seqs, max_pages, context_lens, max_context, schedule, grid, buf,
+                                           stride, status_dev, s));
+  if (st != FP4IDX_OK) return st;
+  return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_ws,
+                                       topk_idx, status_dev, s));
+}
+
 namespace {
 
 int check_page_args(const void* payload, const void* scale, int64_t num_pages, const int32_t* page_ids,

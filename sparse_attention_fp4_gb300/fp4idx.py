@@ -68,6 +68,8 @@ _SIGS = {
                                      _vp, _sz, _vp, _i64, _vp, _vp]),
     "fp4idx_logits_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
                                          _vp, _sz, _vp, _i64, _vp, _vp]),
+    "fp4idx_logits_topk_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
+                                              _i32, _vp, _sz, _vp, _sz, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_topk_workspace_bytes": (_sz, [_i64, _i32]),
     "fp4idx_topk": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
     "fp4idx_topk_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _i32, _vp, _vp, _vp]),
@@ -265,6 +267,24 @@ def logits_fp8(q8, q8_scale, w, fp8_pages, page_table, row_seq, context_lens, ma
         schedule.numel(), _ptr(logits_out, "logits_out", _F32), logits_out.shape[1],
         _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
     _check("fp4idx_logits_fp8", rc)
+
+
+def logits_topk_fp8(q8, q8_scale, w, fp8_pages, page_table, row_seq, context_lens, max_context, k, schedule,
+                    workspace, topk_idx, logits_out=None, status=None, stream=None):
+    """FP8 logits and the top-k selection in one call (workspace: logits_workspace_bytes)."""
+    T = q8.shape[0]
+    num_pages = fp8_pages.shape[0]
+    S, max_pages = page_table.shape
+    stride = logits_out.shape[1] if logits_out is not None else 0
+    rc = _lib.fp4idx_logits_topk_fp8(
+        _ptr(q8, "q8", _U8, T * 8192), _ptr(q8_scale, "q8_scale", _F32, T * NUM_HEADS),
+        _ptr(w, "w", _F32, T * NUM_HEADS), T, NUM_HEADS, _ptr(fp8_pages, "fp8_pages", _U8, num_pages * FP8_PAGE_BYTES),
+        num_pages, _ptr(page_table, "page_table", _I32), S, max_pages, _ptr(row_seq, "row_seq", _I32, T),
+        _ptr(context_lens, "context_lens", _I32, T), int(max_context), int(k), _ptr(schedule, "schedule", _U8),
+        schedule.numel(), _ptr(workspace, "workspace", _U8), workspace.numel(),
+        _ptr(topk_idx, "topk_idx", _I32, T * int(k)), _ptr(logits_out, "logits_out", _F32, nullable=True), stride,
+        _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
+    _check("fp4idx_logits_topk_fp8", rc)
 
 
 def topk_workspace_bytes(max_rows, max_context) -> int:

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from sparse_attention_fp4_gb300 import workloads as wl
-from tests.gpu_util import bf16, check_logits, dev, host
+from tests.gpu_util import bf16, check_logits, check_topk, check_topk_self, dev, host
 
 pytestmark = pytest.mark.gpu
 
@@ -21,8 +21,9 @@ def cs():
     return wl.rope_cos_sin_table()
 
 
-def run_fp8(b, cs_np, page_table=None):
-    """FP8 K store, FP8 query pack, schedule and FP8 logits, all on the GPU."""
+def run_fp8(b, cs_np, page_table=None, k=None):
+    """FP8 K store, FP8 query pack, schedule and FP8 logits, all on the GPU; with k, the
+    fused logits + top-k call instead (once with logits_out, once through the workspace)."""
     from sparse_attention_fp4_gb300 import fp4idx
     cs = bf16(cs_np)
     ks = b.kstore
@@ -40,9 +41,19 @@ def run_fp8(b, cs_np, page_table=None):
     fp4idx.build_schedule(cl, rs, sched)
     lg = torch.full((T, Lmax), float(UNWRITTEN), dtype=torch.float32, device="cuda")
     pt = dev(b.page_table if page_table is None else page_table)
-    fp4idx.logits_fp8(q8, s8, dev(b.w), pages, pt, rs, cl, Lmax, sched, lg, status=status)
+    sel = sel_ws = None
+    if k is None:
+        fp4idx.logits_fp8(q8, s8, dev(b.w), pages, pt, rs, cl, Lmax, sched, lg, status=status)
+    else:
+        ws = torch.empty(fp4idx.logits_workspace_bytes(T, Lmax, k), dtype=torch.uint8, device="cuda")
+        sel = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        sel_ws = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = dev(b.w)
+        fp4idx.logits_topk_fp8(q8, s8, w, pages, pt, rs, cl, Lmax, k, sched, ws, sel, logits_out=lg, status=status)
+        fp4idx.logits_topk_fp8(q8, s8, w, pages, pt, rs, cl, Lmax, k, sched, ws, sel_ws, status=status)
     torch.cuda.synchronize()
-    return dict(status=fp4idx.read_status(status), pages=host(pages), q8=host(q8), s8=host(s8), logits=host(lg))
+    return dict(status=fp4idx.read_status(status), pages=host(pages), q8=host(q8), s8=host(s8), logits=host(lg),
+                topk=None if sel is None else host(sel), topk_ws=None if sel_ws is None else host(sel_ws))
 
 
 def oracle_operands(b, cs_np):
@@ -115,3 +126,23 @@ def test_fp8_decode_batch_sampled_rows(cs):
     assert st == 0
     for i, t in enumerate(rows):
         check_logits(got["logits"][t], lg[i], bnd[i], int(b.context_lens[t]), "decode fp8 row %d" % t)
+
+
+@pytest.mark.parametrize("seed,lens,rps,k", [(21, [3000, 700, 1, 2500], 2, 256), (22, [5000, 33, 0, 64], 1, 2048),
+                                             (23, [128, 129, 4100], 3, 100)])
+def test_fp8_logits_topk_against_oracle(cs, seed, lens, rps, k):
+    """The fused FP8 call: the k highest oracle logits (up to swaps within tolerance of the
+    k-th), ascending, -1 padding; the same selection with and without logits_out."""
+    b = wl.small_batch(seed, lens, rows_per_seq=rps, topk=k)
+    got = run_fp8(b, cs, k=k)
+    assert got["status"] == 0
+    assert np.array_equal(got["topk"], got["topk_ws"])
+    pages, q8, s8 = oracle_operands(b, cs)
+    assert_same_operands(got, pages, q8, s8)
+    lg, bnd, st = oracle.logits_fp8(q8, s8, b.w, pages, b.page_table, b.row_seq, b.context_lens)
+    assert st == 0
+    for t in range(b.n_rows):
+        L = int(b.context_lens[t])
+        check_logits(got["logits"][t], lg[t], bnd[t], L, "fp8 row %d" % t)
+        check_topk(got["topk"][t], lg[t], bnd[t], L, k, "fp8 row %d" % t)
+        check_topk_self(got["topk"][t], got["logits"][t], L, k, "fp8 row %d" % t)
