@@ -6,15 +6,16 @@ wait for parity P succeeds while the barrier's current phase index has the other
 Such a wait cannot tell a phase from the one two later, so every waiter must be at most
 one phase behind the barrier it waits on.  The model keeps the kernels' ownership rules
 (producer warp pw fills the stages with kctr % producers == pw; MMA issuer m reads those
-with kctr % issuers == m; every issuer releases each item's query buffer once) and checks
-that no reader ever sees a buffer that holds another stage's or item's data, with the
-reads of an MMA spanning other warps' steps.
+with kctr % issuers == m; every issuer releases each item's query buffer once; an
+accumulator slot is rewritten only after every epilogue warp released its previous use)
+and checks that no reader ever sees a buffer that holds another stage's, item's or use's
+data, with the reads of an MMA or a tensor-memory load spanning other warps' steps.
 
-Two failures are planted in the model's configuration, not in any kernel: a stage ring
-whose size is not a multiple of the producer count, and the earlier query-buffer release
-(an issuer with no stage in an item arrived on the release barrier without waiting for
-the item's rows).  Both must be found; the configurations the two kernels use must run
-clean and never deadlock."""
+Three failures are planted in the model's configuration, not in any kernel: a stage ring
+whose size is not a multiple of the producer count, the earlier query-buffer release (an
+issuer with no stage in an item arrived on the release barrier without waiting for the
+item's rows), and a slot reused after all but one epilogue warp released it.  All must be
+found; the configurations the two kernels use must run clean and never deadlock."""
 import numpy as np
 import pytest
 
@@ -131,6 +132,48 @@ def query_buffers(n_buf, stages_per_item, wait_before_release, rng, n_issuers=2)
     schedule([producer()] + [issuer(m) for m in range(n_issuers)], rng)
 
 
+def acc_slots(n_slots, n_issuers, n_epi, items, rng, need_releases=None):
+    """Accumulator slots in tensor memory: per (stage, query row) a use u writes slot
+    u % n_slots once every epilogue warp has released the slot's previous use (a release
+    counter that only grows), and completes it on the slot's barrier; every epilogue warp
+    reads every use in order.  items: list of (stages, rows)."""
+    need = n_epi if need_releases is None else need_releases
+    accfull = [Bar(1) for _ in range(n_slots)]
+    released = [0] * n_slots
+    acc = [None] * n_slots
+
+    def issuer(m):
+        kctr = ucnt = 0
+        for n_st, rows in items:
+            for _ in range(n_st):
+                if kctr % n_issuers == m:
+                    for r in range(rows):
+                        u = ucnt + r
+                        slot = u % n_slots
+                        yield lambda: released[slot] >= need * (u // n_slots)
+                        acc[slot] = u  # the MMAs of this use start writing
+                        yield None
+                        accfull[slot].arrive()
+                kctr += 1
+                ucnt += rows
+
+    def epilogue():
+        u = 0
+        for n_st, rows in items:
+            for _ in range(n_st * rows):
+                slot = u % n_slots
+                yield lambda: accfull[slot].parity_done((u // n_slots) & 1)
+                if acc[slot] != u:
+                    raise Violation("slot %d read as use %d holds %r" % (slot, u, acc[slot]))
+                yield None  # tensor-memory load in flight
+                if acc[slot] != u:
+                    raise Violation("slot %d overwritten under use %d" % (slot, u))
+                released[slot] += 1
+                u += 1
+
+    schedule([issuer(m) for m in range(n_issuers)] + [epilogue() for _ in range(n_epi)], rng)
+
+
 def runs(fn, trials, seed):
     """(violations, deadlocks) over `trials` random schedules of fn(rng)."""
     rng = np.random.default_rng(seed)
@@ -168,4 +211,20 @@ def test_query_release_after_the_rows_landed_is_safe(n_buf):
 @pytest.mark.parametrize("n_buf", [2, 1])
 def test_early_query_release_is_caught(n_buf):
     v, _ = runs(lambda rng: query_buffers(n_buf, _items(rng), False, rng), 400, 4)
+    assert v > 0
+
+
+def _groups(rng):
+    # (stages, query rows) per item: decode items (one row) and draft groups (up to six)
+    n = int(rng.integers(3, 8))
+    return [(int(rng.integers(1, 4)), int(rng.integers(1, 7))) for _ in range(n)]
+
+
+def test_accumulator_slots_of_the_kernels_are_safe():
+    # both kernels: three slots, two issuers, eight epilogue warps (four here keep it small)
+    assert runs(lambda rng: acc_slots(3, 2, 4, _groups(rng), rng), 200, 5) == (0, 0)
+
+
+def test_accumulator_slot_reused_before_every_release_is_caught():
+    v, _ = runs(lambda rng: acc_slots(3, 2, 4, _groups(rng), rng, need_releases=3), 200, 6)
     assert v > 0
