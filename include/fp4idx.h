@@ -30,6 +30,10 @@
  *     context length above the stated maximum, a pipeline wait that ran out).
  *     They skip the offending access and never trap.
  *   - Fixed shapes: head_dim 128, 64 indexer heads, 64 tokens per cache page.
+ *   - One device per process: the logits kernels' shared-memory size attribute is
+ *     set on the first call and not again, so a process that also calls on a second
+ *     device gets FP4IDX_ERR_CUDA from the logits entry points there.  Make the
+ *     first logits call of a process outside stream capture.
  *
  * Cache layout (split, [P2] Motivation): per physical page p and token j < 64,
  *   payload[p][c][j][0..15]  (uint8, [num_pages,4,64,16]; 64 B per token)
