@@ -30,6 +30,8 @@ def lib():
         "fp4idx_export_pages": [V, V, I64, V, I64, V, V, V, V],
         "fp4idx_import_pages": [V, V, V, I64, V, V, I64, V, V],
         "fp4idx_logits_fp8": [V, V, V, I64, I32, V, I64, V, I64, I32, V, V, I32, V, SZ, V, I64, V, V],
+        "fp4idx_logits_topk_fp8": [V, V, V, I64, I32, V, I64, V, I64, I32, V, V, I32, I32, V, SZ, V, SZ, V, V, I64,
+                                   V, V],
         "fp4idx_read_status": [V, V, V],
     }
     for name, args in sig.items():
@@ -145,4 +147,20 @@ def test_logits_fp8(lib):
     assert call(s8=M4) == INVALID      # q8_scale must be 16-byte aligned
     assert call(pages=M4) == INVALID   # the tensor map wants a 16-byte aligned base
     assert call(cl=M1) == INVALID
+    assert call(status=M1) == INVALID
+
+
+def test_logits_topk_fp8(lib):
+    f = lib.fp4idx_logits_topk_fp8
+
+    def call(q8=A, s8=A, n=4, heads=64, pages=A, max_ctx=256, k=16, status=None):
+        return f(q8, s8, A, n, heads, pages, 8, A, 2, 4, A, A, max_ctx, k, A, 1 << 20, A, 1 << 24, A, None, 0,
+                 status, None)
+
+    assert call(n=-1) == INVALID
+    assert call(heads=128) == UNSUPPORTED
+    assert call(max_ctx=(1 << 30)) == UNSUPPORTED
+    assert call(q8=None) == INVALID
+    assert call(s8=M4) == INVALID
+    assert call(pages=M1) == INVALID
     assert call(status=M1) == INVALID
