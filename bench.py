@@ -34,7 +34,6 @@ UNIT = "query rows/s"
 L2_FLUSH_BYTES = 256 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_decode_b64_traffic.json")
 LOGITS_SRC = os.path.join(ROOT, "sparse_attention_fp4_gb300", "csrc", "logits_mxf4.cu")
-KERNELS_PER_STEP = 5  # store_k, quant_q, build_schedule, logits, top-k (the fused call needs no clearing launch)
 
 WORKLOADS = {
     "decode_b64": ("decode_batch64", 1001),
@@ -114,7 +113,7 @@ def algorithmic_bytes(b):
     return dict(k_cache=kbytes, logits_pass=logits_pass, topk_out=4.0 * T * b.topk)
 
 
-LOGITS_DEPS = ("logits_mxf4.cu", "ptx.cuh", "schedule.cuh", "fp4idx_internal.cuh")
+LOGITS_DEPS = ("logits_mxf4.cu", "ptx.cuh", "schedule.cuh", "fp4idx_internal.cuh", "select.cuh", "pipeline.cuh")
 
 
 def kernel_source_hash():
@@ -273,16 +272,24 @@ class DecodeStep:
                                    device=device)
         self.fused_ws = torch.empty(fp4idx.logits_workspace_bytes(self.T, self.max_ctx, self.k), dtype=torch.uint8,
                                     device=device)
+        self.fused = self.T <= fp4idx.num_sms()  # fp4idx_logits_topk selects inside the logits launch
         torch.cuda.synchronize(device)
 
     def calls(self):
-        """The five launches of a step, in order, as (name, callable)."""
+        """The launches of a step, in order, as (name, callable).  With at most one row per
+        SM the read side is the fused call (one launch: logits and the selection); larger
+        batches issue the logits and the top-k launch as the fused entry point does for
+        them."""
         f = self.fp4idx
-        return [
+        base = [
             ("store_k", lambda: f.store_k(self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.cs,
                                           self.payload, self.scale, status=self.status)),
             ("quant_q", lambda: f.quant_q(self.q, self.qpos, self.cs, self.qp, self.qs, status=self.status)),
             ("build_schedule", lambda: f.build_schedule(self.cl, self.rs, self.sched)),
+        ]
+        if self.fused:
+            return base + [("logits_topk", self.logits_topk)]
+        return base + [
             ("logits", lambda: f.logits(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
                                         self.max_ctx, self.sched, self.logits, status=self.status)),
             ("topk", lambda: f.topk(self.logits, self.cl, self.max_ctx, self.k, self.topk_ws, self.topk,
@@ -290,8 +297,8 @@ class DecodeStep:
         ]
 
     def logits_topk(self):
-        """The fused entry point a caller uses for the read side: logits into the
-        workspace, then the top-k selection (whose counters the logits launch clears)."""
+        """The read side's entry point as a caller uses it: paged-MQA logits and the top-k
+        selection in one call (fp4idx_logits_topk)."""
         self.fp4idx.logits_topk(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
                                 self.max_ctx, self.k, self.sched, self.fused_ws, self.topk, status=self.status)
 
@@ -299,45 +306,39 @@ class DecodeStep:
         for _, fn in self.calls():
             fn()
 
-    def launch_user(self):
-        """The step as a caller issues it, in order on one stream: schedule, K store, Q
-        quant, then the fused logits + top-k call."""
-        calls = dict(self.calls())
-        for name in ("build_schedule", "store_k", "quant_q"):
-            calls[name]()
-        self.logits_topk()
-
     def launch_forked(self, side_streams, marks=None):
         """The step with its independent launches overlapped: K store, Q quant and the
         schedule depend on nothing but their inputs, so they run on three streams, and the
-        fused logits + top-k call waits for all three (the form captured into the step's
-        graph).  With `marks` (three timing events) the read side is issued as its two
-        separate calls instead, with the marks recorded before the logits, between logits
-        and top-k, and after the top-k."""
+        read side waits for all three (the form captured into the step's graph).  With
+        `marks` (timing events, one more than the read side's launches) the read side's
+        launches are issued one by one with a mark before each and after the last."""
         import torch
-        calls = dict(self.calls())
+        calls = self.calls()
         cur = torch.cuda.current_stream()
         start = torch.cuda.Event()
         start.record(cur)
         done = []
+        branch = dict(calls[:3])
         # the longest branch first: a graph starts its root branches one after another
         for name, st in zip(("build_schedule", "store_k", "quant_q"), side_streams):
             st.wait_event(start)
             with torch.cuda.stream(st):
-                calls[name]()
+                branch[name]()
                 ev = torch.cuda.Event()
                 ev.record(st)
             done.append(ev)
         for ev in done:
             cur.wait_event(ev)
-        if marks:  # separate calls, so that each kernel can be timed
-            marks[0].record(cur)
-            calls["logits"]()
-            marks[1].record(cur)
-            calls["topk"]()
-            marks[2].record(cur)
+        if marks:
+            for i, (_, fn) in enumerate(calls[3:]):
+                marks[i].record(cur)
+                fn()
+            marks[len(calls) - 3].record(cur)
         else:
             self.logits_topk()
+
+    def read_side_names(self):
+        return [n for n, _ in self.calls()[3:]]
 
 
 def run_gpu(args):
@@ -373,10 +374,11 @@ def run_gpu(args):
     side = [torch.cuda.Stream(device) for _ in range(3)]
     with torch.cuda.graph(g):
         st.launch_forked(side)
-    # an instrumented copy of the step: event-record nodes around its logits and top-k
-    # launches (the marks slow a step a little, so the timed loop replays the plain graph)
+    # an instrumented copy of the step: event-record nodes around each launch of the read
+    # side (the marks slow a step a little, so the timed loop replays the plain graph)
+    names = st.read_side_names()
     try:
-        marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
         gm = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gm):
             st.launch_forked(side, marks)
@@ -412,15 +414,15 @@ def run_gpu(args):
 
     # kernel times inside the step, from the instrumented graph (same flush and spin)
     Kb = min(K, 500)
-    live = {"logits": [], "topk": []}
+    live = {n: [] for n in names}
     if marks:
         for i in range(Kb):
             flush_l2()
             torch.cuda._sleep(spin_cycles)
             gm.replay()
-            marks[2].synchronize()  # every replay re-records the marks: read them now
-            live["logits"].append(marks[0].elapsed_time(marks[1]) * 1e3)
-            live["topk"].append(marks[1].elapsed_time(marks[2]) * 1e3)
+            marks[-1].synchronize()  # every replay re-records the marks: read them now
+            for j, n in enumerate(names):
+                live[n].append(marks[j].elapsed_time(marks[j + 1]) * 1e3)
 
     # per-kernel breakdown: each launch captured in its own graph and replayed alone
     # (L2 flushed, a spin kernel ahead of it so no host time falls inside the events)
@@ -444,30 +446,34 @@ def run_gpu(args):
             per_times[name].append((e0, e1))
     torch.cuda.synchronize()
     per = {n: statistics.median([a.elapsed_time(b) for a, b in v]) * 1e3 for n, v in per_times.items()}
+    main = names[0]  # the logits launch (with the fused selection when the batch takes it)
     if marks:
-        logits_us = statistics.mean(live["logits"])
+        logits_us = statistics.mean(live[main])
         live_us = {n: {"mean": round(statistics.mean(v), 2), "median": round(statistics.median(v), 2)}
                    for n, v in live.items()}
         timing_src = ("event-record nodes around the launch inside an instrumented copy of the step graph, "
-                      "mean over %d replays (L2 flushed before each)" % len(live["logits"]))
+                      "mean over %d replays (L2 flushed before each)" % len(live[main]))
     else:
-        logits_us = statistics.mean([a.elapsed_time(b) for a, b in per_times["logits"]]) * 1e3
+        logits_us = statistics.mean([a.elapsed_time(b) for a, b in per_times[main]]) * 1e3
         live_us = None
         timing_src = "the launch captured alone in a graph (includes the graph launch), mean"
     status = st.fp4idx.read_status(st.status)
 
     ab = algorithmic_bytes(b)
     peak, peak_kind = measured_peaks()
-    achieved = ab["logits_pass"] / (logits_us * 1e-6) / 1e9
+    # the fused launch also writes the selection (4 B an index)
+    main_bytes = ab["logits_pass"] + (ab["topk_out"] if st.fused else 0.0)
+    achieved = main_bytes / (logits_us * 1e-6) / 1e9
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
             tr = json.load(f)
         if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == args.workload:
             traffic = tr.get("dram_bytes_per_launch")
+    kname = "logits_mxf4_kernel" + (" (with the fused top-k selection)" if st.fused else "")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": "logits_mxf4_kernel",
-                "algorithmic_bytes": ab["logits_pass"], "avg_launch_us": round(logits_us, 2),
+                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
+                "algorithmic_bytes": main_bytes, "avg_launch_us": round(logits_us, 2),
                 "launch_timing": timing_src,
                 "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
     if args.workload == "prefill":
@@ -477,7 +483,7 @@ def run_gpu(args):
         tpk, tpk_src = measured_fp4_tflops()
         tach = fl / (logits_us * 1e-6) / 1e12
         roofline = {"bound": "tensor", "achieved": round(tach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
-                    "frac": round(tach / tpk, 4), "traffic": traffic, "kernel": "logits_mxf4_kernel",
+                    "frac": round(tach / tpk, 4), "traffic": traffic, "kernel": kname,
                     "algorithmic_flops": fl, "avg_launch_us": round(logits_us, 2), "launch_timing": timing_src,
                     "peak_source": tpk_src}
 
@@ -503,7 +509,7 @@ def run_gpu(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": KERNELS_PER_STEP * K,
+            "gpu_launches": len(st.calls()) * K,
             "clocks": clocks,
             "wall_s_timed_region": round(t_wall, 3),
             "device_status": status,

@@ -30,10 +30,10 @@
  *     context length above the stated maximum, a pipeline wait that ran out).
  *     They skip the offending access and never trap.
  *   - Fixed shapes: head_dim 128, 64 indexer heads, 64 tokens per cache page.
- *   - One device per process: the logits kernels' shared-memory size attribute is
- *     set on the first call and not again, so a process that also calls on a second
- *     device gets FP4IDX_ERR_CUDA from the logits entry points there.  Make the
- *     first logits call of a process outside stream capture.
+ *   - Devices: calls run on the current device.  The first call of a kernel on each
+ *     device sets that kernel's shared-memory size attribute there (once per device,
+ *     thread-safe), so make the first call of each entry point on a device outside
+ *     stream capture.
  *
  * Cache layout (split, [P2] Motivation): per physical page p and token j < 64,
  *   payload[p][c][j][0..15]  (uint8, [num_pages,4,64,16]; 64 B per token)
@@ -73,7 +73,8 @@ typedef enum {
   FP4IDX_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its iteration limit */
   FP4IDX_ERR_BAD_POSITION = 7, /* device: RoPE position outside [0, max_pos) */
   FP4IDX_ERR_BAD_LENGTH = 8,   /* device: context length < 0 or above max_context / page-table width */
-  FP4IDX_ERR_SCHEDULE = 9,     /* schedule built for another row count or grid */
+  FP4IDX_ERR_SCHEDULE = 9,     /* schedule built for another row count or grid, or its selection
+                                  counters were left non-zero by a call that failed: rebuild it */
   FP4IDX_ERR_SCRATCH_LIMIT = 10 /* fp4idx_topk_noalloc: the call needs more than its fixed scratch */
 } fp4idx_status;
 
@@ -174,6 +175,9 @@ int fp4idx_quant_q_w(const uint16_t* q, int64_t n_rows, int32_t n_heads, const i
  *                                of one sequence that are adjacent share K tiles
  *   num_ctas                     grid the logits kernel will use (0 = SM count)
  *   schedule     device buffer of at least fp4idx_schedule_workspace_bytes(n_rows, num_ctas)
+ * Besides the work split, the schedule holds one counter per group of rows that
+ * fp4idx_logits_topk's fused selection counts up and puts back to zero; the build
+ * zeroes them.
  */
 size_t fp4idx_schedule_workspace_bytes(int64_t max_rows, int32_t num_ctas);
 int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int64_t n_rows,
@@ -191,22 +195,31 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
  *   row_seq, context_lens  as given to fp4idx_build_schedule (same arrays)
  *   max_context         host-known upper bound of context_lens (<= FP4IDX_MAX_CONTEXT)
  *   k                   1..FP4IDX_MAX_TOPK
- *   schedule            built by fp4idx_build_schedule for these rows
+ *   schedule            built by fp4idx_build_schedule for these rows.  When n_rows is
+ *                       at most the device's SM count the logits launch also selects:
+ *                       the CTA that writes the last tile of a row's group counts it
+ *                       complete on the group's counter in the schedule and selects the
+ *                       group's rows from the logits the launch wrote, so there is no
+ *                       second launch.  The call leaves the counters at zero; calls that
+ *                       share one schedule must therefore be ordered (one stream), and
+ *                       after a call that reported an error, rebuild the schedule.
+ *                       Larger batches run the logits launch, then the top-k launch of
+ *                       fp4idx_topk (one CTA per row).  Both give the same selection.
  *   workspace           >= fp4idx_logits_workspace_bytes(n_rows, max_context, k) bytes:
  *                       a logits buffer (unused when logits_out is given) and the
- *                       top-k scratch
+ *                       selection's scratch; nothing in it needs to be initialised
  *   topk_idx  [n_rows,k] int32 (written): the k highest-logit token indices of each
  *             row in ascending order; all of them when context_len <= k; -1 pads.
  *   logits_out [n_rows, logits_stride] fp32 (nullable): when given, receives
  *             logits[t,s] for s < context_lens[t] (the rest is not written).
  * Device errors: BAD_PAGE (page id out of range: the tile is skipped),
- * BAD_LENGTH, TIMEOUT, SCHEDULE.
+ * BAD_LENGTH, TIMEOUT (the rows of the CTA that gave up are not selected), SCHEDULE.
  */
 size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int32_t k);
 int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
                        int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
                        const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
-                       const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
+                       const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
                        size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                        float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream);
 
@@ -277,15 +290,22 @@ int fp4idx_logits_topk_fp8(const uint8_t* q8, const float* q8_scale, const float
  *
  * Same arguments and result as fp4idx_topk, without workspace/workspace_bytes.  The
  * top-k scratch is a fixed array of the library's device code,
- * FP4IDX_TOPK_NOALLOC_MAX_BYTES per device; no call allocates or frees anything.
+ * FP4IDX_TOPK_NOALLOC_MAX_BYTES per device; no call allocates or frees anything
+ * itself (but see the set-up below).
  *   - Limit: fp4idx_topk_workspace_bytes(n_rows, max_context) must not exceed
  *     FP4IDX_TOPK_NOALLOC_MAX_BYTES (any row count fits at max_context <= 32768, up to
  *     128 rows at 65536); a larger call returns FP4IDX_ERR_SCRATCH_LIMIT and enqueues
  *     nothing.
  *   - Setup: the first valid call on each device (with that device current) looks up
- *     the array's address once; make that first call before any stream capture begins.
- *     Of the conventions at the top of this file, the one on graph capture is not
- *     stated for this entry point.
+ *     the array's address once.  Under CUDA's default lazy module loading that is also
+ *     when the array's memory is committed on the device, so the first call can fail
+ *     for lack of memory and may synchronise: make it at start-up, before a memory pool
+ *     reserves the device's memory and before any stream capture begins.  A call with
+ *     n_rows = 0 (other pointers may then be null) does the set-up and nothing else.
+ *     Argument errors are reported before the set-up is attempted.  The address is
+ *     kept for the life of the process; after cudaDeviceReset the entry point must not
+ *     be used on that device again.  Of the conventions at the top of this file, the
+ *     one on graph capture is not stated for this entry point.
  *   - Nothing in the array needs to start at zero: a call writes every key it
  *     reads back.
  *   - All calls on a device share the array: calls whose kernels may overlap (unordered
@@ -346,6 +366,19 @@ int fp4idx_topk_values(const float* logits, int64_t logits_stride, const int32_t
                        float* values, void* stream);
 int fp4idx_topk_merge(const float* cand_values, const int32_t* cand_idx, int64_t n_rows, int32_t n_shards, int32_t k,
                       void* workspace, size_t workspace_bytes, int32_t* topk_idx, int32_t* status_dev, void* stream);
+
+/*
+ * Test support for the logits kernels' bounded waits (failure detection), with no
+ * counterpart on the pages.  Every wait of a logits pipeline gives up after
+ * wait_limit_ns (0 restores the default, 2 s): the CTA then records FP4IDX_ERR_TIMEOUT
+ * in status_dev, lets the copies it issued land, frees its tensor memory and returns,
+ * and the context stays usable.  idle_producers != 0 tells the producer warps of
+ * later logits launches to issue nothing, so that every launch ends in that timeout;
+ * a test sets it with a short limit, checks the status, and calls
+ * fp4idx_test_pipeline_waits(0, 0) to restore normal operation.  Process-wide; host
+ * only (takes effect at the next launch).
+ */
+int fp4idx_test_pipeline_waits(int32_t idle_producers, int64_t wait_limit_ns);
 
 /* Copy the device status word to *host_out (host pointer).  Synchronises `stream`:
  * a test/diagnostic helper, not for the hot path. */

@@ -157,10 +157,18 @@ size_t fp4idx_topk_workspace_bytes(int64_t max_rows, int32_t max_context) {
   return fp4idx::topk_workspace_bytes(max_rows, max_context);
 }
 
+// Scratch after the logits region: the top-k kernel's (separate selection) or the fused
+// selection's (the sort keys of positions past what a CTA keeps in shared memory).
+inline size_t select_scratch_bytes(int64_t rows, int32_t max_context) {
+  const size_t a = fp4idx::topk_workspace_bytes(rows, max_context);
+  const size_t b = fp4idx::logits_select_spill_bytes(rows, max_context);
+  return a > b ? a : b;
+}
+
 size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int32_t k) {
   (void)k;
   if (max_rows < 0 || max_context < 0) return 0;
-  return logits_region_bytes(max_rows, max_context) + fp4idx::topk_workspace_bytes(max_rows, max_context);
+  return logits_region_bytes(max_rows, max_context) + select_scratch_bytes(max_rows, max_context);
 }
 
 namespace {
@@ -190,14 +198,14 @@ int check_logits_args(const uint8_t* q_payload, const uint8_t* q_scale, const fl
 int launch_logits_checked(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
                           const uint8_t* payload, const uint8_t* scale, int64_t num_pages, const int32_t* page_table,
                           int64_t num_seqs, int32_t max_pages, const int32_t* row_seq, const int32_t* context_lens,
-                          int32_t max_context, const void* schedule, float* buf, int64_t stride, int32_t* status_dev,
-                          cudaStream_t s) {
+                          int32_t max_context, const void* schedule, float* buf, int64_t stride, int32_t k,
+                          int32_t* topk_idx, void* spill, int32_t* status_dev, cudaStream_t s) {
   int32_t grid = 0;
   int st = device_sms(&grid);
   if (st != FP4IDX_OK) return st;
   return from_cuda(fp4idx::launch_logits_mxf4(q_payload, q_scale, w, (int32_t)n_rows, payload, scale, num_pages,
                                               page_table, num_seqs, max_pages, row_seq, context_lens, max_context,
-                                              schedule, grid, buf, stride, status_dev, s));
+                                              schedule, grid, buf, stride, k, topk_idx, spill, status_dev, s));
 }
 
 }  // namespace
@@ -212,8 +220,8 @@ int fp4idx_logits(const uint8_t* q_payload, const uint8_t* q_scale, const float*
   if (st != FP4IDX_OK || n_rows == 0) return st;
   if (!logits_out || !aligned4(logits_out) || logits_stride < max_context) return FP4IDX_ERR_INVALID_ARG;
   return launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs,
-                               max_pages, row_seq, context_lens, max_context, schedule, logits_out, logits_stride,
-                               status_dev, as_stream(stream));
+                               max_pages, row_seq, context_lens, max_context, schedule, logits_out, logits_stride, 0,
+                               nullptr, nullptr, status_dev, as_stream(stream));
 }
 
 int fp4idx_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t n_rows, int32_t n_heads,
@@ -256,7 +264,7 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
 int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
                        int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
                        const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
-                       const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
+                       const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
                        size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                        float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream) {
   int st = check_logits_args(q_payload, q_scale, w, n_rows, n_heads, payload, scale, num_pages, page_table, num_seqs,
@@ -279,8 +287,21 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
   }
   void* topk_ws = reinterpret_cast<uint8_t*>(workspace) + logits_region_bytes(n_rows, max_context);
   cudaStream_t s = as_stream(stream);
+  int32_t sms = 0;
+  st = device_sms(&sms);
+  if (st != FP4IDX_OK) return st;
+  if (n_rows <= sms) {
+    // Few rows (decode): the logits launch selects too.  The CTA that completes a row
+    // selects it from the logits the launch wrote, with no second launch.
+    return launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs,
+                                 max_pages, row_seq, context_lens, max_context, schedule, buf, stride, k, topk_idx,
+                                 topk_ws, status_dev, s);
+  }
+  // Many rows (draft batches, prefill chunks): one CTA of the top-k launch per row
+  // selects with the whole GPU's parallelism.
   st = launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs, max_pages,
-                             row_seq, context_lens, max_context, schedule, buf, stride, status_dev, s);
+                             row_seq, context_lens, max_context, schedule, buf, stride, 0, nullptr, nullptr,
+                             status_dev, s);
   if (st != FP4IDX_OK) return st;
   return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_ws,
                                        topk_idx, status_dev, s));

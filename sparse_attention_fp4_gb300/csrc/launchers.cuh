@@ -2,9 +2,28 @@
 // launchers that compose others.
 #pragma once
 
+#include <cuda.h>
+
 #include "fp4idx_internal.cuh"
 
 namespace fp4idx {
+
+// ---------------------------------------------------------------- shared host helpers (host_util.cu)
+// cuTensorMapEncodeTiled, looked up once through the runtime.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+// 2-D view of `rows` rows of `row_bytes` bytes as uint64 elements; box = one row.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, uint32_t row_bytes);
+// A kernel's dynamic shared-memory limit, set once per (kernel, device); thread-safe.
+cudaError_t set_smem_attr_once(const void* kernel, size_t bytes);
+// How long one pipeline wait of the logits kernels may last before the kernel records
+// FP4IDX_ERR_TIMEOUT and winds down, and whether their producers are told to issue
+// nothing (a test switch, off by default: with it on, every launch ends in that timeout).
+constexpr int64_t kDefaultWaitLimitNs = 2000000000;
+uint64_t pipeline_wait_limit_ns();
+bool pipeline_idle_producers();
 
 // ---------------------------------------------------------------- launchers (host)
 cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
@@ -32,7 +51,10 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
                                const int32_t* page_table, int64_t num_seqs, int32_t max_pages,
                                const int32_t* row_seq, const int32_t* context_lens, int32_t max_context,
                                const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
-                               int32_t* status, cudaStream_t stream);
+                               int32_t k, int32_t* topk, void* spill, int32_t* status, cudaStream_t stream);
+// Scratch of the fused selection (k > 0 in launch_logits_mxf4): the sort keys of row
+// positions past what one CTA keeps in shared memory.  Nothing in it needs initialising.
+size_t logits_select_spill_bytes(int64_t n_rows, int32_t max_context);
 cudaError_t launch_logits_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int32_t n_rows,
                               const uint8_t* pages, int64_t num_pages, const int32_t* page_table, int64_t num_seqs,
                               int32_t max_pages, const int32_t* context_lens, int32_t max_context,

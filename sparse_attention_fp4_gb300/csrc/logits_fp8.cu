@@ -29,6 +29,7 @@
 
 #include "fp4idx_internal.cuh"
 #include "launchers.cuh"
+#include "pipeline.cuh"
 #include "ptx.cuh"
 #include "schedule.cuh"
 
@@ -50,8 +51,11 @@ constexpr int kWarpMma = kProducers, kWarpEpi0 = kProducers + kMmaWarps + kIdleW
 static_assert(kStages % kProducers == 0 && kStages % kMmaWarps == 0, "stage ownership");
 static_assert(kEpiWarps == 8 && kWarpEpi0 % 4 == 0, "four consecutive warps per epilogue half, quad = warp % 4");
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr uint32_t kSuspendNs = 20000;
+using pipe::Ctl;
+using pipe::poll;
+using pipe::prefetch_l2;
+using pipe::wait_lane0;
+using pipe::wait_warp;
 
 constexpr uint32_t kPageBytes = 8448;   // 64 x 128 B e4m3, then 64 x 4 B fp32 scales
 constexpr uint32_t kScaleOff = 8192;
@@ -98,57 +102,13 @@ struct LogitsFp8Params {
   float* out;
   int64_t out_stride;
   int32_t* status;
+  uint64_t wait_limit_ns;  // how long one pipeline wait may last
+  int32_t idle_producers;  // test switch: the producers issue nothing (every wait then runs out)
 };
 
-struct Ctl {
-  volatile int32_t* abort;
-  int32_t* status;
-};
-
-// Bounded poll of an mbarrier phase by the calling thread (suspended between probes).
-// False on timeout, which raises the abort flag, or, when honor_abort, once another warp
-// has aborted.
-__device__ __forceinline__ bool poll(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
-    if ((it & 7u) == 0) {
-      if (honor_abort && *c.abort) return false;
-      if (ptx::globaltimer() - t0 > kTimeoutNs) {
-        *c.abort = 1;
-        record_error(c.status, FP4IDX_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// Bounded wait, by one thread, until the counter at `a` has reached `need` (wrap-safe).
+// Bounded wait, by one thread, until the shared-memory counter at `a` has reached `need`.
 __device__ __forceinline__ bool wait_count(uint32_t a, uint32_t need, const Ctl& c) {
-  if ((int32_t)(ptx::smem_ld_acquire(a) - need) >= 0) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if ((int32_t)(ptx::smem_ld_acquire(a) - need) >= 0) return true;
-    if ((it & 63u) == 0) {
-      if (*c.abort) return false;
-      if (ptx::globaltimer() - t0 > kTimeoutNs) {
-        *c.abort = 1;
-        record_error(c.status, FP4IDX_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Ctl& c) {
-  return __all_sync(kFull, poll(bar, parity, c, true));
-}
-
-__device__ __forceinline__ bool wait_lane0(uint32_t bar, uint32_t parity, const Ctl& c, bool honor_abort = true) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = poll(bar, parity, c, honor_abort) ? 1 : 0;
-  return __shfl_sync(kFull, ok, 0) != 0;
+  return pipe::wait_counts(a, need, a, need, c);
 }
 
 // TMA tiled load of one box of a 3-D tensor map; x is the innermost coordinate (bytes
@@ -179,8 +139,6 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
-__device__ __forceinline__ void prefetch_l2(const void* a) { asm volatile("prefetch.global.L2 [%0];" ::"l"(a)); }
 
 // Lane l's share of the 32 page ids starting at logical page 2 * tile0 of the item's
 // sequence: the physical page, or -2 past the item's longest context or for a sequence
@@ -235,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fp8_kernel(const __grid_co
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Ctl ctl{abort_flag, p.status};
+  const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
 
   if (warp < kProducers) {
     // ------------------------------------------------------------ producers
@@ -243,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fp8_kernel(const __grid_co
     uint32_t kctr = 0, ictr = 0;
     bool ok = true;
     Item it;
-    bool have = items.next(it);
+    bool have = !p.idle_producers && items.next(it);
     int32_t pid_cur = -2, pid_next = -2;
     if (have) {
       pid_cur = page_ids(p, it, it.t0, lane);
@@ -469,23 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fp8_kernel(const __grid_co
   if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 // The fused pages as a 3-D uint8 tensor {128 B, 66 rows, num_pages}; box = 16 B of 64 rows
 // of one page.
 bool encode_pages(CUtensorMap* map, const uint8_t* pages, int64_t num_pages) {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* q = nullptr;
-    cudaDriverEntryPointQueryResult r;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) !=
-            cudaSuccess ||
-        r != cudaDriverEntryPointSuccess)
-      return false;
-    fn = reinterpret_cast<EncodeTiledFn>(q);
-  }
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
   cuuint64_t dims[3] = {128, kPageBytes / 128, (cuuint64_t)num_pages};
   cuuint64_t strides[2] = {128, kPageBytes};
   cuuint32_t box[3] = {16, 64, 1};
@@ -502,13 +448,8 @@ cudaError_t launch_logits_fp8(const uint8_t* q8, const float* q8_scale, const fl
                               int32_t max_pages, const int32_t* context_lens, int32_t max_context,
                               const void* schedule, int32_t num_ctas, float* out, int64_t out_stride,
                               int32_t* status, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(logits_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(logits_fp8_kernel), kSmemBytes);
+  if (e != cudaSuccess) return e;
   if (num_pages < 1 || num_pages > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
   CUtensorMap k_map;
   if (!encode_pages(&k_map, pages, num_pages)) return cudaErrorInvalidValue;
@@ -528,6 +469,8 @@ cudaError_t launch_logits_fp8(const uint8_t* q8, const float* q8_scale, const fl
   prm.out = out;
   prm.out_stride = out_stride;
   prm.status = status;
+  prm.wait_limit_ns = pipeline_wait_limit_ns();
+  prm.idle_producers = pipeline_idle_producers() ? 1 : 0;
   logits_fp8_kernel<<<num_ctas, kThreads, kSmemBytes, stream>>>(k_map, prm);
   return cudaGetLastError();
 }

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kThreads) build_schedule_kernel(const int32_t*
     if (n_groups <= kThreads) row0_s[n_groups] = n_rows;
   }
   len_s[tid] = len0;
+  for (int32_t t = tid; t < n_rows; t += kThreads) s.sel_cnt[t] = 0u;
   __syncthreads();
 
   // Phase B: per-group longest (clamped) context and cost prefix.

@@ -52,6 +52,9 @@ struct SchedView {
   int32_t* seq;      // [n_rows] the group's sequence (row_seq of its rows), so that a work
                      // item's first page-table read need not wait on a row_seq load
   int64_t* prefix;   // [n_rows + 1] exclusive prefix of group costs
+  uint32_t* sel_cnt; // [n_rows] per row, in a fused logits + selection call: the (tile,
+                     // TMEM lane quarter) pieces of the row's logits written so far; zeroed
+                     // by the build, put back to zero by the CTA that selects the row
   CtaStart* cta;     // [num_ctas] each logits CTA's cost range and first item
 };
 
@@ -63,6 +66,7 @@ __host__ __device__ inline size_t sched_bytes(int64_t n_rows, int64_t num_ctas) 
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   b += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
+  b += sched_align16(sizeof(uint32_t) * (size_t)(n_rows + 1));
   b += sizeof(CtaStart) * (size_t)num_ctas;
   return b;
 }
@@ -80,6 +84,8 @@ __host__ __device__ inline SchedView sched_view(void* base, int64_t n_rows) {
   p += sched_align16(sizeof(int32_t) * (size_t)(n_rows + 1));
   v.prefix = reinterpret_cast<int64_t*>(p);
   p += sched_align16(sizeof(int64_t) * (size_t)(n_rows + 1));
+  v.sel_cnt = reinterpret_cast<uint32_t*>(p);
+  p += sched_align16(sizeof(uint32_t) * (size_t)(n_rows + 1));
   v.cta = reinterpret_cast<CtaStart*>(p);
   return v;
 }

@@ -79,6 +79,7 @@ _SIGS = {
     "fp4idx_topk_merge_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "fp4idx_topk_values": (ctypes.c_int, [_vp, _i64, _vp, _i64, _i32, _vp, _vp]),
     "fp4idx_topk_merge": (ctypes.c_int, [_vp, _vp, _i64, _i32, _i32, _vp, _sz, _vp, _vp, _vp]),
+    "fp4idx_test_pipeline_waits": (ctypes.c_int, [_i32, _i64]),
     "fp4idx_read_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
 }
 
@@ -373,6 +374,15 @@ def topk_merge(cand_values, cand_idx, workspace, topk_idx, status=None, stream=N
                                 _ptr(topk_idx, "topk_idx", _I32, T * k), _ptr(status, "status", _I32, 1, nullable=True),
                                 _stream_ptr(stream))
     _check("fp4idx_topk_merge", rc)
+
+
+def test_pipeline_waits(idle_producers: bool, wait_limit_ns: int = 0) -> None:
+    """Test switch of the logits kernels' bounded waits: with idle_producers the producer
+    warps of later logits launches issue nothing, so every wait runs out after
+    wait_limit_ns and the launch records FP4IDX_ERR_TIMEOUT.  (False, 0) restores normal
+    operation and the default limit."""
+    _check("fp4idx_test_pipeline_waits", _lib.fp4idx_test_pipeline_waits(1 if idle_producers else 0,
+                                                                          int(wait_limit_ns)))
 
 
 def read_status(status, stream=None) -> int:

@@ -24,6 +24,7 @@ def lib():
         "fp4idx_quant_q_w": [V, I64, I32, V, V, I32, V, I32, V, F32, V, V, V, V, V],
         "fp4idx_build_schedule": [V, V, I64, I32, V, SZ, V],
         "fp4idx_topk": [V, I64, V, I64, I32, I32, V, SZ, V, V, V],
+        "fp4idx_topk_noalloc": [V, I64, V, I64, I32, I32, V, V, V],
         "fp4idx_topk_values": [V, I64, V, I64, I32, V, V],
         "fp4idx_topk_merge": [V, V, I64, I32, I32, V, SZ, V, V, V],
         "fp4idx_dequant_pages": [V, V, I64, V, I64, V, V, V],
@@ -92,6 +93,28 @@ def test_topk(lib):
     assert f(M1, 100, A, 2, 100, 16, A, 1 << 20, A, None, None) == INVALID
     assert f(A, 100, A, 2, 100, 16, A, 0, A, None, None) == WORKSPACE
     assert lib.fp4idx_topk_workspace_bytes(-1, 100) == 0
+
+
+def test_topk_noalloc(lib):
+    """Argument errors are reported before the fixed scratch's set-up (a CUDA call) runs."""
+    SCRATCH_LIMIT = 10
+    f = lib.fp4idx_topk_noalloc
+    assert f(A, 100, A, 2, 100, 0, A, None, None) == INVALID             # k = 0
+    assert f(A, 100, A, 2, 100, 4097, A, None, None) == INVALID          # k above the maximum
+    assert f(A, 100, A, -1, 100, 16, A, None, None) == INVALID           # negative rows
+    assert f(A, 70000, A, 2, 70000, 16, A, None, None) == UNSUPPORTED    # context above the maximum
+    assert f(None, 100, A, 2, 100, 16, A, None, None) == INVALID         # null logits
+    assert f(A, 100, None, 2, 100, 16, A, None, None) == INVALID         # null context_lens
+    assert f(A, 100, A, 2, 100, 16, None, None, None) == INVALID         # null output
+    assert f(M1, 100, A, 2, 100, 16, A, None, None) == INVALID           # logits misaligned
+    assert f(A, 100, M1, 2, 100, 16, A, None, None) == INVALID
+    assert f(A, 100, A, 2, 100, 16, M1, None, None) == INVALID
+    assert f(A, 100, A, 2, 100, 16, A, M1, None) == INVALID              # status misaligned
+    assert f(A, 50, A, 2, 100, 16, A, None, None) == INVALID             # stride below max_context
+    # 128 rows of 65,536 fit the 16 MiB exactly; one more row does not
+    assert lib.fp4idx_topk_workspace_bytes(128, 65536) <= 16 << 20
+    assert f(A, 65536, A, 129, 65536, 16, A, None, None) == SCRATCH_LIMIT
+    assert f(None, 65536, None, 129, 65536, 16, None, None, None) == SCRATCH_LIMIT
 
 
 def test_topk_values_and_merge(lib):

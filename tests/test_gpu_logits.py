@@ -38,7 +38,9 @@ def test_small_batches_against_oracle(cs, seed, lens, rps, k, zeros):
     assert got["status"] == 0
     ref = oracle.run_indexer(b, cs)
     assert np.array_equal(got["payload"].cpu().numpy(), ref["payload"])
+    assert np.array_equal(got["scale"].cpu().numpy(), ref["scale"])
     assert np.array_equal(got["q_payload"].cpu().numpy(), ref["q_payload"])
+    assert np.array_equal(got["q_scale"].cpu().numpy(), ref["q_scale"])
     for t in range(b.n_rows):
         L = int(b.context_lens[t])
         check_logits(got["logits"][t], ref["logits"][t], ref["bound"][t], L, "row %d" % t)
@@ -140,3 +142,113 @@ def test_workloads_against_oracle(cs, maker, nsample):
     self_rows = np.arange(b.n_rows) if b.n_rows <= 2048 else _sampled_rows(b, 512, rng, must)
     for t in self_rows:
         check_topk_self(got["topk"][t], got["logits"][t], int(b.context_lens[t]), b.topk, "%s row %d" % (b.name, t))
+
+
+def _read_side(b, cs, payload, scale, sched=None, separate=False, k=None):
+    """The read side alone on a stored cache: Q quant, schedule (unless given), then either
+    the fused call (fp4idx_logits_topk) or the two separate calls (fp4idx_logits, then
+    fp4idx_topk).  Returns (status, logits, topk)."""
+    from sparse_attention_fp4_gb300 import fp4idx
+    from tests.gpu_util import bf16, dev
+    k = b.topk if k is None else k
+    T = b.n_rows
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qp, qs = fp4idx.alloc_query(T)
+    fp4idx.quant_q(bf16(b.q), dev(b.q_positions), bf16(cs), qp, qs, status=status)
+    cl, rs, pt = dev(b.context_lens), dev(b.row_seq), dev(b.page_table)
+    Lmax = int(max(1, b.context_lens.max()))
+    if sched is None:
+        sched = torch.empty(fp4idx.schedule_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+        fp4idx.build_schedule(cl, rs, sched)
+    lg = torch.full((T, Lmax), float("nan"), dtype=torch.float32, device="cuda")
+    topk = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    if separate:
+        fp4idx.logits(qp, qs, dev(b.w), payload, scale, pt, rs, cl, Lmax, sched, lg, status=status)
+        ws = torch.empty(fp4idx.topk_workspace_bytes(T, Lmax), dtype=torch.uint8, device="cuda")
+        fp4idx.topk(lg, cl, Lmax, k, ws, topk, status=status)
+    else:
+        ws = torch.empty(fp4idx.logits_workspace_bytes(T, Lmax, k), dtype=torch.uint8, device="cuda")
+        fp4idx.logits_topk(qp, qs, dev(b.w), payload, scale, pt, rs, cl, Lmax, k, sched, ws, topk, logits_out=lg,
+                           status=status)
+    torch.cuda.synchronize()
+    return fp4idx.read_status(status), lg.cpu().numpy(), topk.cpu().numpy()
+
+
+def _stored(b, cs):
+    from sparse_attention_fp4_gb300 import fp4idx
+    from tests.gpu_util import bf16, dev
+    ks = b.kstore
+    payload, scale = fp4idx.alloc_cache(b.num_pages)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fp4idx.store_k(bf16(ks.k_rows), dev(ks.positions), dev(ks.slots), bf16(ks.norm_w), ks.eps, bf16(cs), payload,
+                   scale, status=status)
+    assert fp4idx.read_status(status) == 0
+    return payload, scale
+
+
+@pytest.mark.parametrize("seed,lens,rps,k,zeros", [SMALL[3], SMALL[4], SMALL[5], SMALL[9], SMALL[10]])
+def test_fused_selection_equals_separate_launches(cs, seed, lens, rps, k, zeros):
+    """The logits launch's own selection (few rows) and the separate top-k launch select
+    from bit-identical logits with the same rule, so they agree exactly."""
+    b = wl.small_batch(seed, lens, rows_per_seq=rps, topk=k, zero_rows=zeros)
+    payload, scale = _stored(b, cs)
+    st1, lg1, tk1 = _read_side(b, cs, payload, scale)
+    st2, lg2, tk2 = _read_side(b, cs, payload, scale, separate=True)
+    assert st1 == 0 and st2 == 0
+    for t in range(b.n_rows):
+        L = int(b.context_lens[t])
+        assert np.array_equal(lg1[t, :L], lg2[t, :L]), t
+    assert np.array_equal(tk1, tk2)
+
+
+def test_schedule_reused_across_calls(cs):
+    """A schedule built once serves several fused calls in a row (as every layer of a
+    forward would use it): each call counts its groups complete and leaves the counters at
+    zero for the next."""
+    from sparse_attention_fp4_gb300 import fp4idx
+    from tests.gpu_util import dev
+    b = wl.small_batch(44, [3000, 129, 5000, 64, 2100], rows_per_seq=3, topk=256, zero_rows=(4,))
+    payload, scale = _stored(b, cs)
+    sched = torch.empty(fp4idx.schedule_workspace_bytes(b.n_rows), dtype=torch.uint8, device="cuda")
+    fp4idx.build_schedule(dev(b.context_lens), dev(b.row_seq), sched)
+    runs = [_read_side(b, cs, payload, scale, sched=sched) for _ in range(3)]
+    ref = oracle.run_indexer(b, cs)
+    for st, lg, tk in runs:
+        assert st == 0
+        assert np.array_equal(tk, runs[0][2])
+        for t in range(b.n_rows):
+            L = int(b.context_lens[t])
+            check_topk(tk[t], ref["logits"][t], ref["bound"][t], L, b.topk, "row %d" % t)
+
+
+def test_fused_selection_of_rows_past_shared_memory(cs):
+    """Rows longer than the 32,768 sort keys a CTA keeps in shared memory spill the rest
+    to the workspace; the fused selection still equals the oracle's."""
+    b = wl.small_batch(45, [40000, 33000, 65536, 32769], rows_per_seq=1, topk=2048)
+    # the decode query position 4L - 1 would pass the RoPE table for these lengths
+    b.q_positions = np.minimum(b.q_positions, wl.ROPE_MAX_POS - 1).astype(np.int32)
+    got = run_gpu_indexer(b, cs)
+    assert got["status"] == 0
+    ref = oracle.run_indexer(b, cs)
+    for t in range(b.n_rows):
+        L = int(b.context_lens[t])
+        check_logits(got["logits"][t], ref["logits"][t], ref["bound"][t], L, "row %d" % t)
+        check_topk(got["topk"][t], ref["logits"][t], ref["bound"][t], L, b.topk, "row %d" % t)
+        check_topk_self(got["topk"][t], got["logits"][t], L, b.topk, "row %d" % t)
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_row_count_at_the_fused_limit(cs, extra):
+    """As many rows as SMs (the fused selection) and one more (the separate top-k launch)."""
+    from sparse_attention_fp4_gb300 import fp4idx
+    n = fp4idx.num_sms() + extra
+    rng = np.random.default_rng(46 + extra)
+    lens = [int(x) for x in rng.integers(0, 3000, size=n)]
+    b = wl.small_batch(46 + extra, lens, rows_per_seq=1, topk=300)
+    got = run_gpu_indexer(b, cs)
+    assert got["status"] == 0
+    ref = oracle.run_indexer(b, cs)
+    for t in range(b.n_rows):
+        L = int(b.context_lens[t])
+        check_topk(got["topk"][t], ref["logits"][t], ref["bound"][t], L, b.topk, "row %d" % t)
+        check_topk_self(got["topk"][t], got["logits"][t], L, b.topk, "row %d" % t)

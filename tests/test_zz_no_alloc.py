@@ -34,10 +34,8 @@ def _inputs(rows, lens, stride):
 
 
 def _expected(row, L, k):
-    order = np.lexsort((np.arange(L), -row[:L].astype(np.float64)))[:min(k, L)]
-    out = -np.ones(k, np.int32)
-    out[:order.size] = np.sort(order)
-    return out
+    import oracle
+    return oracle.topk(np.asarray(row[:L], np.float64), L, k)
 
 
 def _with_workspace(lg, cl, Lmax, k):
