@@ -221,7 +221,7 @@ def gpu_id_for(device_index):
 class DecodeStep:
     """Device-resident inputs of one decode batch and the five launches of a step."""
 
-    def __init__(self, b, device):
+    def __init__(self, b, device, fused=False):
         import torch
 
         from sparse_attention_fp4_gb300 import fp4idx
@@ -272,23 +272,20 @@ class DecodeStep:
                                    device=device)
         self.fused_ws = torch.empty(fp4idx.logits_workspace_bytes(self.T, self.max_ctx, self.k), dtype=torch.uint8,
                                     device=device)
-        self.fused = self.T <= fp4idx.num_sms()  # fp4idx_logits_topk selects inside the logits launch
+        self.fused = fused  # False: fp4idx_logits_topk (two launches); True: fp4idx_logits_topk_fused
         torch.cuda.synchronize(device)
 
     def calls(self):
-        """The launches of a step, in order, as (name, callable).  With at most one row per
-        SM the read side is the fused call (one launch: logits and the selection); larger
-        batches issue the logits and the top-k launch as the fused entry point does for
-        them."""
+        """The launches of a step, in order, as (name, callable): the step preparation
+        (fp4idx_prepare_step: schedule, K store of the newest rows, Q quant, one launch),
+        then the read side -- the logits launch and the top-k launch of
+        fp4idx_logits_topk, or with `fused` the one launch of fp4idx_logits_topk_fused."""
         f = self.fp4idx
-        base = [
-            ("store_k", lambda: f.store_k(self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.cs,
-                                          self.payload, self.scale, status=self.status)),
-            ("quant_q", lambda: f.quant_q(self.q, self.qpos, self.cs, self.qp, self.qs, status=self.status)),
-            ("build_schedule", lambda: f.build_schedule(self.cl, self.rs, self.sched)),
-        ]
+        base = [("prepare_step", lambda: f.prepare_step(
+            self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.q, self.qpos, self.cs, self.payload,
+            self.scale, self.qp, self.qs, self.cl, self.rs, self.sched, status=self.status))]
         if self.fused:
-            return base + [("logits_topk", self.logits_topk)]
+            return base + [("logits_topk_fused", self.logits_topk)]
         return base + [
             ("logits", lambda: f.logits(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
                                         self.max_ctx, self.sched, self.logits, status=self.status)),
@@ -297,48 +294,35 @@ class DecodeStep:
         ]
 
     def logits_topk(self):
-        """The read side's entry point as a caller uses it: paged-MQA logits and the top-k
-        selection in one call (fp4idx_logits_topk)."""
+        """The read side's entry point as a caller uses it: fp4idx_logits_topk (or, with
+        `fused`, fp4idx_logits_topk_fused)."""
         self.fp4idx.logits_topk(self.qp, self.qs, self.w, self.payload, self.scale, self.pt, self.rs, self.cl,
-                                self.max_ctx, self.k, self.sched, self.fused_ws, self.topk, status=self.status)
+                                self.max_ctx, self.k, self.sched, self.fused_ws, self.topk, status=self.status,
+                                fused=self.fused)
 
     def launch(self):
         for _, fn in self.calls():
             fn()
 
-    def launch_forked(self, side_streams, marks=None):
-        """The step with its independent launches overlapped: K store, Q quant and the
-        schedule depend on nothing but their inputs, so they run on three streams, and the
-        read side waits for all three (the form captured into the step's graph).  With
-        `marks` (timing events, one more than the read side's launches) the read side's
-        launches are issued one by one with a mark before each and after the last."""
+    def launch_step(self, marks=None):
+        """The step as a caller issues it on one stream: fp4idx_prepare_step, then the read
+        side's call (the form captured into the step's graph).  With `marks` (timing
+        events, one more than the read side's launches) the read side's launches are
+        issued one by one with a mark before each and after the last."""
         import torch
         calls = self.calls()
-        cur = torch.cuda.current_stream()
-        start = torch.cuda.Event()
-        start.record(cur)
-        done = []
-        branch = dict(calls[:3])
-        # the longest branch first: a graph starts its root branches one after another
-        for name, st in zip(("build_schedule", "store_k", "quant_q"), side_streams):
-            st.wait_event(start)
-            with torch.cuda.stream(st):
-                branch[name]()
-                ev = torch.cuda.Event()
-                ev.record(st)
-            done.append(ev)
-        for ev in done:
-            cur.wait_event(ev)
+        calls[0][1]()
         if marks:
-            for i, (_, fn) in enumerate(calls[3:]):
+            cur = torch.cuda.current_stream()
+            for i, (_, fn) in enumerate(calls[1:]):
                 marks[i].record(cur)
                 fn()
-            marks[len(calls) - 3].record(cur)
+            marks[len(calls) - 1].record(cur)
         else:
             self.logits_topk()
 
     def read_side_names(self):
-        return [n for n, _ in self.calls()[3:]]
+        return [n for n, _ in self.calls()[1:]]
 
 
 def run_gpu(args):
@@ -349,7 +333,7 @@ def run_gpu(args):
     device = torch.device("cuda", local)
     dist_init("nccl")
     b = make_batch(args.workload)
-    st = DecodeStep(b, device)
+    st = DecodeStep(b, device, fused=args.fused)
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -371,9 +355,8 @@ def run_gpu(args):
         st.launch()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    side = [torch.cuda.Stream(device) for _ in range(3)]
     with torch.cuda.graph(g):
-        st.launch_forked(side)
+        st.launch_step()
     # an instrumented copy of the step: event-record nodes around each launch of the read
     # side (the marks slow a step a little, so the timed loop replays the plain graph)
     names = st.read_side_names()
@@ -381,7 +364,7 @@ def run_gpu(args):
         marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
         gm = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gm):
-            st.launch_forked(side, marks)
+            st.launch_step(marks)
     except TypeError:
         marks, gm = None, None
     for _ in range(max(3, args.warmup)):
@@ -446,7 +429,7 @@ def run_gpu(args):
             per_times[name].append((e0, e1))
     torch.cuda.synchronize()
     per = {n: statistics.median([a.elapsed_time(b) for a, b in v]) * 1e3 for n, v in per_times.items()}
-    main = names[0]  # the logits launch (with the fused selection when the batch takes it)
+    main = names[0]  # the logits launch (with the selection, for fp4idx_logits_topk_fused)
     if marks:
         logits_us = statistics.mean(live[main])
         live_us = {n: {"mean": round(statistics.mean(v), 2), "median": round(statistics.median(v), 2)}
@@ -499,8 +482,10 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1,ue8m0)->f32", "data": "synthetic",
             "config": {"workload": b.name, "rows": b.n_rows, "heads": 64, "head_dim": 128, "topk": b.topk,
                        "context_tokens": int(b.context_lens.sum()), "cache_pages": b.num_pages,
-                       "step": "K store (newest token per sequence) + Q quant + schedule + fused logits/top-k "
-                               "call, one CUDA graph replay (store, quant and schedule on parallel branches)",
+                       "step": "fp4idx_prepare_step (schedule + K store of the newest token per sequence + Q "
+                               "quant, one launch) + %s, one CUDA graph replay" % (
+                                   "fp4idx_logits_topk_fused (logits and selection in one launch)" if st.fused else
+                                   "fp4idx_logits_topk (logits launch, top-k launch)"),
                        "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "kcache_gbs": round(ab["k_cache"] / (logits_us * 1e-6) / 1e9, 1),
@@ -519,9 +504,8 @@ def run_gpu(args):
 
 def run_e2e(st, args, flush_l2):
     """Same metric through the C ABI with host buffers: every step copies its inputs from
-    pinned host memory, makes the four calls a caller makes (K store, Q quant and the
-    schedule on three streams, then the fused logits + top-k) and reads the selection
-    back."""
+    pinned host memory, makes the two calls a caller makes (fp4idx_prepare_step, then the
+    logits + top-k call) and reads the selection back."""
     import torch
     b = st.b
     # the step's inputs, each as a 256-byte aligned slice of one pinned staging buffer and
@@ -546,11 +530,10 @@ def run_e2e(st, args, flush_l2):
     h2d = total
     d2h = out.numel() * out.element_size()
     K = min(args.steps, 200)
-    side = [torch.cuda.Stream(st.device) for _ in range(3)]
 
     def step():
         dev_in.copy_(host, non_blocking=True)
-        st.launch_forked(side)
+        st.launch_step()
         out.copy_(st.topk, non_blocking=True)
 
     # the step as a serving loop replays it: one CUDA graph holding the copies in from
@@ -581,8 +564,8 @@ def run_e2e(st, args, flush_l2):
     return {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": K, "ms_per_step": round(sum(times) / K * 1e3, 4),
             "how": "one CUDA graph replay per step: one host-to-device copy of the step's inputs (packed in one "
-                   "pinned buffer), the store/quant/schedule calls on three branches and the fused logits/top-k "
-                   "call, device-to-host copy of the selection",
+                   "pinned buffer), the step-preparation call and the logits/top-k call, device-to-host copy of "
+                   "the selection",
             "selection_read_back_matches": bool(ok)}
 
 
@@ -1004,6 +987,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="read side through fp4idx_logits_topk_fused (one launch) instead of fp4idx_logits_topk")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -175,13 +175,32 @@ int fp4idx_quant_q_w(const uint16_t* q, int64_t n_rows, int32_t n_heads, const i
  *                                of one sequence that are adjacent share K tiles
  *   num_ctas                     grid the logits kernel will use (0 = SM count)
  *   schedule     device buffer of at least fp4idx_schedule_workspace_bytes(n_rows, num_ctas)
- * Besides the work split, the schedule holds one counter per group of rows that
- * fp4idx_logits_topk's fused selection counts up and puts back to zero; the build
+ * Besides the work split, the schedule holds one counter per row that the fused
+ * selection of fp4idx_logits_topk_fused counts up and puts back to zero; the build
  * zeroes them.
  */
 size_t fp4idx_schedule_workspace_bytes(int64_t max_rows, int32_t num_ctas);
 int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int64_t n_rows,
                           int32_t num_ctas, void* schedule, size_t schedule_bytes, void* stream);
+
+/*
+ * The decode step's preparation in one launch: the work of fp4idx_build_schedule,
+ * fp4idx_store_k and fp4idx_quant_q, with the same arguments and the same results
+ * (bit for bit), in one grid -- [P2] Attention runtime (the schedule is built in the
+ * captured step) and Modifications (the fused K writer and the Q packer).  One block builds
+ * the schedule, the others store the n_new K rows and pack the n_rows query rows; they
+ * run side by side, and the whole grid allows the logits launch that follows on the
+ * stream (fp4idx_logits_topk, fp4idx_logits) to start its own set-up before the grid ends.
+ * Arguments as in the three calls; q_positions, context_lens and row_seq describe the
+ * n_rows query rows, k, positions and slots the n_new K rows (n_new may be 0).
+ * Device errors: those of the three calls.
+ */
+int fp4idx_prepare_step(const uint16_t* k, int64_t n_new, const int32_t* positions, const int32_t* slots,
+                        const uint16_t* norm_w, float eps, const uint16_t* q, int64_t n_rows, int32_t n_heads,
+                        const int32_t* q_positions, const uint16_t* cos_sin, int32_t max_pos, uint8_t* payload,
+                        uint8_t* scale, int64_t num_pages, uint8_t* q_payload, uint8_t* q_scale,
+                        const int32_t* context_lens, const int32_t* row_seq, int32_t num_ctas, void* schedule,
+                        size_t schedule_bytes, int32_t* status_dev, void* stream);
 
 /*
  * Paged-MQA logits + top-k -- [P2] Modifications: "Dispatch decode and prefill
@@ -195,16 +214,7 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
  *   row_seq, context_lens  as given to fp4idx_build_schedule (same arrays)
  *   max_context         host-known upper bound of context_lens (<= FP4IDX_MAX_CONTEXT)
  *   k                   1..FP4IDX_MAX_TOPK
- *   schedule            built by fp4idx_build_schedule for these rows.  When n_rows is
- *                       at most the device's SM count the logits launch also selects:
- *                       the CTA that writes the last tile of a row's group counts it
- *                       complete on the group's counter in the schedule and selects the
- *                       group's rows from the logits the launch wrote, so there is no
- *                       second launch.  The call leaves the counters at zero; calls that
- *                       share one schedule must therefore be ordered (one stream), and
- *                       after a call that reported an error, rebuild the schedule.
- *                       Larger batches run the logits launch, then the top-k launch of
- *                       fp4idx_topk (one CTA per row).  Both give the same selection.
+ *   schedule            built by fp4idx_build_schedule for these rows (read only here)
  *   workspace           >= fp4idx_logits_workspace_bytes(n_rows, max_context, k) bytes:
  *                       a logits buffer (unused when logits_out is given) and the
  *                       selection's scratch; nothing in it needs to be initialised
@@ -212,16 +222,40 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
  *             row in ascending order; all of them when context_len <= k; -1 pads.
  *   logits_out [n_rows, logits_stride] fp32 (nullable): when given, receives
  *             logits[t,s] for s < context_lens[t] (the rest is not written).
+ * Two launches: the logits kernel, then the top-k kernel (one CTA, or a pair of CTAs
+ * in a cluster, per row).
  * Device errors: BAD_PAGE (page id out of range: the tile is skipped),
- * BAD_LENGTH, TIMEOUT (the rows of the CTA that gave up are not selected), SCHEDULE.
+ * BAD_LENGTH, TIMEOUT, SCHEDULE.
  */
 size_t fp4idx_logits_workspace_bytes(int64_t max_rows, int32_t max_context, int32_t k);
 int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
                        int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
                        const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
-                       const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
+                       const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
                        size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
                        float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream);
+
+/*
+ * fp4idx_logits_topk in one launch ([P3] Changes: "sorted top-k selection"; the
+ * selection is folded into the logits kernel).  Same arguments, result and errors, with
+ * one difference: `schedule` is written.  When n_rows is at most the device's SM count,
+ * the epilogue warps count, per row, the pieces of its logits they have written (a
+ * release add on a counter in the schedule); after its own work the CTA of each row --
+ * or a pair of CTAs in a cluster, when the grid holds two for every row -- waits for all
+ * of the row's pieces (bounded) and selects the row from the logits in L2.  The launch
+ * is cooperative (every CTA resident at once).  The counters go back to zero, so calls
+ * that share a schedule must be ordered (one stream), and after a call that reported an
+ * error the schedule must be built again.  Larger batches run the two launches of
+ * fp4idx_logits_topk.  Both give the same selection.  Inside a CUDA graph, where the
+ * second launch of fp4idx_logits_topk costs little, that call is the faster of the two on
+ * GB300; this one saves the launch where launches are not overlapped.
+ */
+int fp4idx_logits_topk_fused(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                             int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                             const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                             const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
+                             size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                             float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream);
 
 /*
  * The two halves of fp4idx_logits_topk, for callers that want the logits themselves or

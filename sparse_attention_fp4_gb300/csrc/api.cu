@@ -147,6 +147,37 @@ int fp4idx_build_schedule(const int32_t* context_lens, const int32_t* row_seq, i
                                                  as_stream(stream)));
 }
 
+int fp4idx_prepare_step(const uint16_t* k, int64_t n_new, const int32_t* positions, const int32_t* slots,
+                        const uint16_t* norm_w, float eps, const uint16_t* q, int64_t n_rows, int32_t n_heads,
+                        const int32_t* q_positions, const uint16_t* cos_sin, int32_t max_pos, uint8_t* payload,
+                        uint8_t* scale, int64_t num_pages, uint8_t* q_payload, uint8_t* q_scale,
+                        const int32_t* context_lens, const int32_t* row_seq, int32_t num_ctas, void* schedule,
+                        size_t schedule_bytes, int32_t* status_dev, void* stream) {
+  // the checks of fp4idx_store_k, fp4idx_quant_q and fp4idx_build_schedule
+  int st = check_store_args(k, n_new, positions, slots, norm_w, cos_sin, max_pos, num_pages);
+  if (st != FP4IDX_OK) return st;
+  if (n_new > 0 && (!payload || !scale || !aligned16(payload))) return FP4IDX_ERR_INVALID_ARG;
+  if (n_rows < 0 || n_rows > INT32_MAX - 1 || num_ctas < 0) return FP4IDX_ERR_INVALID_ARG;
+  if (n_heads != fp4idx::kHeads) return FP4IDX_ERR_UNSUPPORTED;
+  if (n_rows > 0) {
+    if (!q || !q_positions || !cos_sin || !q_payload || !q_scale || !context_lens || !row_seq) return FP4IDX_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(cos_sin) || !aligned16(q_payload) || !aligned4(q_positions) ||
+        !aligned4(context_lens) || !aligned4(row_seq))
+      return FP4IDX_ERR_INVALID_ARG;
+  }
+  if (!schedule || !aligned16(schedule)) return FP4IDX_ERR_INVALID_ARG;
+  if (status_dev && !aligned4(status_dev)) return FP4IDX_ERR_INVALID_ARG;
+  if (num_ctas == 0) {
+    st = device_sms(&num_ctas);
+    if (st != FP4IDX_OK) return st;
+  }
+  if (schedule_bytes < fp4idx::sched_bytes(n_rows, num_ctas)) return FP4IDX_ERR_WORKSPACE;
+  return from_cuda(fp4idx::launch_prepare_step(k, n_new, positions, slots, norm_w, eps, q, n_rows, q_positions,
+                                               cos_sin, max_pos, payload, scale, num_pages, q_payload, q_scale,
+                                               context_lens, row_seq, num_ctas, schedule, status_dev,
+                                               as_stream(stream)));
+}
+
 // Layout of the logits + top-k workspace: [logits buffer][top-k scratch].
 inline size_t logits_region_bytes(int64_t rows, int32_t max_context) {
   return ((size_t)rows * (size_t)logits_row_stride(max_context) * sizeof(float) + 255) & ~(size_t)255;
@@ -261,12 +292,16 @@ int fp4idx_topk(const float* logits, int64_t logits_stride, const int32_t* conte
                                        workspace, topk_idx, status_dev, as_stream(stream)));
 }
 
-int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
-                       int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
-                       const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
-                       const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
-                       size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
-                       float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream) {
+namespace {
+
+// fp4idx_logits_topk and fp4idx_logits_topk_fused: the same checks and buffers; `fused`
+// asks for the selection inside the logits launch where the grid has a CTA for every row.
+int logits_topk_impl(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                     int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                     const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                     const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
+                     size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                     float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream, bool fused) {
   int st = check_logits_args(q_payload, q_scale, w, n_rows, n_heads, payload, scale, num_pages, page_table, num_seqs,
                              max_pages, row_seq, context_lens, max_context, schedule, schedule_bytes, status_dev);
   if (st != FP4IDX_OK) return st;
@@ -290,21 +325,44 @@ int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const f
   int32_t sms = 0;
   st = device_sms(&sms);
   if (st != FP4IDX_OK) return st;
-  if (n_rows <= sms) {
-    // Few rows (decode): the logits launch selects too.  The CTA that completes a row
-    // selects it from the logits the launch wrote, with no second launch.
+  if (fused && n_rows <= sms) {
+    // the CTA (pair) of each row selects it from the logits the launch wrote
     return launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs,
                                  max_pages, row_seq, context_lens, max_context, schedule, buf, stride, k, topk_idx,
                                  topk_ws, status_dev, s);
   }
-  // Many rows (draft batches, prefill chunks): one CTA of the top-k launch per row
-  // selects with the whole GPU's parallelism.
+  // the logits launch, then the top-k launch (one CTA, or a pair of CTAs, per row)
   st = launch_logits_checked(q_payload, q_scale, w, n_rows, payload, scale, num_pages, page_table, num_seqs, max_pages,
                              row_seq, context_lens, max_context, schedule, buf, stride, 0, nullptr, nullptr,
                              status_dev, s);
   if (st != FP4IDX_OK) return st;
   return from_cuda(fp4idx::launch_topk(buf, stride, context_lens, (int32_t)n_rows, max_context, k, topk_ws,
                                        topk_idx, status_dev, s));
+}
+
+}  // namespace
+
+int fp4idx_logits_topk(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                       int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                       const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                       const int32_t* context_lens, int32_t max_context, int32_t k, const void* schedule,
+                       size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                       float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream) {
+  return logits_topk_impl(q_payload, q_scale, w, n_rows, n_heads, payload, scale, num_pages, page_table, num_seqs,
+                          max_pages, row_seq, context_lens, max_context, k, const_cast<void*>(schedule),
+                          schedule_bytes, workspace, workspace_bytes, topk_idx, logits_out, logits_stride, status_dev,
+                          stream, false);
+}
+
+int fp4idx_logits_topk_fused(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int64_t n_rows,
+                             int32_t n_heads, const uint8_t* payload, const uint8_t* scale, int64_t num_pages,
+                             const int32_t* page_table, int64_t num_seqs, int32_t max_pages, const int32_t* row_seq,
+                             const int32_t* context_lens, int32_t max_context, int32_t k, void* schedule,
+                             size_t schedule_bytes, void* workspace, size_t workspace_bytes, int32_t* topk_idx,
+                             float* logits_out, int64_t logits_stride, int32_t* status_dev, void* stream) {
+  return logits_topk_impl(q_payload, q_scale, w, n_rows, n_heads, payload, scale, num_pages, page_table, num_seqs,
+                          max_pages, row_seq, context_lens, max_context, k, schedule, schedule_bytes, workspace,
+                          workspace_bytes, topk_idx, logits_out, logits_stride, status_dev, stream, true);
 }
 
 int fp4idx_logits_topk_fp8(const uint8_t* q8, const float* q8_scale, const float* w, int64_t n_rows, int32_t n_heads,

@@ -44,6 +44,13 @@ cudaError_t launch_quant_q_w(const uint16_t* q, int64_t n_rows, const int32_t* q
                              int32_t dim, const uint16_t* w_proj, float w_scale, float* w_out, int32_t* status,
                              cudaStream_t stream);
 
+// The decode step's preparation (schedule, K store, Q quant) in one launch.
+cudaError_t launch_prepare_step(const uint16_t* k, int64_t n_new, const int32_t* positions, const int32_t* slots,
+                                const uint16_t* norm_w, float eps, const uint16_t* q, int64_t n_rows,
+                                const int32_t* q_positions, const uint16_t* cos_sin, int32_t max_pos,
+                                uint8_t* payload, uint8_t* scale, int64_t num_pages, uint8_t* q_payload,
+                                uint8_t* q_scale, const int32_t* context_lens, const int32_t* row_seq,
+                                int32_t num_ctas, void* schedule, int32_t* status, cudaStream_t stream);
 cudaError_t launch_build_schedule(const int32_t* context_lens, const int32_t* row_seq, int32_t n_rows,
                                   int32_t num_ctas, void* ws, cudaStream_t stream);
 cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale, const float* w, int32_t n_rows,

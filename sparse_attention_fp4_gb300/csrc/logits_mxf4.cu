@@ -282,32 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sb = ptx::smem_addr(smem);
 
-  // The schedule must describe exactly these rows and this grid.  The CTA's start record
-  // (inside the workspace the host checked against this grid) loads with the header.
-  const SchedView sv = sched_view(const_cast<void*>(p.schedule), p.n_rows);
-  const SchedHeader hdr = *sv.hdr;
-  const CtaStart cs = sv.cta[blockIdx.x];
-  if (hdr.magic != kSchedMagic || hdr.n_rows != p.n_rows || hdr.num_ctas != (int32_t)gridDim.x ||
-      hdr.group_max != kGroupMax) {
-    if (threadIdx.x == 0) record_error(p.status, FP4IDX_ERR_SCHEDULE);
-    return;
-  }
-  ItemIter items;
-  items.init(sv, cs);
-  // The producers request their first item's page ids before the prologue barrier, so the
-  // page-table read overlaps barrier set-up and the tensor-memory allocation.
-  const bool is_producer = warp >= kWarpProducer && warp < kWarpEpi0;
-  Item it;
-  bool have = false;
-  int32_t pid_cur = -2, pid_next = -2;
-  if (is_producer && !p.idle_producers) {
-    have = items.next(it);
-    if (have) {
-      pid_cur = page_ids(p, it, it.t0, lane);
-      pid_next = page_ids(p, it, it.t0 + 16, lane);
-    }
-  }
-
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + OFF_MISC + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   if (threadIdx.x == 0) {
@@ -336,7 +310,37 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.wait_limit_ns};
 
-  if (is_producer) {
+  // Everything above runs while a preceding kernel launched as this launch's programmatic
+  // primary (the step preparation: schedule, queries, new cache rows) may still be working;
+  // nothing below may read before its results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // The schedule must describe exactly these rows and this grid (the same header in every
+  // CTA, so every CTA takes the same branch).  The CTA's start record (inside the
+  // workspace the host checked against this grid) loads with the header.
+  const SchedView sv = sched_view(const_cast<void*>(p.schedule), p.n_rows);
+  const SchedHeader hdr = *sv.hdr;
+  const CtaStart cs = sv.cta[blockIdx.x];
+  const bool valid = hdr.magic == kSchedMagic && hdr.n_rows == p.n_rows && hdr.num_ctas == (int32_t)gridDim.x &&
+                     hdr.group_max == kGroupMax;
+  if (!valid && threadIdx.x == 0) record_error(p.status, FP4IDX_ERR_SCHEDULE);
+  ItemIter items;
+  items.init(sv, cs);
+  const bool is_producer = warp >= kWarpProducer && warp < kWarpEpi0;
+  Item it;
+  bool have = false;
+  int32_t pid_cur = -2, pid_next = -2;
+  if (valid && is_producer && !p.idle_producers) {
+    have = items.next(it);
+    if (have) {
+      pid_cur = page_ids(p, it, it.t0, lane);
+      pid_next = page_ids(p, it, it.t0 + 16, lane);
+    }
+  }
+
+  if (!valid) {
+    // no work: straight to the end
+  } else if (is_producer) {
     // ------------------------------------------------------------ producers
     const int pw = warp - kWarpProducer;  // issues the stages with kctr % kProducers == pw
     uint32_t kctr = 0, ictr = 0;
@@ -630,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (p.k > 0) {
+  if (p.k > 0 && valid) {
     __shared__ sel::Shared sel_sh;
     __shared__ int32_t sel_go;
     select_own_row<kSelC>(p, sv, reinterpret_cast<uint32_t*>(smem), sel_sh, &sel_go, *abort_flag != 0);
@@ -742,6 +746,13 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = prm.k > 0 ? sel_c : 0;
+  if (prm.k == 0) {
+    // a programmatic dependent launch: its set-up may overlap the end of the kernel before
+    // it on the stream (the kernel waits for that kernel's results before reading them)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
   if (sel_c == 2) return cudaLaunchKernelEx(&cfg, logits_mxf4_kernel<2>, pay_map, sc_map, prm);
   return cudaLaunchKernelEx(&cfg, logits_mxf4_kernel<1>, pay_map, sc_map, prm);
 }

@@ -21,6 +21,7 @@
 //     exponent/mantissa bits of amax; e2m1 by the hardware RNE-satfinite convert,
 //     the sign of zero taken from the input.
 #include "launchers.cuh"
+#include "schedule_build.cuh"
 
 #include <atomic>
 
@@ -151,13 +152,15 @@ __device__ __forceinline__ uint32_t fp4_encode_lane(const float v[8], uint32_t& 
 // ------------------------------------------------------------------ kernels
 constexpr int kRowsPerBlock = 16;  // 256 threads, a half-warp per row
 
-__global__ void __launch_bounds__(256) store_k_kernel(
-    const uint16_t* __restrict__ k, int64_t n_rows, const int32_t* __restrict__ positions,
-    const int32_t* __restrict__ slots, const uint16_t* __restrict__ norm_w, float eps,
-    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ payload,
-    uint8_t* __restrict__ scale, int64_t num_pages, int32_t* status) {
+// K store of the 16 rows of block `block` (a half-warp per row).
+__device__ __forceinline__ void store_k_block(int64_t block, const uint16_t* __restrict__ k, int64_t n_rows,
+                                              const int32_t* __restrict__ positions,
+                                              const int32_t* __restrict__ slots, const uint16_t* __restrict__ norm_w,
+                                              float eps, const uint16_t* __restrict__ cos_sin, int32_t max_pos,
+                                              uint8_t* __restrict__ payload, uint8_t* __restrict__ scale,
+                                              int64_t num_pages, int32_t* status) {
   const int lh = threadIdx.x & 15;
-  const int64_t n = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4);
+  const int64_t n = block * kRowsPerBlock + (threadIdx.x >> 4);
   const bool in_range = n < n_rows;
   int32_t slot = -1, pos = 0;
   if (in_range) {
@@ -194,6 +197,15 @@ __global__ void __launch_bounds__(256) store_k_kernel(
     *reinterpret_cast<uint32_t*>(dst) = word;
     if ((lh & 3) == 0) scale[(page * 4 + c) * kPage + j] = (uint8_t)sb;
   }
+}
+
+__global__ void __launch_bounds__(256) store_k_kernel(
+    const uint16_t* __restrict__ k, int64_t n_rows, const int32_t* __restrict__ positions,
+    const int32_t* __restrict__ slots, const uint16_t* __restrict__ norm_w, float eps,
+    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ payload,
+    uint8_t* __restrict__ scale, int64_t num_pages, int32_t* status) {
+  store_k_block(blockIdx.x, k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, payload, scale, num_pages,
+                status);
 }
 
 __global__ void __launch_bounds__(256) store_k_fp8_kernel(
@@ -290,6 +302,50 @@ __global__ void __launch_bounds__(256) quant_q_kernel(
     const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ q_payload,
     uint8_t* __restrict__ q_scale, int32_t* status) {
   quant_q_block(blockIdx.x, q, n_rows, q_positions, cos_sin, max_pos, q_payload, q_scale, status);
+}
+
+// The decode step's preparation in one launch: block 0 builds the logits schedule (the
+// build of schedule_build.cuh with 256 threads), the next kb blocks store the new K rows,
+// the rest pack the queries -- the launches of fp4idx_build_schedule, fp4idx_store_k and
+// fp4idx_quant_q, doing the same work, with the same results, in one grid.  Every block
+// signals at its start that a programmatic dependent launch (the logits kernel) may
+// begin its own set-up; that launch waits for this grid's results before reading them.
+struct PrepareParams {
+  const uint16_t* k;
+  int64_t n_new;
+  const int32_t* positions;
+  const int32_t* slots;
+  const uint16_t* norm_w;
+  float eps;
+  const uint16_t* q;
+  int64_t n_rows;
+  const int32_t* q_positions;
+  const uint16_t* cos_sin;
+  int32_t max_pos;
+  uint8_t* payload;
+  uint8_t* scale;
+  int64_t num_pages;
+  uint8_t* q_payload;
+  uint8_t* q_scale;
+  const int32_t* context_lens;
+  const int32_t* row_seq;
+  int32_t num_ctas;
+  void* schedule;
+  int32_t* status;
+  int64_t kb;  // blocks of the K store
+};
+
+__global__ void __launch_bounds__(256) prepare_step_kernel(const PrepareParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0) {
+    build_schedule_block<256>(p.context_lens, p.row_seq, (int32_t)p.n_rows, p.num_ctas, p.schedule);
+  } else if ((int64_t)blockIdx.x <= p.kb) {
+    store_k_block(blockIdx.x - 1, p.k, p.n_new, p.positions, p.slots, p.norm_w, p.eps, p.cos_sin, p.max_pos,
+                  p.payload, p.scale, p.num_pages, p.status);
+  } else {
+    quant_q_block(blockIdx.x - 1 - p.kb, p.q, p.n_rows, p.q_positions, p.cos_sin, p.max_pos, p.q_payload,
+                  p.q_scale, p.status);
+  }
 }
 
 // FP8 query pack (the comparison path of the 132 B/token layout): per (row t, head h), RoPE
@@ -461,6 +517,43 @@ cudaError_t launch_quant_q(const uint16_t* q, int64_t n_rows, const int32_t* q_p
   if (e != cudaSuccess) return e;
   quant_q_kernel<<<grid_for(n_rows * kHeads), 256, 0, stream>>>(q, n_rows, q_positions, cos_sin, max_pos,
                                                                  q_payload, q_scale, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_step(const uint16_t* k, int64_t n_new, const int32_t* positions, const int32_t* slots,
+                                const uint16_t* norm_w, float eps, const uint16_t* q, int64_t n_rows,
+                                const int32_t* q_positions, const uint16_t* cos_sin, int32_t max_pos,
+                                uint8_t* payload, uint8_t* scale, int64_t num_pages, uint8_t* q_payload,
+                                uint8_t* q_scale, const int32_t* context_lens, const int32_t* row_seq,
+                                int32_t num_ctas, void* schedule, int32_t* status, cudaStream_t stream) {
+  static std::atomic<bool> done[64];
+  cudaError_t e = prefer_max_shared(prepare_step_kernel, done);
+  if (e != cudaSuccess) return e;
+  PrepareParams p;
+  p.k = k;
+  p.n_new = n_new;
+  p.positions = positions;
+  p.slots = slots;
+  p.norm_w = norm_w;
+  p.eps = eps;
+  p.q = q;
+  p.n_rows = n_rows;
+  p.q_positions = q_positions;
+  p.cos_sin = cos_sin;
+  p.max_pos = max_pos;
+  p.payload = payload;
+  p.scale = scale;
+  p.num_pages = num_pages;
+  p.q_payload = q_payload;
+  p.q_scale = q_scale;
+  p.context_lens = context_lens;
+  p.row_seq = row_seq;
+  p.num_ctas = num_ctas;
+  p.schedule = schedule;
+  p.status = status;
+  p.kb = (n_new + kRowsPerBlock - 1) / kRowsPerBlock;
+  const int64_t qb = (n_rows * kHeads + kRowsPerBlock - 1) / kRowsPerBlock;
+  prepare_step_kernel<<<(unsigned)(1 + p.kb + qb), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -59,11 +59,15 @@ _SIGS = {
     "fp4idx_quant_q_fp8": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "fp4idx_quant_q_w": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i32, _vp, _i32, _vp, _f32, _vp, _vp, _vp, _vp,
                                         _vp]),
+    "fp4idx_prepare_step": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _f32, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp,
+                                           _i64, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp, _vp]),
     "fp4idx_schedule_workspace_bytes": (_sz, [_i64, _i32]),
     "fp4idx_build_schedule": (ctypes.c_int, [_vp, _vp, _i64, _i32, _vp, _sz, _vp]),
     "fp4idx_logits_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "fp4idx_logits_topk": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _i32, _vp, _vp,
                                           _i32, _i32, _vp, _sz, _vp, _sz, _vp, _vp, _i64, _vp, _vp]),
+    "fp4idx_logits_topk_fused": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _i32, _vp,
+                                                _vp, _i32, _i32, _vp, _sz, _vp, _sz, _vp, _vp, _i64, _vp, _vp]),
     "fp4idx_logits": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
                                      _vp, _sz, _vp, _i64, _vp, _vp]),
     "fp4idx_logits_fp8": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i32, _vp, _i64, _vp, _i64, _i32, _vp, _vp, _i32,
@@ -220,13 +224,39 @@ def build_schedule(context_lens, row_seq, schedule, num_ctas=0, stream=None):
     _check("fp4idx_build_schedule", rc)
 
 
+def prepare_step(k, positions, slots, norm_w, eps, q, q_positions, cos_sin, payload, scale, q_payload, q_scale,
+                 context_lens, row_seq, schedule, num_ctas=0, status=None, stream=None):
+    """fp4idx_prepare_step: the K store of the new rows, the Q quant and the schedule build
+    in one launch (the results of store_k, quant_q and build_schedule)."""
+    n_new = k.shape[0]
+    if k.dim() != 2 or k.shape[1] != HEAD_DIM:
+        raise ValueError("k must be [n_new, 128]")
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
+        raise ValueError("q must be [n_rows, heads, 128]")
+    T, H = q.shape[0], q.shape[1]
+    num_pages = payload.shape[0]
+    rc = _lib.fp4idx_prepare_step(
+        _ptr(k, "k", _BF16, nullable=n_new == 0), n_new, _ptr(positions, "positions", _I32, n_new, nullable=n_new == 0),
+        _ptr(slots, "slots", _I32, n_new, nullable=n_new == 0), _ptr(norm_w, "norm_w", _BF16, HEAD_DIM), float(eps),
+        _ptr(q, "q", _BF16), T, H, _ptr(q_positions, "q_positions", _I32, T), _ptr(cos_sin, "cos_sin", _BF16),
+        cos_sin.shape[0], _ptr(payload, "payload", _U8, num_pages * 4096), _ptr(scale, "scale", _U8, num_pages * 256),
+        num_pages, _ptr(q_payload, "q_payload", _U8, T * 4096), _ptr(q_scale, "q_scale", _U8, T * 256),
+        _ptr(context_lens, "context_lens", _I32, T), _ptr(row_seq, "row_seq", _I32, T), int(num_ctas),
+        _ptr(schedule, "schedule", _U8), schedule.numel(), _ptr(status, "status", _I32, 1, nullable=True),
+        _stream_ptr(stream))
+    _check("fp4idx_prepare_step", rc)
+
+
 def logits_topk(q_payload, q_scale, w, payload, scale, page_table, row_seq, context_lens, max_context, k,
-                schedule, workspace, topk_idx, logits_out=None, status=None, stream=None):
+                schedule, workspace, topk_idx, logits_out=None, status=None, stream=None, fused=False):
+    """fp4idx_logits_topk (the logits launch, then the top-k launch), or with fused=True
+    fp4idx_logits_topk_fused (the selection inside the logits launch; writes `schedule`)."""
     T = q_payload.shape[0]
     num_pages = payload.shape[0]
     S, max_pages = page_table.shape
     stride = logits_out.shape[1] if logits_out is not None else 0
-    rc = _lib.fp4idx_logits_topk(
+    fn = _lib.fp4idx_logits_topk_fused if fused else _lib.fp4idx_logits_topk
+    rc = fn(
         _ptr(q_payload, "q_payload", _U8, T * 4096), _ptr(q_scale, "q_scale", _U8, T * 256),
         _ptr(w, "w", _F32, T * NUM_HEADS), T, NUM_HEADS, _ptr(payload, "payload", _U8, num_pages * 4096),
         _ptr(scale, "scale", _U8, num_pages * 256), num_pages, _ptr(page_table, "page_table", _I32), S, max_pages,
@@ -235,7 +265,7 @@ def logits_topk(q_payload, q_scale, w, payload, scale, page_table, row_seq, cont
         _ptr(workspace, "workspace", _U8), workspace.numel(),
         _ptr(topk_idx, "topk_idx", _I32, T * int(k)), _ptr(logits_out, "logits_out", _F32, nullable=True),
         stride, _ptr(status, "status", _I32, 1, nullable=True), _stream_ptr(stream))
-    _check("fp4idx_logits_topk", rc)
+    _check("fp4idx_logits_topk_fused" if fused else "fp4idx_logits_topk", rc)
 
 
 def logits(q_payload, q_scale, w, payload, scale, page_table, row_seq, context_lens, max_context, schedule,

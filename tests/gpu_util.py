@@ -23,8 +23,10 @@ def kstore_to_device(ks):
     return dict(k=bf16(ks.k_rows), positions=dev(ks.positions), slots=dev(ks.slots), norm_w=bf16(ks.norm_w))
 
 
-def run_gpu_indexer(b, cos_sin_np, with_logits=True, page_table=None, payload=None, scale=None, k=None):
-    """Whole path on the GPU through the binding: K store, Q quant, schedule, logits + top-k."""
+def run_gpu_indexer(b, cos_sin_np, with_logits=True, page_table=None, payload=None, scale=None, k=None,
+                    fused=False):
+    """Whole path on the GPU through the binding: K store, Q quant, schedule, logits + top-k
+    (fp4idx_logits_topk, or fp4idx_logits_topk_fused with fused=True)."""
     from sparse_attention_fp4_gb300 import fp4idx
     cs = bf16(cos_sin_np)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -49,7 +51,7 @@ def run_gpu_indexer(b, cos_sin_np, with_logits=True, page_table=None, payload=No
     else:
         lg = None
     fp4idx.logits_topk(qp, qs, dev(b.w), payload, scale, pt, rs, cl, Lmax, k, sched, ws, topk, logits_out=lg,
-                       status=status)
+                       status=status, fused=fused)
     torch.cuda.synchronize()
     return dict(status=fp4idx.read_status(status), payload=payload, scale=scale, q_payload=qp, q_scale=qs,
                 logits=None if lg is None else lg.cpu().numpy(), topk=topk.cpu().numpy())

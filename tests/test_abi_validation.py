@@ -23,6 +23,7 @@ def lib():
         "fp4idx_quant_q": [V, I64, I32, V, V, I32, V, V, V, V],
         "fp4idx_quant_q_w": [V, I64, I32, V, V, I32, V, I32, V, F32, V, V, V, V, V],
         "fp4idx_build_schedule": [V, V, I64, I32, V, SZ, V],
+        "fp4idx_prepare_step": [V, I64, V, V, V, F32, V, I64, I32, V, V, I32, V, V, I64, V, V, V, V, I32, V, SZ, V, V],
         "fp4idx_topk": [V, I64, V, I64, I32, I32, V, SZ, V, V, V],
         "fp4idx_topk_noalloc": [V, I64, V, I64, I32, I32, V, V, V],
         "fp4idx_topk_values": [V, I64, V, I64, I32, V, V],
@@ -82,6 +83,31 @@ def test_schedule(lib):
     need = lib.fp4idx_schedule_workspace_bytes(4, 152)
     assert need > 0 and f(A, A, 4, 152, A, need - 1, None) == WORKSPACE
     assert lib.fp4idx_schedule_workspace_bytes(-1, 152) == 0
+
+
+def test_prepare_step(lib):
+    f = lib.fp4idx_prepare_step
+    def args(**kw):
+        a = dict(k=A, n_new=4, pos=A, slots=A, norm_w=A, eps=1e-6, q=A, n_rows=2, heads=64, qpos=A, cs=A, max_pos=16,
+                 payload=A, scale=A, num_pages=8, qp=A, qs=A, cl=A, rs=A, num_ctas=152, sched=A, sched_bytes=1 << 20,
+                 status=None)
+        a.update(kw)
+        return (a["k"], a["n_new"], a["pos"], a["slots"], a["norm_w"], a["eps"], a["q"], a["n_rows"], a["heads"],
+                a["qpos"], a["cs"], a["max_pos"], a["payload"], a["scale"], a["num_pages"], a["qp"], a["qs"], a["cl"],
+                a["rs"], a["num_ctas"], a["sched"], a["sched_bytes"], a["status"], None)
+    assert f(*args(n_new=-1)) == INVALID
+    assert f(*args(heads=32)) == UNSUPPORTED
+    assert f(*args(pos=None)) == INVALID          # K store arguments
+    assert f(*args(payload=M4)) == INVALID
+    assert f(*args(q=None)) == INVALID            # Q quant arguments
+    assert f(*args(qp=M4)) == INVALID
+    assert f(*args(cl=M1)) == INVALID             # schedule arguments
+    assert f(*args(sched=None)) == INVALID
+    assert f(*args(sched=M4)) == INVALID
+    assert f(*args(status=M1)) == INVALID
+    need = lib.fp4idx_schedule_workspace_bytes(2, 152)
+    assert f(*args(sched_bytes=need - 1)) == WORKSPACE
+    assert f(*args(max_pos=0)) == INVALID
 
 
 def test_topk(lib):

@@ -31,10 +31,11 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["two_launches", "fused"])
 @pytest.mark.parametrize("seed,lens,rps,k,zeros", SMALL)
-def test_small_batches_against_oracle(cs, seed, lens, rps, k, zeros):
+def test_small_batches_against_oracle(cs, seed, lens, rps, k, zeros, fused):
     b = wl.small_batch(seed, lens, rows_per_seq=rps, topk=k, zero_rows=zeros)
-    got = run_gpu_indexer(b, cs)
+    got = run_gpu_indexer(b, cs, fused=fused)
     assert got["status"] == 0
     ref = oracle.run_indexer(b, cs)
     assert np.array_equal(got["payload"].cpu().numpy(), ref["payload"])
@@ -146,8 +147,8 @@ def test_workloads_against_oracle(cs, maker, nsample):
 
 def _read_side(b, cs, payload, scale, sched=None, separate=False, k=None):
     """The read side alone on a stored cache: Q quant, schedule (unless given), then either
-    the fused call (fp4idx_logits_topk) or the two separate calls (fp4idx_logits, then
-    fp4idx_topk).  Returns (status, logits, topk)."""
+    the fused call (fp4idx_logits_topk_fused) or the two separate calls (fp4idx_logits,
+    then fp4idx_topk).  Returns (status, logits, topk)."""
     from sparse_attention_fp4_gb300 import fp4idx
     from tests.gpu_util import bf16, dev
     k = b.topk if k is None else k
@@ -169,7 +170,7 @@ def _read_side(b, cs, payload, scale, sched=None, separate=False, k=None):
     else:
         ws = torch.empty(fp4idx.logits_workspace_bytes(T, Lmax, k), dtype=torch.uint8, device="cuda")
         fp4idx.logits_topk(qp, qs, dev(b.w), payload, scale, pt, rs, cl, Lmax, k, sched, ws, topk, logits_out=lg,
-                           status=status)
+                           status=status, fused=True)
     torch.cuda.synchronize()
     return fp4idx.read_status(status), lg.cpu().numpy(), topk.cpu().numpy()
 
@@ -227,7 +228,7 @@ def test_fused_selection_of_rows_past_shared_memory(cs):
     b = wl.small_batch(45, [40000, 33000, 65536, 32769], rows_per_seq=1, topk=2048)
     # the decode query position 4L - 1 would pass the RoPE table for these lengths
     b.q_positions = np.minimum(b.q_positions, wl.ROPE_MAX_POS - 1).astype(np.int32)
-    got = run_gpu_indexer(b, cs)
+    got = run_gpu_indexer(b, cs, fused=True)
     assert got["status"] == 0
     ref = oracle.run_indexer(b, cs)
     for t in range(b.n_rows):
@@ -237,15 +238,18 @@ def test_fused_selection_of_rows_past_shared_memory(cs):
         check_topk_self(got["topk"][t], got["logits"][t], L, b.topk, "row %d" % t)
 
 
-@pytest.mark.parametrize("extra", [0, 1])
-def test_row_count_at_the_fused_limit(cs, extra):
-    """As many rows as SMs (the fused selection) and one more (the separate top-k launch)."""
+@pytest.mark.parametrize("rows", ["half", "half+1", "sms", "sms+1"])
+def test_row_count_at_the_fused_limits(cs, rows):
+    """The fused call at its limits: a CTA pair per row up to half as many rows as SMs, one
+    CTA per row up to as many rows as SMs, the two launches beyond."""
     from sparse_attention_fp4_gb300 import fp4idx
-    n = fp4idx.num_sms() + extra
+    sms = fp4idx.num_sms()
+    n = {"half": sms // 2, "half+1": sms // 2 + 1, "sms": sms, "sms+1": sms + 1}[rows]
+    extra = n % 2
     rng = np.random.default_rng(46 + extra)
     lens = [int(x) for x in rng.integers(0, 3000, size=n)]
     b = wl.small_batch(46 + extra, lens, rows_per_seq=1, topk=300)
-    got = run_gpu_indexer(b, cs)
+    got = run_gpu_indexer(b, cs, fused=True)
     assert got["status"] == 0
     ref = oracle.run_indexer(b, cs)
     for t in range(b.n_rows):

@@ -33,15 +33,16 @@ def _check_batch(b, cs, got):
         check_topk(got["topk"][t], ref["logits"][t], ref["bound"][t], L, b.topk, "row %d" % t)
 
 
-def test_fp4_logits_wait_runs_out_then_recovers(cs, waits_restored):
+@pytest.mark.parametrize("fused", [False, True], ids=["two_launches", "fused"])
+def test_fp4_logits_wait_runs_out_then_recovers(cs, waits_restored, fused):
     fp4idx = waits_restored
     b = wl.small_batch(60, [3000, 700, 64], rows_per_seq=2, topk=128)
     fp4idx.test_pipeline_waits(True, LIMIT_NS)
-    stalled = run_gpu_indexer(b, cs)
+    stalled = run_gpu_indexer(b, cs, fused=fused)
     assert stalled["status"] == TIMEOUT
     fp4idx.test_pipeline_waits(False, 0)
     # the same cache and a fresh schedule: the context is intact and the result exact
-    _check_batch(b, cs, run_gpu_indexer(b, cs, payload=stalled["payload"], scale=stalled["scale"]))
+    _check_batch(b, cs, run_gpu_indexer(b, cs, payload=stalled["payload"], scale=stalled["scale"], fused=fused))
 
 
 def test_fp8_logits_wait_runs_out_then_recovers(cs, waits_restored):
