@@ -27,10 +27,12 @@
 // through distributed shared memory after each counting pass; the emit then places each
 // CTA's slice from the lower CTA's totals.
 //
-// The code runs once per row and is bound by instruction issue and by fetching its own
-// instructions, not by bytes: its loops are kept rolled (a copy of the code that fits the
-// instruction cache) and the row is brought in by the copy engine instead of by unrolled
-// register loads.
+// The code runs once per row and is bound by latency and instruction issue, not by bytes.
+// Two forms of its loops: in the standalone kernel (1,024 threads, little other code) they
+// are unrolled, with the row's first 128 KB loaded into registers at once; inside the
+// logits kernel (512 threads, a large kernel around it) they are kept rolled, so that the
+// selection fits the instruction cache, and the row arrives by one bulk copy instead of
+// unrolled register loads.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -138,6 +140,8 @@ template <int NT>
 struct Select {
   static constexpr int kThreads = NT;
   static constexpr int kWarps = NT / 32;
+  static constexpr bool kCompact = NT < 1024;  // rolled loops, bulk-copied row (see above)
+  static constexpr int kU = 8192 / NT;         // 16-byte loads in flight per thread in the unrolled form
   // groups of four positions per emit block: runs of at most 16 groups (64 positions, one
   // 64-bit mask) a thread; 512 threads cover 32,768 positions in one block, so half of the
   // longest row (a CTA of a pair) is always one block
@@ -247,7 +251,7 @@ struct Select {
   // Start of a row: thread 0 sets up the barrier of the row's bulk copy; the caller's
   // next CTA barrier makes it visible before anyone waits on it.
   static __device__ __forceinline__ void begin_row(Shared& sh) {
-    if (threadIdx.x == 0) {
+    if (kCompact && threadIdx.x == 0) {  // the unrolled form loads without a bulk copy
       ptx::mbar_init(ptx::smem_addr(&sh.bar), 1);
       ptx::fence_mbar_init();
     }
@@ -262,13 +266,47 @@ struct Select {
   // copy's barrier comes from begin_row(), with a CTA barrier in between.
   template <bool kCoherent, class Count>
   static __device__ __forceinline__ void load_keys(const float* lg, int L, int vs, int ve, const RowKeys& keys,
-                                                   Shared& sh, int32_t* status, Count count) {
+                                                   Shared& sh, int32_t* status, int* clear, int nclear,
+                                                   Count count) {
     const int tid = threadIdx.x;
     const bool vec = (reinterpret_cast<uintptr_t>(lg) & 15) == 0;
+    if constexpr (!kCompact) {
+      // the first kU groups a thread in registers, issued before the counts are cleared
+      float4 r[kU];
+#pragma unroll
+      for (int u = 0; u < kU; u++) {
+        const int v = vs + u * NT + tid;
+        if (v < ve) r[u] = load_group<kCoherent>(lg, vec, v, L);
+      }
+      for (int b = tid; b < nclear; b += NT) clear[b] = 0;
+      __syncthreads();
+      for (int v0 = vs; v0 < ve; v0 += kU * NT) {
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+          const int v = v0 + u * NT + tid;
+          if (v < ve) {
+            const uint4 q = keys_of(r[u]);
+            keys.put(v, q);
+            count(v, q);
+          }
+        }
+        const int vn = v0 + kU * NT;
+        if (vn < ve) {
+#pragma unroll
+          for (int u = 0; u < kU; u++) {
+            const int v = vn + u * NT + tid;
+            if (v < ve) r[u] = load_group<kCoherent>(lg, vec, v, L);
+          }
+        }
+      }
+      __syncthreads();
+      return;
+    }
     const int vsm = min(ve, vs + keys.res / 4);  // end of the groups held in shared memory
     const int vfull = min(vsm, L >> 2);          // ... of those wholly inside the row
     const bool bulk = vec && vfull > vs;
     const uint32_t bar = ptx::smem_addr(&sh.bar);
+    for (int b = tid; b < nclear; b += NT) clear[b] = 0;
     if (bulk && tid == 0) {
       if constexpr (kCoherent) ptx::fence_proxy_async_global();
       const uint32_t bytes = 16u * (uint32_t)(vfull - vs);
@@ -331,14 +369,25 @@ struct Select {
     const int tid = threadIdx.x;
     for (int b = tid; b < kDigits; b += NT) hist[b] = 0;
     __syncthreads();
-#pragma unroll 1
-    for (int v = vs + tid; v < ve; v += NT) {
+    auto one = [&](int v) {
       const uint4 q = keys.get(v);
       const uint32_t m = group_mask(q, v, L, [&](uint32_t u) { return (u >> match_shift) == match; });
       if (m) {  // members are a few percent of the row
 #pragma unroll
         for (int e = 0; e < 4; e++)
           if ((m >> e) & 1u) atomicAdd(&hist[(lane_of(q, e) >> shift) & (kDigits - 1)], 1);
+      }
+    };
+    if constexpr (kCompact) {
+#pragma unroll 1
+      for (int v = vs + tid; v < ve; v += NT) one(v);
+    } else {
+      for (int v0 = vs; v0 < ve; v0 += kU * NT) {
+#pragma unroll
+        for (int j = 0; j < kU; j++) {
+          const int v = v0 + j * NT + tid;
+          if (v < ve) one(v);
+        }
       }
     }
     __syncthreads();
@@ -350,12 +399,19 @@ struct Select {
                                                    uint64_t& gtm, uint64_t& eqm) {
     gtm = 0;
     eqm = 0;
-#pragma unroll 1
-    for (int j = 0; j < mine; j++) {
+    auto one = [&](int j) {
       const int g = g0 + j;
       const uint4 q = keys.get(g);
       gtm |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return u > tau; }) << (4 * j);
       eqm |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return u == tau; }) << (4 * j);
+    };
+    if constexpr (kCompact) {
+#pragma unroll 1
+      for (int j = 0; j < mine; j++) one(j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRunMax; j++)
+        if (j < mine) one(j);
     }
   }
 
@@ -470,12 +526,19 @@ struct Select {
     const int g0 = vs + min(nbg, tid * run);
     const int mine = min(run, ve - g0);
     uint64_t sel = 0, mem = 0;
-#pragma unroll 1
-    for (int j = 0; j < mine; j++) {
+    auto one = [&](int j) {
       const int g = g0 + j;
       const uint4 q = keys.get(g);
       sel |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return (u >> kDigitBits) > hi22; }) << (4 * j);
       mem |= (uint64_t)group_mask(q, g, L, [&](uint32_t u) { return (u >> kDigitBits) == hi22; }) << (4 * j);
+    };
+    if constexpr (kCompact) {
+#pragma unroll 1
+      for (int j = 0; j < mine; j++) one(j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kRunMax; j++)
+        if (j < mine) one(j);
     }
     // the sub-bin's keys (a few in the whole row) into the list
     for (uint64_t mm = mem; mm;) {
@@ -550,9 +613,17 @@ struct Select {
       const int g0 = b0 + min(nbg, tid * run);
       const int mine = min(run, b0 + nbg - g0);
       uint64_t gtm = 0;
-#pragma unroll 1
-      for (int j = 0; j < mine; j++)
+      auto one = [&](int j) {
         gtm |= (uint64_t)group_mask(keys.get(g0 + j), g0 + j, L, [&](uint32_t u) { return u > tau; }) << (4 * j);
+      };
+      if constexpr (kCompact) {
+#pragma unroll 1
+        for (int j = 0; j < mine; j++) one(j);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kRunMax; j++)
+          if (j < mine) one(j);
+      }
       uint32_t tot;
       const uint32_t pre = block_excl_scan((uint32_t)__popcll(gtm), sh.scratch, tot);
       int w = (rank == 1 ? k - (int)tot : done) + (int)pre;
@@ -649,8 +720,7 @@ struct Select {
     const RowKeys keys{spill, dyn + (kC > 1 ? 2 * kHist + kDigits : kHist), res, vs};
 
     // ---- 1. keys of the slice and their top-bits histogram
-    for (int b = tid; b < kHist; b += NT) hist[b] = 0;
-    load_keys<kCoherent>(lg, L, vs, ve, keys, sh, status, [&](int v, const uint4& q) {
+    load_keys<kCoherent>(lg, L, vs, ve, keys, sh, status, hist, kHist, [&](int v, const uint4& q) {
       const int i = 4 * v;
       atomicAdd(&hist[q.x >> kLowBits], 1);
       if (i + 1 < L) atomicAdd(&hist[q.y >> kLowBits], 1);
