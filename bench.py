@@ -36,10 +36,12 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_decode_b64_traffic.js
 LOGITS_SRC = os.path.join(ROOT, "sparse_attention_fp4_gb300", "csrc", "logits_mxf4.cu")
 
 WORKLOADS = {
-    "decode_b64": ("decode_batch64", 1001),
-    "tiny": ("tiny_decode", 1000),
-    "draft_b256": ("draft_batch256", 1002),
-    "prefill": ("prefill_chunk", 1003),
+    "decode_b64": ("decode_batch64", 1001, {}),
+    "tiny": ("tiny_decode", 1000, {}),
+    "draft_b256": ("draft_batch256", 1002, {}),
+    "prefill": ("prefill_chunk", 1003, {}),
+    # the last 1,024 rows of the prefill chunk (for profiling captures)
+    "prefill_1024": ("prefill_chunk", 1003, {"rows": 1024}),
 }
 
 
@@ -84,8 +86,8 @@ def aggregate(rows_this_rank: int, seconds_this_rank: float, device=None):
 # ------------------------------------------------------------------ workload
 def make_batch(name):
     from sparse_attention_fp4_gb300 import workloads as wl
-    fn, seed = WORKLOADS[name]
-    return getattr(wl, fn)(seed)
+    fn, seed, kw = WORKLOADS[name]
+    return getattr(wl, fn)(seed, **kw)
 
 
 def newest_rows(b):
@@ -221,7 +223,7 @@ def gpu_id_for(device_index):
 class DecodeStep:
     """Device-resident inputs of one decode batch and the five launches of a step."""
 
-    def __init__(self, b, device, fused=False):
+    def __init__(self, b, device, fused=False, prep="one"):
         import torch
 
         from sparse_attention_fp4_gb300 import fp4idx
@@ -273,6 +275,7 @@ class DecodeStep:
         self.fused_ws = torch.empty(fp4idx.logits_workspace_bytes(self.T, self.max_ctx, self.k), dtype=torch.uint8,
                                     device=device)
         self.fused = fused  # False: fp4idx_logits_topk (two launches); True: fp4idx_logits_topk_fused
+        self.prep = prep  # "one": fp4idx_prepare_step; "three": schedule, K store and Q quant calls
         torch.cuda.synchronize(device)
 
     def calls(self):
@@ -281,9 +284,17 @@ class DecodeStep:
         then the read side -- the logits launch and the top-k launch of
         fp4idx_logits_topk, or with `fused` the one launch of fp4idx_logits_topk_fused."""
         f = self.fp4idx
-        base = [("prepare_step", lambda: f.prepare_step(
-            self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.q, self.qpos, self.cs, self.payload,
-            self.scale, self.qp, self.qs, self.cl, self.rs, self.sched, status=self.status))]
+        if self.prep == "one":
+            base = [("prepare_step", lambda: f.prepare_step(
+                self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps, self.q, self.qpos, self.cs,
+                self.payload, self.scale, self.qp, self.qs, self.cl, self.rs, self.sched, status=self.status))]
+        else:  # the three calls fp4idx_prepare_step stands for, one after another
+            base = [
+                ("build_schedule", lambda: f.build_schedule(self.cl, self.rs, self.sched)),
+                ("store_k", lambda: f.store_k(self.new_k, self.new_pos, self.new_slots, self.norm_w, self.eps,
+                                              self.cs, self.payload, self.scale, status=self.status)),
+                ("quant_q", lambda: f.quant_q(self.q, self.qpos, self.cs, self.qp, self.qs, status=self.status)),
+            ]
         if self.fused:
             return base + [("logits_topk_fused", self.logits_topk)]
         return base + [
@@ -311,18 +322,23 @@ class DecodeStep:
         issued one by one with a mark before each and after the last."""
         import torch
         calls = self.calls()
-        calls[0][1]()
+        n = self.n_prep()
+        for _, fn in calls[:n]:
+            fn()
         if marks:
             cur = torch.cuda.current_stream()
-            for i, (_, fn) in enumerate(calls[1:]):
+            for i, (_, fn) in enumerate(calls[n:]):
                 marks[i].record(cur)
                 fn()
-            marks[len(calls) - 1].record(cur)
+            marks[len(calls) - n].record(cur)
         else:
             self.logits_topk()
 
     def read_side_names(self):
-        return [n for n, _ in self.calls()[1:]]
+        return [n for n, _ in self.calls()[self.n_prep():]]
+
+    def n_prep(self):
+        return 1 if self.prep == "one" else 3
 
 
 def run_gpu(args):
@@ -333,7 +349,7 @@ def run_gpu(args):
     device = torch.device("cuda", local)
     dist_init("nccl")
     b = make_batch(args.workload)
-    st = DecodeStep(b, device, fused=args.fused)
+    st = DecodeStep(b, device, fused=args.fused, prep=args.prep)
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -459,7 +475,7 @@ def run_gpu(args):
                 "algorithmic_bytes": main_bytes, "avg_launch_us": round(logits_us, 2),
                 "launch_timing": timing_src,
                 "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
-    if args.workload == "prefill":
+    if args.workload.startswith("prefill"):
         # one sequence's 1.2 MB of K stays in L2: the launch is bound by the contraction and
         # its epilogue, so it is measured against the tensor peak
         fl = logits_flops(b)
@@ -482,8 +498,10 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1,ue8m0)->f32", "data": "synthetic",
             "config": {"workload": b.name, "rows": b.n_rows, "heads": 64, "head_dim": 128, "topk": b.topk,
                        "context_tokens": int(b.context_lens.sum()), "cache_pages": b.num_pages,
-                       "step": "fp4idx_prepare_step (schedule + K store of the newest token per sequence + Q "
-                               "quant, one launch) + %s, one CUDA graph replay" % (
+                       "step": "%s + %s, one CUDA graph replay" % (
+                                   "fp4idx_prepare_step (schedule + K store of the newest token per sequence + Q "
+                                   "quant, one launch)" if st.prep == "one" else
+                                   "fp4idx_build_schedule, fp4idx_store_k, fp4idx_quant_q",
                                    "fp4idx_logits_topk_fused (logits and selection in one launch)" if st.fused else
                                    "fp4idx_logits_topk (logits launch, top-k launch)"),
                        "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
@@ -987,6 +1005,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prep", choices=["one", "three"], default="one",
+                    help="step preparation as fp4idx_prepare_step (one launch) or as its three calls")
     ap.add_argument("--fused", action="store_true",
                     help="read side through fp4idx_logits_topk_fused (one launch) instead of fp4idx_logits_topk")
     args = ap.parse_args(argv)
