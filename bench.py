@@ -8,9 +8,13 @@ tokens, pages from a permuted 40,960-page pool, 64 heads x 128, k = 2,048.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fp4idx|reference]
 
-Prints one JSON line (rank 0).  --impl reference times the CPU oracle on this
-host's cores on the same workload (rows sampled per step).  Under torchrun each
-rank runs its own replica of the batch (weak scaling, no data-path collective).
+Prints one JSON line (rank 0).  On one GPU the default line also carries
+`per_config`: the tiny decode, the draft batch (256 x 6 rows), the 8,192-row prefill
+chunk and the 65,536-row K store, each measured the same way with a bounded number of
+steps, with its own roofline object and a bounded oracle sample (--no-per-config leaves
+them out).  --impl reference times the CPU oracle on this host's cores on the same
+workload (rows sampled per step).  Under torchrun each rank runs its own replica of the
+batch (weak scaling, no data-path collective).
 """
 from __future__ import annotations
 
@@ -32,7 +36,7 @@ if ROOT not in sys.path:
 METRIC = "FP4 indexer decode: K-cache GB/s vs HBM peak; query rows/s (logits+top-k)"
 UNIT = "query rows/s"
 L2_FLUSH_BYTES = 256 << 20
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_decode_b64_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "logits_mxf4_traffic.json")
 LOGITS_SRC = os.path.join(ROOT, "sparse_attention_fp4_gb300", "csrc", "logits_mxf4.cu")
 
 WORKLOADS = {
@@ -118,15 +122,19 @@ def algorithmic_bytes(b):
 LOGITS_DEPS = ("logits_mxf4.cu", "ptx.cuh", "schedule.cuh", "fp4idx_internal.cuh", "select.cuh", "pipeline.cuh")
 
 
-def kernel_source_hash():
-    """Hash of the logits kernel's sources: a stored DRAM traffic figure is reported only
-    while the kernel it was measured on is unchanged."""
+def source_hash(deps):
+    """Hash of a kernel's sources: a stored DRAM traffic figure is reported only while the
+    kernel it was measured on is unchanged."""
     h = hashlib.sha256()
-    for f in LOGITS_DEPS:
+    for f in deps:
         with open(os.path.join(os.path.dirname(LOGITS_SRC), f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    return source_hash(LOGITS_DEPS)
 
 
 def measured_peaks():
@@ -341,24 +349,40 @@ class DecodeStep:
         return 1 if self.prep == "one" else 3
 
 
-def run_gpu(args):
+def make_flush(device):
+    """L2 flush between timed launches: a 256 MiB write and a 256 MiB read (twice the L2)."""
     import torch
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist_init("nccl")
-    b = make_batch(args.workload)
-    st = DecodeStep(b, device, fused=args.fused, prep=args.prep)
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     def flush_l2():
         flush_w.zero_()
         _ = flush_r.sum()
+    return flush_l2
 
-    # warm-up (also sets kernel attributes before capture)
-    for _ in range(max(3, args.warmup)):
+
+SPIN_CYCLES = int(2e5)  # ~0.1 ms at GB300 clocks: covers the host's enqueue of the next step
+
+
+def stored_traffic(workload):
+    """DRAM bytes per logits launch from an ncu capture of this workload, or None when no
+    capture exists or the kernel's sources changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        tr = json.load(f)
+    if tr.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    w = tr.get("workloads", {}).get(workload)
+    return w.get("dram_bytes_per_launch") if w else None
+
+
+def time_step(st, steps, warmup, flush_l2, device, live_n=500, alone_n=200):
+    """Times the step of `st` as one CUDA graph replay per step (L2 flushed and a spin
+    kernel ahead of each, outside the events), then the read side's launches inside an
+    instrumented copy of the graph, then every launch captured and replayed alone."""
+    import torch
+    for _ in range(max(3, warmup)):  # warm-up (also sets kernel attributes before capture)
         st.launch()
     torch.cuda.synchronize()
     assert st.fp4idx.read_status(st.status) == 0, "device status after warm-up"
@@ -383,22 +407,21 @@ def run_gpu(args):
             st.launch_step(marks)
     except TypeError:
         marks, gm = None, None
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         g.replay()
     torch.cuda.synchronize()
 
-    spin_cycles = int(2e5)  # ~0.1 ms at GB300 clocks: covers the host's enqueue of the next step
-    K = args.steps
+    K = steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    sampler = ClockSampler(gpu_id_for(local)).start()
+    sampler = ClockSampler(gpu_id_for(device.index)).start()
     time.sleep(0.3)
     dist_barrier()
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
     for i in range(K):
         flush_l2()
-        torch.cuda._sleep(spin_cycles)
+        torch.cuda._sleep(SPIN_CYCLES)
         starts[i].record()
         g.replay()
         ends[i].record()
@@ -407,25 +430,19 @@ def run_gpu(args):
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
     step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
-    total_s = sum(step_ms) / 1e3
-    value, slowest = aggregate(st.T * K, total_s, device)
-    ms_per_step = slowest / K * 1e3
 
     # kernel times inside the step, from the instrumented graph (same flush and spin)
-    Kb = min(K, 500)
     live = {n: [] for n in names}
     if marks:
-        for i in range(Kb):
+        for i in range(min(K, live_n)):
             flush_l2()
-            torch.cuda._sleep(spin_cycles)
+            torch.cuda._sleep(SPIN_CYCLES)
             gm.replay()
             marks[-1].synchronize()  # every replay re-records the marks: read them now
             for j, n in enumerate(names):
                 live[n].append(marks[j].elapsed_time(marks[j + 1]) * 1e3)
 
     # per-kernel breakdown: each launch captured in its own graph and replayed alone
-    # (L2 flushed, a spin kernel ahead of it so no host time falls inside the events)
-    Kb = min(K, 200)
     subs = []
     for name, fn in st.calls():
         sg = torch.cuda.CUDAGraph()
@@ -433,12 +450,12 @@ def run_gpu(args):
             fn()
         subs.append((name, sg))
     per_times = {name: [] for name, _ in subs}
-    for i in range(Kb):
+    for i in range(min(K, alone_n)):
         for name, sg in subs:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             flush_l2()
-            torch.cuda._sleep(spin_cycles)
+            torch.cuda._sleep(SPIN_CYCLES)
             e0.record()
             sg.replay()
             e1.record()
@@ -456,40 +473,98 @@ def run_gpu(args):
         logits_us = statistics.mean([a.elapsed_time(b) for a, b in per_times[main]]) * 1e3
         live_us = None
         timing_src = "the launch captured alone in a graph (includes the graph launch), mean"
-    status = st.fp4idx.read_status(st.status)
+    return dict(total_s=sum(step_ms) / 1e3, t_wall=t_wall, clocks=clocks, live_us=live_us,
+                alone_us={k: round(v, 2) for k, v in per.items()}, logits_us=logits_us, timing_src=timing_src,
+                status=st.fp4idx.read_status(st.status))
 
+
+def roofline_for(b, workload, st, logits_us, timing_src):
+    """Roofline object of the logits launch: HBM-bound against the measured copy
+    bandwidth, except for the prefill chunk, whose one sequence's K stays in L2 and which is
+    measured against the FP4 tensor peak."""
     ab = algorithmic_bytes(b)
+    traffic = stored_traffic(workload)
+    kname = "logits_mxf4_kernel" + (" (with the fused top-k selection)" if st.fused else "")
+    if workload.startswith("prefill"):
+        fl = logits_flops(b)
+        tpk, tpk_src = measured_fp4_tflops()
+        tach = fl / (logits_us * 1e-6) / 1e12
+        return {"bound": "tensor", "achieved": round(tach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
+                "frac": round(tach / tpk, 4), "traffic": traffic, "kernel": kname, "algorithmic_flops": fl,
+                "avg_launch_us": round(logits_us, 2), "launch_timing": timing_src, "peak_source": tpk_src}
     peak, peak_kind = measured_peaks()
     # the fused launch also writes the selection (4 B an index)
     main_bytes = ab["logits_pass"] + (ab["topk_out"] if st.fused else 0.0)
     achieved = main_bytes / (logits_us * 1e-6) / 1e9
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f)
-        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == args.workload:
-            traffic = tr.get("dram_bytes_per_launch")
-    kname = "logits_mxf4_kernel" + (" (with the fused top-k selection)" if st.fused else "")
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
-                "algorithmic_bytes": main_bytes, "avg_launch_us": round(logits_us, 2),
-                "launch_timing": timing_src,
-                "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
-    if args.workload.startswith("prefill"):
-        # one sequence's 1.2 MB of K stays in L2: the launch is bound by the contraction and
-        # its epilogue, so it is measured against the tensor peak
-        fl = logits_flops(b)
-        tpk, tpk_src = measured_fp4_tflops()
-        tach = fl / (logits_us * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(tach, 1), "peak": round(tpk, 1), "unit": "TFLOP/s",
-                    "frac": round(tach / tpk, 4), "traffic": traffic, "kernel": kname,
-                    "algorithmic_flops": fl, "avg_launch_us": round(logits_us, 2), "launch_timing": timing_src,
-                    "peak_source": tpk_src}
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname,
+            "algorithmic_bytes": main_bytes, "avg_launch_us": round(logits_us, 2), "launch_timing": timing_src,
+            "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
 
+
+def step_description(st):
+    return "%s + %s, one CUDA graph replay" % (
+        "fp4idx_prepare_step (schedule + K store of the newest token per sequence + Q quant, one launch)"
+        if st.prep == "one" else "fp4idx_build_schedule, fp4idx_store_k, fp4idx_quant_q",
+        "fp4idx_logits_topk_fused (logits and selection in one launch)" if st.fused else
+        "fp4idx_logits_topk (logits launch, top-k launch)")
+
+
+# the other configurations the default line carries: (workload, timed steps, CPU seconds)
+PER_CONFIG = (("tiny", 2000, 3.0), ("draft_b256", 200, 5.0), ("prefill", 50, 5.0))
+
+
+def measure_config(workload, steps, cpu_seconds, args, device, flush_l2):
+    """One of the other configurations, measured the way the headline is (step graph, L2
+    flushed between steps) with a bounded number of steps, and its oracle on the host
+    cores for a bounded sample."""
+    import torch
+    b = make_batch(workload)
+    st = DecodeStep(b, device, fused=args.fused, prep=args.prep)
+    r = time_step(st, steps, args.warmup, flush_l2, device, live_n=min(steps, 200), alone_n=min(steps, 50))
+    value = st.T * steps / r["total_s"]
+    out = {"workload": b.name, "rows": b.n_rows, "topk": b.topk, "context_tokens": int(b.context_lens.sum()),
+           "value": round(value, 1), "unit": UNIT, "steps": steps, "ms_per_step": round(r["total_s"] / steps * 1e3, 5),
+           "kernel_us_in_step": r["live_us"], "kernel_us_alone": r["alone_us"],
+           "roofline": roofline_for(b, workload, st, r["logits_us"], r["timing_src"]),
+           "clocks": r["clocks"], "device_status": r["status"], "gpu_launches": len(st.calls()) * steps}
+    del st
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(b, cpu_seconds)
+    return out
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init("nccl")
+    b = make_batch(args.workload)
+    st = DecodeStep(b, device, fused=args.fused, prep=args.prep)
+    flush_l2 = make_flush(device)
+
+    K = args.steps
+    r = time_step(st, K, args.warmup, flush_l2, device)
+    value, slowest = aggregate(st.T * K, r["total_s"], device)
+    ms_per_step = slowest / K * 1e3
+    ab = algorithmic_bytes(b)
+    roofline = roofline_for(b, args.workload, st, r["logits_us"], r["timing_src"])
+
+    desc = step_description(st)
+    launches = len(st.calls()) * K
     e2e = run_e2e(st, args, flush_l2) if not args.no_e2e else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(b, args)
+        cpu = cpu_baseline(b, args.cpu_seconds)
+    per_config = None
+    if world == 1 and args.workload == "decode_b64" and not args.no_per_config:
+        del st
+        torch.cuda.empty_cache()
+        per_config = {w: measure_config(w, n, c, args, device, flush_l2) for w, n, c in PER_CONFIG}
+        per_config["kstore"] = measure_kstore(args, device)
 
     if rank == 0:
         line = {
@@ -498,25 +573,22 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1,ue8m0)->f32", "data": "synthetic",
             "config": {"workload": b.name, "rows": b.n_rows, "heads": 64, "head_dim": 128, "topk": b.topk,
                        "context_tokens": int(b.context_lens.sum()), "cache_pages": b.num_pages,
-                       "step": "%s + %s, one CUDA graph replay" % (
-                                   "fp4idx_prepare_step (schedule + K store of the newest token per sequence + Q "
-                                   "quant, one launch)" if st.prep == "one" else
-                                   "fp4idx_build_schedule, fp4idx_store_k, fp4idx_quant_q",
-                                   "fp4idx_logits_topk_fused (logits and selection in one launch)" if st.fused else
-                                   "fp4idx_logits_topk (logits launch, top-k launch)"),
+                       "step": desc,
                        "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "kcache_gbs": round(ab["k_cache"] / (logits_us * 1e-6) / 1e9, 1),
-            "kernel_us_in_step": live_us,
-            "kernel_us_alone": {k: round(v, 2) for k, v in per.items()},
+            "kcache_gbs": round(ab["k_cache"] / (r["logits_us"] * 1e-6) / 1e9, 1),
+            "kernel_us_in_step": r["live_us"],
+            "kernel_us_alone": r["alone_us"],
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": len(st.calls()) * K,
-            "clocks": clocks,
-            "wall_s_timed_region": round(t_wall, 3),
-            "device_status": status,
+            "gpu_launches": launches,
+            "clocks": r["clocks"],
+            "wall_s_timed_region": round(r["t_wall"], 3),
+            "device_status": r["status"],
         }
+        if per_config is not None:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
 
 
@@ -622,13 +694,13 @@ class OracleStep:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(b, args):
+def cpu_baseline(b, seconds):
     import oracle
     cores = oracle.max_threads()
     step = OracleStep(b)
     rows_per = 8
     done, secs, i = 0, 0.0, 0
-    while secs < args.cpu_seconds and done < b.n_rows * 4:
+    while secs < seconds and done < b.n_rows * 4:
         rows = np.arange(i, i + rows_per) % b.n_rows
         secs += step.run(rows)
         done += rows_per
@@ -664,7 +736,21 @@ def run_reference(args):
     }), flush=True)
 
 
-def run_kstore(args):
+KSTORE_DEPS = ("store_quant.cu", "schedule_build.cuh", "schedule.cuh", "launchers.cuh", "fp4idx_internal.cuh")
+KSTORE_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "store_k_traffic.json")
+
+
+def stored_kstore_traffic():
+    """DRAM bytes per launch of store_k_kernel on the 65,536-row workload, from an ncu
+    capture, while the kernel's sources are unchanged since it was taken."""
+    if not os.path.exists(KSTORE_TRAFFIC_FILE):
+        return None
+    with open(KSTORE_TRAFFIC_FILE) as f:
+        tr = json.load(f)
+    return tr.get("dram_bytes_per_launch") if tr.get("kernel_source_hash") == source_hash(KSTORE_DEPS) else None
+
+
+def measure_kstore(args, device):
     """The K-store configuration alone: 65,536 bf16 index-K rows through RMSNorm, RoPE,
     Hadamard and FP4 quantisation into scattered slots of a 2,048-page split cache (and the
     same rows into the 132 B/token FP8 layout), timed as captured graphs with the L2
@@ -672,8 +758,6 @@ def run_kstore(args):
     import torch
     from sparse_attention_fp4_gb300 import fp4idx
     from sparse_attention_fp4_gb300 import workloads as wl
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
     ks = wl.kstore_65536()
     bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
     k = bf16(ks.k_rows)
@@ -681,13 +765,15 @@ def run_kstore(args):
     slots = torch.from_numpy(ks.slots).to(device)
     nw = bf16(ks.norm_w)
     cs = bf16(wl.rope_cos_sin_table())
-    payload, scale = fp4idx.alloc_cache(ks.num_pages)
+    payload, scale = fp4idx.alloc_cache(ks.num_pages, device=device)
     fp8 = torch.zeros((ks.num_pages, fp4idx.FP8_PAGE_BYTES), dtype=torch.uint8, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     calls = {"fp4": lambda: fp4idx.store_k(k, pos, slots, nw, ks.eps, cs, payload, scale, status=status),
              "fp8": lambda: fp4idx.store_k_fp8(k, pos, slots, nw, ks.eps, cs, fp8, status=status)}
     res = {}
+    n_timed = min(args.steps, 200)
+    sampler = ClockSampler(gpu_id_for(device.index)).start()
     for name, fn in calls.items():
         for _ in range(max(3, args.warmup)):
             fn()
@@ -696,9 +782,9 @@ def run_kstore(args):
         with torch.cuda.graph(g):
             fn()
         ts = []
-        for _ in range(min(args.steps, 200)):
+        for _ in range(n_timed):
             flush.zero_()
-            torch.cuda._sleep(200000)
+            torch.cuda._sleep(SPIN_CYCLES)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -710,7 +796,9 @@ def run_kstore(args):
         out_b = 68 if name == "fp4" else 132
         nbytes = len(ks.positions) * (256 + 128 + 8 + out_b)  # row + cos/sin + position/slot + written entry
         res[name] = {"us": round(us, 2), "rows_per_s": round(len(ks.positions) / (us * 1e-6), 1),
-                     "algorithmic_gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "bytes_per_token": out_b}
+                     "algorithmic_bytes": nbytes, "algorithmic_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "bytes_per_token": out_b}
+    clocks = sampler.stop()
     assert fp4idx.read_status(status) == 0
     cpu = None
     if not args.no_cpu_baseline:
@@ -719,7 +807,7 @@ def run_kstore(args):
         import oracle
         cs_np = wl.rope_cos_sin_table()
         n, secs, done = 4096, 0.0, 0
-        while secs < args.cpu_seconds and done < len(ks.positions):
+        while secs < min(args.cpu_seconds, 5.0) and done < len(ks.positions):
             sub = dataclasses.replace(ks, k_rows=ks.k_rows[done:done + n], positions=ks.positions[done:done + n],
                                       slots=ks.slots[done:done + n])
             t0 = time.perf_counter()
@@ -728,13 +816,33 @@ def run_kstore(args):
             done += len(sub.positions)
         cpu = {"value": round(done / secs, 1), "unit": "rows/s", "cores": oracle.max_threads(), "kind": "oracle",
                "sample": "%d rows of the same workload in slices of %d; %.1f s" % (done, n, secs)}
-    peak, _ = measured_peaks()
-    print(json.dumps({"metric": "K store rows/s (65,536 rows, split FP4 cache)", "value": res["fp4"]["rows_per_s"],
-                      "unit": "rows/s", "n_gpus": 1, "higher_is_better": True, "data": "synthetic",
-                      "config": {"workload": "kstore_65536", "rows": len(ks.positions), "cache_pages": ks.num_pages,
-                                 "l2": "flushed before every launch"},
-                      "fp4": res["fp4"], "fp8_132B": res["fp8"], "cpu_baseline": cpu,
-                      "frac_of_measured_hbm": round(res["fp4"]["algorithmic_gbs"] / peak, 4)}), flush=True)
+    peak, peak_kind = measured_peaks()
+    fp4 = res["fp4"]
+    roofline = {"bound": "hbm", "achieved": fp4["algorithmic_gbs"], "peak": peak, "unit": "GB/s",
+                "frac": round(fp4["algorithmic_gbs"] / peak, 4), "traffic": stored_kstore_traffic(),
+                "kernel": "store_k_kernel", "algorithmic_bytes": fp4["algorithmic_bytes"], "avg_launch_us": fp4["us"],
+                "launch_timing": "the launch captured alone in a graph, median of %d replays (L2 flushed before each)"
+                                 % n_timed,
+                "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
+    return {"workload": "kstore_65536", "rows": len(ks.positions), "cache_pages": ks.num_pages,
+            "value": fp4["rows_per_s"], "unit": "rows/s", "steps": n_timed, "ms_per_step": round(fp4["us"] / 1e3, 5),
+            "fp4": fp4, "fp8_132B": res["fp8"], "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
+            "gpu_launches": 2 * n_timed}
+
+
+def run_kstore(args):
+    import torch
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    r = measure_kstore(args, device)
+    line = {"metric": "K store rows/s (65,536 rows, split FP4 cache)", "value": r["value"], "unit": "rows/s",
+            "n_gpus": 1, "steps": r["steps"], "warmup": max(3, args.warmup), "ms_per_step": r["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e2m1,ue8m0",
+            "data": "synthetic",
+            "config": {"workload": "kstore_65536", "rows": r["rows"], "cache_pages": r["cache_pages"],
+                       "l2": "flushed before every launch"}}
+    line.update({k: r[k] for k in ("fp4", "fp8_132B", "roofline", "cpu_baseline", "clocks", "gpu_launches")})
+    print(json.dumps(line), flush=True)
 
 
 def run_pages(args):
@@ -1005,6 +1113,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="leave out the other configurations (tiny, draft, prefill, K store) of the default line")
     ap.add_argument("--prep", choices=["one", "three"], default="one",
                     help="step preparation as fp4idx_prepare_step (one launch) or as its three calls")
     ap.add_argument("--fused", action="store_true",

@@ -1,7 +1,9 @@
 // Host helpers shared by the launchers: the tensor-map encoder, per-device kernel
 // attributes, and the pipeline-wait settings (including the test switch that makes a
 // wait run out on purpose).
+#include <algorithm>
 #include <atomic>
+#include <map>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -48,6 +50,28 @@ cudaError_t set_smem_attr_once(const void* kernel, size_t bytes) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) done.insert({kernel, dev});
   return e;
+}
+
+cudaError_t resident_ctas(const void* kernel, int threads, size_t smem, int* out) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> known;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = known.find({kernel, dev});
+  if (it != known.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  int per_sm = 0, sms = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  *out = std::max(1, per_sm) * sms;
+  known[{kernel, dev}] = *out;
+  return cudaSuccess;
 }
 
 namespace {

@@ -18,6 +18,9 @@ EncodeTiledFn encode_tiled_fn();
 bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, uint32_t row_bytes);
 // A kernel's dynamic shared-memory limit, set once per (kernel, device); thread-safe.
 cudaError_t set_smem_attr_once(const void* kernel, size_t bytes);
+// How many CTAs of `threads` threads and `smem` bytes of dynamic shared memory fit on the
+// current device at once (SMs x CTAs per SM), computed once per (kernel, device).
+cudaError_t resident_ctas(const void* kernel, int threads, size_t smem, int* out);
 // How long one pipeline wait of the logits kernels may last before the kernel records
 // FP4IDX_ERR_TIMEOUT and winds down, and whether their producers are told to issue
 // nothing (a test switch, off by default: with it on, every launch ends in that timeout).

@@ -6,23 +6,26 @@
 // even: dsv4.1-amd: KV cache layouts, FP4 indexer, compressor and router kernels --
 // Summary.
 //
-// Mapping: a half-warp owns one 128-wide row, lane l (0..15) holds elements
-// 8l..8l+7 (one 16-byte bf16 load).  Every floating-point operation is an explicit
-// round-to-nearest intrinsic in a fixed order, so the bytes written do not depend
-// on the compiler's contraction choices:
-//   * RMSNorm: each lane sums its 8 squares left to right, the 16 partials are
-//     combined by an xor butterfly (1,2,4,8), which is the pairwise tree in index
-//     order; r = 1/sqrt(mean + eps) with IEEE sqrt and divide; y = (x*r)*w.
-//   * RoPE on dims 0..63, pairs (i, i+32): lanes 0..3 hold the first halves, lanes
-//     4..7 the second halves, exchanged with one xor-4 shuffle.
-//   * Hadamard: stages h = 1,2,4 inside the lane, h = 8..64 across lanes (xor
-//     1,2,4,8), then one multiply by fp32(1/sqrt(128)).
-//   * UE8M0 per 32-element block (4 lanes): smallest e with 6*2^e >= amax, from the
+// Two mappings of a 128-wide row onto lanes.  The query packers give a half-warp a row,
+// lane l (0..15) holding elements 8l..8l+7 (one 16-byte bf16 load); the K stores give a
+// quarter-warp a row (the qw helpers below), with fewer shuffles and redundant per-row
+// steps per row.  Every floating-point operation is an explicit round-to-nearest
+// intrinsic in a fixed order, so the bytes written do not depend on the compiler's
+// contraction choices or on the mapping:
+//   * RMSNorm: each group of 8 squares summed left to right, the 16 group sums combined
+//     by the pairwise tree in index order; r = 1/sqrt(mean + eps) with IEEE sqrt and
+//     divide; y = (x*r)*w.
+//   * RoPE on dims 0..63, pairs (i, i+32): a' = a*c - b*s, b' = b*c + a*s, each product
+//     rounded.
+//   * Hadamard: stages h = 1, 2, 4, ..., 64 in that order, (a, b) -> (a+b, a-b), then one
+//     multiply by fp32(1/sqrt(128)).
+//   * UE8M0 per 32-element block: smallest e with 6*2^e >= amax, from the
 //     exponent/mantissa bits of amax; e2m1 by the hardware RNE-satfinite convert,
 //     the sign of zero taken from the input.
 #include "launchers.cuh"
 #include "schedule_build.cuh"
 
+#include <algorithm>
 #include <atomic>
 
 namespace fp4idx {
@@ -39,19 +42,6 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 u, float v[8]) {
 }
 
 __device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-
-// y <- RMSNorm(x) * w over the half-warp's row.
-__device__ __forceinline__ void rmsnorm_row(float v[8], const float w[8], float eps) {
-  float s = __fmul_rn(v[0], v[0]);
-#pragma unroll
-  for (int e = 1; e < 8; e++) s = __fadd_rn(s, __fmul_rn(v[e], v[e]));
-#pragma unroll
-  for (int m = 1; m < 16; m <<= 1) s = __fadd_rn(s, __shfl_xor_sync(kFull, s, m));
-  const float mean = __fmul_rn(s, 0.0078125f);
-  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-#pragma unroll
-  for (int e = 0; e < 8; e++) v[e] = __fmul_rn(__fmul_rn(v[e], r), w[e]);
-}
 
 // RoPE on dims 0..63 with the bf16 table row at cs_row (cos 0..31 | sin 32..63).
 __device__ __forceinline__ void rope_row(float v[8], const uint16_t* cs_row, int lh) {
@@ -149,114 +139,348 @@ __device__ __forceinline__ uint32_t fp4_encode_lane(const float v[8], uint32_t& 
   return word;
 }
 
-// ------------------------------------------------------------------ kernels
-constexpr int kRowsPerBlock = 16;  // 256 threads, a half-warp per row
+// ------------------------------------------------------------------ quarter-warp row transform
+// The K store maps a row to four lanes (eight rows a warp): lane l of the quarter holds the
+// elements i = 32 m + 8 l + e (m = 0..3 its four 16-byte chunks, e = 0..7), as float pairs
+// x[m][p] = (element 32 m + 8 l + 2 p, element 32 m + 8 l + 2 p + 1).  Index bits 0-2 and 5-6
+// are in the lane's registers, bits 3-4 across the quarter, so that
+//   * RoPE's pairs (i, i + 32) sit in one lane (chunks m = 0 and 1), and every lane rotates
+//     eight of them with its own 16 bytes of cos and of sin;
+//   * five of the seven Hadamard stages run inside the lane, two across it;
+//   * the operations on pairs are the packed f32x2 forms (add/sub/mul/fma .rn), one
+//     rounding per element as in the scalar chain, except where a product feeds a sum
+//     (RoPE): there the scalar forms keep the two roundings apart.
+// The order of every rounded operation is the one the half-warp helpers above follow:
+// squares summed left to right within each group of eight, the sixteen group sums
+// combined by the pairwise tree in index order, the Hadamard stages h = 1 .. 64 in turn.
+namespace qw {
 
-// K store of the 16 rows of block `block` (a half-warp per row).
-__device__ __forceinline__ void store_k_block(int64_t block, const uint16_t* __restrict__ k, int64_t n_rows,
-                                              const int32_t* __restrict__ positions,
-                                              const int32_t* __restrict__ slots, const uint16_t* __restrict__ norm_w,
-                                              float eps, const uint16_t* __restrict__ cos_sin, int32_t max_pos,
-                                              uint8_t* __restrict__ payload, uint8_t* __restrict__ scale,
-                                              int64_t num_pages, int32_t* status) {
-  const int lh = threadIdx.x & 15;
-  const int64_t n = block * kRowsPerBlock + (threadIdx.x >> 4);
-  const bool in_range = n < n_rows;
-  int32_t slot = -1, pos = 0;
-  if (in_range) {
-    slot = __ldg(slots + n);
-    pos = __ldg(positions + n);
-  }
-  bool store = in_range && slot >= 0;
-  if (store && (int64_t)slot >= num_pages * kPage) {
-    if (lh == 0) record_error(status, FP4IDX_ERR_BAD_PAGE);
-    store = false;
-  }
-  if (in_range && (pos < 0 || pos >= max_pos)) {
-    if (lh == 0 && slot >= 0) record_error(status, FP4IDX_ERR_BAD_POSITION);
-    store = false;
-    pos = 0;
-  }
-  float v[8], w[8];
-  if (in_range) unpack_bf16x8(ldg16(k + n * kHeadDim + 8 * lh), v);
-  else {
+struct f2 {
+  float x, y;
+};
+
+__device__ __forceinline__ uint64_t pk(f2 a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ f2 upk(uint64_t r) {
+  f2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+  return upk(d);
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+  return upk(d);
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)));
+  return upk(d);
+}
+// a * b + c with one rounding; with b = (+-1, +-1) it is the correctly rounded c +- a.
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+  return upk(d);
+}
+
+__device__ __forceinline__ void unpack(uint4 u, f2 v[4]) {
+  v[0] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u)};
+  v[1] = {__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)};
+  v[2] = {__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u)};
+  v[3] = {__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u)};
+}
+
+// The lane's 32 elements of the bf16 row at `row`.
+__device__ __forceinline__ void load_raw(const uint16_t* row, int l, uint4 raw[4]) {
 #pragma unroll
-    for (int e = 0; e < 8; e++) v[e] = 0.0f;
+  for (int m = 0; m < 4; m++) raw[m] = __ldg(reinterpret_cast<const uint4*>(row + 32 * m + 8 * l));
+}
+
+// y <- RMSNorm(x) * w.
+__device__ __forceinline__ void rmsnorm(f2 x[4][4], const f2 w[4][4], float eps) {
+  float g[4];  // the sums of the lane's groups 4 m + l, left to right
+#pragma unroll
+  for (int m = 0; m < 4; m++) {
+    const f2 a = mul2(x[m][0], x[m][0]), b = mul2(x[m][1], x[m][1]);
+    const f2 c = mul2(x[m][2], x[m][2]), d = mul2(x[m][3], x[m][3]);
+    float s = __fadd_rn(a.x, a.y);
+    s = __fadd_rn(s, b.x); s = __fadd_rn(s, b.y);
+    s = __fadd_rn(s, c.x); s = __fadd_rn(s, c.y);
+    s = __fadd_rn(s, d.x); s = __fadd_rn(s, d.y);
+    g[m] = s;
   }
-  unpack_bf16x8(ldg16(norm_w + 8 * lh), w);
-  rmsnorm_row(v, w, eps);
-  rope_row(v, cos_sin + (int64_t)pos * kRope, lh);
-  hadamard_row(v, lh);
-  uint32_t sb;
-  const uint32_t word = fp4_encode_lane(v, sb);
-  if (store) {
-    const int64_t page = slot >> 6;
-    const int j = slot & 63;
-    const int c = lh >> 2;
-    uint8_t* dst = payload + ((page * 4 + c) * kPage + j) * 16 + (lh & 3) * 4;
-    *reinterpret_cast<uint32_t*>(dst) = word;
-    if ((lh & 3) == 0) scale[(page * 4 + c) * kPage + j] = (uint8_t)sb;
+  // tree levels 1 and 2 pair groups 4m+l with 4m+(l^1), then with 4m+(l^2): across the quarter
+  f2 p = {g[0], g[1]}, q = {g[2], g[3]};
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    const f2 pp = {__shfl_xor_sync(kFull, p.x, o), __shfl_xor_sync(kFull, p.y, o)};
+    const f2 qq = {__shfl_xor_sync(kFull, q.x, o), __shfl_xor_sync(kFull, q.y, o)};
+    p = add2(p, pp);
+    q = add2(q, qq);
+  }
+  // levels 3 and 4: (m0 + m1) + (m2 + m3), now inside the lane
+  const float s = __fadd_rn(__fadd_rn(p.x, p.y), __fadd_rn(q.x, q.y));
+  const float mean = __fmul_rn(s, 0.0078125f);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+  const f2 rr = {r, r};
+#pragma unroll
+  for (int m = 0; m < 4; m++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) x[m][j] = mul2(mul2(x[m][j], rr), w[m][j]);
+}
+
+// RoPE on dims 0..63: the lane's pairs (32 * 0 + 8 l + e, 32 * 1 + 8 l + e), with cos and
+// sin of index 8 l + e from the bf16 table row.  Scalar operations: a packed product
+// feeding a packed sum may be fused into one rounding by the code generator, which would
+// change the result, so each product and each sum here is its own rounded instruction.
+__device__ __forceinline__ void rope(f2 x[4][4], uint4 cos_raw, uint4 sin_raw) {
+  f2 c[4], s[4];
+  unpack(cos_raw, c);
+  unpack(sin_raw, s);
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    const f2 a = x[0][j], b = x[1][j];
+    x[0][j] = {__fsub_rn(__fmul_rn(a.x, c[j].x), __fmul_rn(b.x, s[j].x)),
+               __fsub_rn(__fmul_rn(a.y, c[j].y), __fmul_rn(b.y, s[j].y))};
+    x[1][j] = {__fadd_rn(__fmul_rn(b.x, c[j].x), __fmul_rn(a.x, s[j].x)),
+               __fadd_rn(__fmul_rn(b.y, c[j].y), __fmul_rn(a.y, s[j].y))};
   }
 }
 
-__global__ void __launch_bounds__(256) store_k_kernel(
-    const uint16_t* __restrict__ k, int64_t n_rows, const int32_t* __restrict__ positions,
-    const int32_t* __restrict__ slots, const uint16_t* __restrict__ norm_w, float eps,
-    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ payload,
-    uint8_t* __restrict__ scale, int64_t num_pages, int32_t* status) {
-  store_k_block(blockIdx.x, k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, payload, scale, num_pages,
-                status);
+__device__ __forceinline__ void hadamard(f2 x[4][4], int l) {
+  // h = 1: inside each pair
+#pragma unroll
+  for (int m = 0; m < 4; m++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float a = x[m][j].x, b = x[m][j].y;
+      x[m][j] = {__fadd_rn(a, b), __fsub_rn(a, b)};
+    }
+  // h = 2, 4: pairs j and j + h/2
+#pragma unroll
+  for (int hj = 1; hj <= 2; hj <<= 1)
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        if (j & hj) continue;
+        const f2 a = x[m][j], b = x[m][j + hj];
+        x[m][j] = add2(a, b);
+        x[m][j + hj] = sub2(a, b);
+      }
+  // h = 8, 16: lanes l and l ^ (h / 8); the lane with the bit set keeps partner - own
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    const float sg = (l & o) ? -1.0f : 1.0f;
+    const f2 sgn = {sg, sg};
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const f2 p = {__shfl_xor_sync(kFull, x[m][j].x, o), __shfl_xor_sync(kFull, x[m][j].y, o)};
+        x[m][j] = fma2(x[m][j], sgn, p);
+      }
+  }
+  // h = 32, 64: chunks m and m + h/32
+#pragma unroll
+  for (int hm = 1; hm <= 2; hm <<= 1)
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+      if (m & hm) continue;
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const f2 a = x[m][j], b = x[m + hm][j];
+        x[m][j] = add2(a, b);
+        x[m + hm][j] = sub2(a, b);
+      }
+    }
+  const float sc = __uint_as_float(kInvSqrt128Bits);
+  const f2 sc2 = {sc, sc};
+#pragma unroll
+  for (int m = 0; m < 4; m++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) x[m][j] = mul2(x[m][j], sc2);
 }
 
-__global__ void __launch_bounds__(256) store_k_fp8_kernel(
-    const uint16_t* __restrict__ k, int64_t n_rows, const int32_t* __restrict__ positions,
-    const int32_t* __restrict__ slots, const uint16_t* __restrict__ norm_w, float eps,
-    const uint16_t* __restrict__ cos_sin, int32_t max_pos, uint8_t* __restrict__ pages, int64_t num_pages,
-    int32_t* status) {
-  const int lh = threadIdx.x & 15;
-  const int64_t n = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4);
-  const bool in_range = n < n_rows;
-  int32_t slot = -1, pos = 0;
-  if (in_range) {
-    slot = __ldg(slots + n);
-    pos = __ldg(positions + n);
-  }
-  bool store = in_range && slot >= 0;
-  if (store && (int64_t)slot >= num_pages * kPage) {
-    if (lh == 0) record_error(status, FP4IDX_ERR_BAD_PAGE);
-    store = false;
-  }
-  if (in_range && (pos < 0 || pos >= max_pos)) {
-    if (lh == 0 && slot >= 0) record_error(status, FP4IDX_ERR_BAD_POSITION);
-    store = false;
-    pos = 0;
-  }
-  float v[8], w[8];
-  if (in_range) unpack_bf16x8(ldg16(k + n * kHeadDim + 8 * lh), v);
-  else {
-#pragma unroll
-    for (int e = 0; e < 8; e++) v[e] = 0.0f;
-  }
-  unpack_bf16x8(ldg16(norm_w + 8 * lh), w);
-  rmsnorm_row(v, w, eps);
-  rope_row(v, cos_sin + (int64_t)pos * kRope, lh);
-  hadamard_row(v, lh);
+// FP4 encoding of block m (elements 32 m .. 32 m + 31, eight of them in each lane of the
+// quarter): this lane's 4 payload bytes and the block's scale byte.
+__device__ __forceinline__ uint32_t fp4_block(const f2 xm[4], uint32_t& scale_byte) {
   float amax = 0.0f;
 #pragma unroll
-  for (int e = 0; e < 8; e++) amax = fmaxf(amax, fabsf(v[e]));
+  for (int j = 0; j < 4; j++) amax = fmaxf(amax, fmaxf(fabsf(xm[j].x), fabsf(xm[j].y)));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+  scale_byte = ue8m0_byte(amax);
+  const float inv = __uint_as_float((254u - scale_byte) << 23);  // 2^-e, exact scaling
+  const f2 inv2 = {inv, inv};
+  uint32_t word = 0;
 #pragma unroll
-  for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-  const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-  uint2 out;
-  out.x = e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) | (e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
-  out.y = e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) | (e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
-  if (store) {
-    const int64_t page = slot >> 6;
-    const int j = slot & 63;
-    uint8_t* base = pages + page * (int64_t)FP4IDX_FP8_PAGE_BYTES;
-    *reinterpret_cast<uint2*>(base + j * kHeadDim + lh * 8) = out;
-    if (lh == 0) *reinterpret_cast<float*>(base + kPage * kHeadDim + j * 4) = s;
+  for (int j = 0; j < 4; j++) {
+    const f2 y = mul2(xm[j], inv2);
+    word |= e2m1x2(y.x, y.y) << (8 * j);
   }
+  return word;
+}
+
+}  // namespace qw
+
+// ------------------------------------------------------------------ K store kernels
+constexpr int kRowsPerBlock = 16;        // half-warp mapping (query packing): 256 threads
+constexpr int kStoreRowsPerBlock = 64;   // quarter-warp mapping (K store): 256 threads
+
+// Checks of one K-store row: the row is written only with a slot in the cache and a
+// position inside the table (a negative slot is padding and skipped silently).  Returns
+// whether to write; `pos` is clamped to 0 for the table read of a rejected row.
+__device__ __forceinline__ bool store_row_ok(bool in_range, int32_t slot, int32_t& pos, int64_t num_pages,
+                                             int32_t max_pos, bool reporter, int32_t* status) {
+  bool store = in_range && slot >= 0;
+  if (store && (int64_t)slot >= num_pages * kPage) {
+    if (reporter) record_error(status, FP4IDX_ERR_BAD_PAGE);
+    store = false;
+  }
+  if (in_range && (pos < 0 || pos >= max_pos)) {
+    if (reporter && slot >= 0) record_error(status, FP4IDX_ERR_BAD_POSITION);
+    store = false;
+  }
+  if (!store) pos = 0;
+  return store;
+}
+
+struct StoreArgs {
+  const uint16_t* k;
+  int64_t n_rows;
+  const int32_t* positions;
+  const int32_t* slots;
+  const uint16_t* norm_w;
+  float eps;
+  const uint16_t* cos_sin;
+  int32_t max_pos;
+  int64_t num_pages;
+  int32_t* status;
+};
+
+// The chain of one K row up to the Hadamard, on the quarter-warp mapping: x holds the
+// lane's 32 values on return.
+__device__ __forceinline__ void k_chain_qw(qw::f2 x[4][4], const uint4 raw[4], const qw::f2 w[4][4], float eps,
+                                           const uint16_t* cs_row, int l) {
+#pragma unroll
+  for (int m = 0; m < 4; m++) qw::unpack(raw[m], x[m]);
+  qw::rmsnorm(x, w, eps);
+  const uint4 c = __ldg(reinterpret_cast<const uint4*>(cs_row + 8 * l));
+  const uint4 s = __ldg(reinterpret_cast<const uint4*>(cs_row + 32 + 8 * l));
+  qw::rope(x, c, s);
+  qw::hadamard(x, l);
+}
+
+__device__ __forceinline__ void load_norm_w(const uint16_t* norm_w, int l, qw::f2 w[4][4]) {
+  uint4 raw[4];
+  qw::load_raw(norm_w, l, raw);
+#pragma unroll
+  for (int m = 0; m < 4; m++) qw::unpack(raw[m], w[m]);
+}
+
+// Rows r = first, first + stride, ... (units of 8 rows a warp): every lane of a warp takes
+// the same number of iterations, as the shuffles need.  The row's raw K, slot and position
+// for the next iteration are loaded before the current row's arithmetic.
+template <bool kFp8>
+__device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_unit, int64_t unit_stride,
+                                             uint8_t* payload, uint8_t* scale, uint8_t* fp8_pages) {
+  const int lane = threadIdx.x & 31, l = lane & 3;
+  const int sub = lane >> 2;
+  const bool reporter = l == 0;
+  qw::f2 w[4][4];
+  load_norm_w(a.norm_w, l, w);
+  const int64_t n_units = (a.n_rows + 7) >> 3;
+  int64_t u = first_unit;
+  if (u >= n_units) return;  // uniform over the warp
+  int64_t n = u * 8 + sub;
+  bool in_range = n < a.n_rows;
+  uint4 raw[4] = {};
+  int32_t slot = -1, pos = 0;
+  if (in_range) {
+    slot = __ldg(a.slots + n);
+    pos = __ldg(a.positions + n);
+    qw::load_raw(a.k + n * kHeadDim, l, raw);
+  }
+  for (;;) {
+    const bool store = store_row_ok(in_range, slot, pos, a.num_pages, a.max_pos, reporter, a.status);
+    const int32_t cur_slot = slot;
+    const int32_t cur_pos = pos;
+    uint4 cur[4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) cur[m] = raw[m];
+    // next row's loads
+    const int64_t un = u + unit_stride;
+    const bool more = un < n_units;
+    const int64_t nn = un * 8 + sub;
+    const bool next_in = more && nn < a.n_rows;
+    if (next_in) {
+      slot = __ldg(a.slots + nn);
+      pos = __ldg(a.positions + nn);
+      qw::load_raw(a.k + nn * kHeadDim, l, raw);
+    } else {
+      slot = -1;
+      pos = 0;
+    }
+    qw::f2 x[4][4];
+    k_chain_qw(x, cur, w, a.eps, a.cos_sin + (int64_t)cur_pos * kRope, l);
+    const int64_t page = cur_slot >> 6;
+    const int j = cur_slot & 63;
+    if constexpr (!kFp8) {
+      uint32_t sb[4], word[4];
+#pragma unroll
+      for (int m = 0; m < 4; m++) word[m] = qw::fp4_block(x[m], sb[m]);
+      if (store) {
+#pragma unroll
+        for (int m = 0; m < 4; m++)
+          *reinterpret_cast<uint32_t*>(payload + ((page * 4 + m) * kPage + j) * 16 + 4 * l) = word[m];
+        const uint32_t mine = l == 0 ? sb[0] : l == 1 ? sb[1] : l == 2 ? sb[2] : sb[3];
+        scale[(page * 4 + l) * kPage + j] = (uint8_t)mine;
+      }
+    } else {
+      float amax = 0.0f;
+#pragma unroll
+      for (int m = 0; m < 4; m++)
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) amax = fmaxf(amax, fmaxf(fabsf(x[m][jj].x), fabsf(x[m][jj].y)));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      uint8_t* base = fp8_pages + page * (int64_t)FP4IDX_FP8_PAGE_BYTES;
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        uint2 out;
+        out.x = e4m3x2(__fdiv_rn(x[m][0].x, s), __fdiv_rn(x[m][0].y, s)) |
+                (e4m3x2(__fdiv_rn(x[m][1].x, s), __fdiv_rn(x[m][1].y, s)) << 16);
+        out.y = e4m3x2(__fdiv_rn(x[m][2].x, s), __fdiv_rn(x[m][2].y, s)) |
+                (e4m3x2(__fdiv_rn(x[m][3].x, s), __fdiv_rn(x[m][3].y, s)) << 16);
+        if (store) *reinterpret_cast<uint2*>(base + j * kHeadDim + 32 * m + 8 * l) = out;
+      }
+      if (store && l == 0) *reinterpret_cast<float*>(base + kPage * kHeadDim + j * 4) = s;
+    }
+    if (!more) break;
+    u = un;
+    in_range = next_in;
+  }
+}
+
+__global__ void __launch_bounds__(256) store_k_kernel(const StoreArgs a, uint8_t* __restrict__ payload,
+                                                      uint8_t* __restrict__ scale) {
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  store_k_rows<false>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, payload, scale, nullptr);
+}
+
+__global__ void __launch_bounds__(256) store_k_fp8_kernel(const StoreArgs a, uint8_t* __restrict__ pages) {
+  const int64_t warps = (int64_t)gridDim.x * 8;
+  store_k_rows<true>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, nullptr, nullptr, pages);
 }
 
 // Q quant of the 16 (row, head) vectors of block `block`.
@@ -332,7 +556,7 @@ struct PrepareParams {
   int32_t num_ctas;
   void* schedule;
   int32_t* status;
-  int64_t kb;  // blocks of the K store
+  int64_t kb;  // blocks of the K store (64 rows each)
 };
 
 __global__ void __launch_bounds__(256) prepare_step_kernel(const PrepareParams p) {
@@ -340,8 +564,10 @@ __global__ void __launch_bounds__(256) prepare_step_kernel(const PrepareParams p
   if (blockIdx.x == 0) {
     build_schedule_block<256>(p.context_lens, p.row_seq, (int32_t)p.n_rows, p.num_ctas, p.schedule);
   } else if ((int64_t)blockIdx.x <= p.kb) {
-    store_k_block(blockIdx.x - 1, p.k, p.n_new, p.positions, p.slots, p.norm_w, p.eps, p.cos_sin, p.max_pos,
-                  p.payload, p.scale, p.num_pages, p.status);
+    const StoreArgs a{p.k, p.n_new, p.positions, p.slots, p.norm_w, p.eps, p.cos_sin, p.max_pos, p.num_pages,
+                      p.status};
+    store_k_rows<false>(a, ((int64_t)blockIdx.x - 1) * 8 + (threadIdx.x >> 5), p.kb * 8, p.payload, p.scale,
+                        nullptr);
   } else {
     quant_q_block(blockIdx.x - 1 - p.kb, p.q, p.n_rows, p.q_positions, p.cos_sin, p.max_pos, p.q_payload,
                   p.q_scale, p.status);
@@ -486,6 +712,16 @@ std::atomic<bool> g_carve_store[64], g_carve_store_fp8[64], g_carve_quant[64], g
 
 }  // namespace
 
+// The K stores run one pass over the rows with at most as many CTAs as fit on the GPU at
+// once (each warp then loops over its share, loading its next row ahead of the arithmetic).
+template <class Kern>
+unsigned store_grid(Kern kernel, int64_t n_rows, cudaError_t* err) {
+  const int64_t need = (n_rows + kStoreRowsPerBlock - 1) / kStoreRowsPerBlock;
+  int fit = 0;
+  *err = resident_ctas(reinterpret_cast<const void*>(kernel), 256, 0, &fit);
+  return (unsigned)std::max<int64_t>(1, std::min<int64_t>(need, fit));
+}
+
 cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* positions, const int32_t* slots,
                            const uint16_t* norm_w, float eps, const uint16_t* cos_sin, int32_t max_pos,
                            uint8_t* payload, uint8_t* scale, int64_t num_pages, int32_t* status,
@@ -493,8 +729,10 @@ cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* pos
   if (n_rows == 0) return cudaSuccess;
   cudaError_t e = prefer_max_shared(store_k_kernel, g_carve_store);
   if (e != cudaSuccess) return e;
-  store_k_kernel<<<grid_for(n_rows), 256, 0, stream>>>(k, n_rows, positions, slots, norm_w, eps, cos_sin,
-                                                        max_pos, payload, scale, num_pages, status);
+  const unsigned grid = store_grid(store_k_kernel, n_rows, &e);
+  if (e != cudaSuccess) return e;
+  const StoreArgs a{k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, num_pages, status};
+  store_k_kernel<<<grid, 256, 0, stream>>>(a, payload, scale);
   return cudaGetLastError();
 }
 
@@ -504,8 +742,10 @@ cudaError_t launch_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t*
   if (n_rows == 0) return cudaSuccess;
   cudaError_t e = prefer_max_shared(store_k_fp8_kernel, g_carve_store_fp8);
   if (e != cudaSuccess) return e;
-  store_k_fp8_kernel<<<grid_for(n_rows), 256, 0, stream>>>(k, n_rows, positions, slots, norm_w, eps, cos_sin,
-                                                            max_pos, pages, num_pages, status);
+  const unsigned grid = store_grid(store_k_fp8_kernel, n_rows, &e);
+  if (e != cudaSuccess) return e;
+  const StoreArgs a{k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, num_pages, status};
+  store_k_fp8_kernel<<<grid, 256, 0, stream>>>(a, pages);
   return cudaGetLastError();
 }
 
@@ -551,7 +791,7 @@ cudaError_t launch_prepare_step(const uint16_t* k, int64_t n_new, const int32_t*
   p.num_ctas = num_ctas;
   p.schedule = schedule;
   p.status = status;
-  p.kb = (n_new + kRowsPerBlock - 1) / kRowsPerBlock;
+  p.kb = (n_new + kStoreRowsPerBlock - 1) / kStoreRowsPerBlock;
   const int64_t qb = (n_rows * kHeads + kRowsPerBlock - 1) / kRowsPerBlock;
   prepare_step_kernel<<<(unsigned)(1 + p.kb + qb), 256, 0, stream>>>(p);
   return cudaGetLastError();

@@ -52,3 +52,24 @@ def test_single_process_aggregate_is_identity():
     import bench
     value, slowest = bench.aggregate(64, 0.02)
     assert slowest == 0.02 and abs(value - 3200.0) < 1e-9
+
+
+def test_stored_traffic_files_are_consistent():
+    """Each stored ncu traffic figure is read + write, and is reported only for the kernel
+    sources it was captured on."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(bench.TRAFFIC_FILE) as f:
+        tr = json.load(f)
+    for w, e in tr["workloads"].items():
+        assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"], w
+        got = bench.stored_traffic(w)
+        assert got is None or got == e["dram_bytes_per_launch"]
+        assert (got is None) == (tr["kernel_source_hash"] != bench.kernel_source_hash())
+    assert bench.stored_traffic("no such workload") is None
+    with open(bench.KSTORE_TRAFFIC_FILE) as f:
+        ks = json.load(f)
+    assert ks["dram_bytes_per_launch"] == ks["dram_bytes_read"] + ks["dram_bytes_write"]
+    got = bench.stored_kstore_traffic()
+    assert (got is None) == (ks["kernel_source_hash"] != bench.source_hash(bench.KSTORE_DEPS))

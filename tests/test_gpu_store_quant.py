@@ -47,7 +47,10 @@ def test_store_k_full_kstore_workload(fx):
     _assert_cache_equal(got_p, got_s, ref_p, ref_s)
 
 
-@pytest.mark.parametrize("n,pages,pad", [(1, 1, 0), (15, 1, 0), (17, 2, 3), (1000, 20, 7), (4097, 70, 0)])
+# 40,003 rows: more rows than one pass of the resident CTAs covers, so warps loop, and
+# the last pass ends in a partial warp
+@pytest.mark.parametrize("n,pages,pad", [(1, 1, 0), (15, 1, 0), (17, 2, 3), (1000, 20, 7), (4097, 70, 0),
+                                         (40003, 700, 11)])
 def test_store_k_small_ragged(fx, n, pages, pad):
     fp4idx, cs, cs_dev = fx
     ks = wl.small_kstore(100 + n, n, pages, pad_every=pad)
@@ -96,15 +99,18 @@ def test_store_k_reports_bad_slot_and_position(fx):
     assert fp4idx.read_status(status) == 7
 
 
-def test_store_k_fp8_full_kstore_workload(fx):
+@pytest.mark.parametrize("n,pages,pad", [(17, 2, 3), (40003, 700, 11), (65536, 2048, 0)],
+                         ids=["17", "40003", "kstore_65536"])
+def test_store_k_fp8_against_oracle(fx, n, pages, pad):
     fp4idx, cs, cs_dev = fx
     from tests.gpu_util import kstore_to_device
-    ks = wl.kstore_65536()
+    ks = wl.kstore_65536() if n == 65536 else wl.small_kstore(300 + n, n, max(pages, 1), pad_every=pad)
     d = kstore_to_device(ks)
     pages = torch.zeros((ks.num_pages, fp4idx.FP8_PAGE_BYTES), dtype=torch.uint8, device="cuda")
     fp4idx.store_k_fp8(d["k"], d["positions"], d["slots"], d["norm_w"], ks.eps, cs_dev, pages)
     ref, st = oracle.store_k_fp8(ks, cs)
     assert st == 0
+    torch.cuda.synchronize()
     got = pages.cpu().numpy()
     if not np.array_equal(got, ref):
         bad = np.argwhere(got != ref)
