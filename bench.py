@@ -461,7 +461,7 @@ def time_step(st, steps, warmup, flush_l2, device, live_n=500, alone_n=200):
             e1.record()
             per_times[name].append((e0, e1))
     torch.cuda.synchronize()
-    per = {n: statistics.median([a.elapsed_time(b) for a, b in v]) * 1e3 for n, v in per_times.items()}
+    per = {n: statistics.mean([a.elapsed_time(b) for a, b in v]) * 1e3 for n, v in per_times.items()}
     main = names[0]  # the logits launch (with the selection, for fp4idx_logits_topk_fused)
     if marks:
         logits_us = statistics.mean(live[main])
@@ -700,7 +700,7 @@ def cpu_baseline(b, seconds):
     step = OracleStep(b)
     rows_per = 8
     done, secs, i = 0, 0.0, 0
-    while secs < seconds and done < b.n_rows * 4:
+    while secs < seconds and done < max(b.n_rows * 4, 64):
         rows = np.arange(i, i + rows_per) % b.n_rows
         secs += step.run(rows)
         done += rows_per
@@ -778,24 +778,29 @@ def measure_kstore(args, device):
         for _ in range(max(3, args.warmup)):
             fn()
         torch.cuda.synchronize()
+        # event-record nodes inside the graph, around the launch: the interval holds the
+        # kernel, not the graph's own launch
+        e0 = torch.cuda.Event(enable_timing=True, external=True)
+        e1 = torch.cuda.Event(enable_timing=True, external=True)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
+            e0.record()
             fn()
+            e1.record()
         ts = []
         for _ in range(n_timed):
             flush.zero_()
             torch.cuda._sleep(SPIN_CYCLES)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
             g.replay()
-            e1.record()
-            torch.cuda.synchronize()
+            e1.synchronize()
             ts.append(e0.elapsed_time(e1) * 1e3)
-        us = statistics.median(ts)
+        # the mean: event timestamps are coarse (steps of about 1 us were seen on GB300), so
+        # a median snaps to a step while the mean of many launches does not
+        us = statistics.mean(ts)
         out_b = 68 if name == "fp4" else 132
         nbytes = len(ks.positions) * (256 + 128 + 8 + out_b)  # row + cos/sin + position/slot + written entry
-        res[name] = {"us": round(us, 2), "rows_per_s": round(len(ks.positions) / (us * 1e-6), 1),
+        res[name] = {"us": round(us, 2), "us_median": round(statistics.median(ts), 2),
+                     "rows_per_s": round(len(ks.positions) / (us * 1e-6), 1),
                      "algorithmic_bytes": nbytes, "algorithmic_gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
                      "bytes_per_token": out_b}
     clocks = sampler.stop()
@@ -815,14 +820,14 @@ def measure_kstore(args, device):
             secs += time.perf_counter() - t0
             done += len(sub.positions)
         cpu = {"value": round(done / secs, 1), "unit": "rows/s", "cores": oracle.max_threads(), "kind": "oracle",
-               "sample": "%d rows of the same workload in slices of %d; %.1f s" % (done, n, secs)}
+               "sample": "%d rows of the same workload in slices of %d; %.3f s" % (done, n, secs)}
     peak, peak_kind = measured_peaks()
     fp4 = res["fp4"]
     roofline = {"bound": "hbm", "achieved": fp4["algorithmic_gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(fp4["algorithmic_gbs"] / peak, 4), "traffic": stored_kstore_traffic(),
                 "kernel": "store_k_kernel", "algorithmic_bytes": fp4["algorithmic_bytes"], "avg_launch_us": fp4["us"],
-                "launch_timing": "the launch captured alone in a graph, median of %d replays (L2 flushed before each)"
-                                 % n_timed,
+                "launch_timing": "event-record nodes around the launch inside its graph, mean of %d replays (L2 "
+                                 "flushed before each)" % n_timed,
                 "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}
     return {"workload": "kstore_65536", "rows": len(ks.positions), "cache_pages": ks.num_pages,
             "value": fp4["rows_per_s"], "unit": "rows/s", "steps": n_timed, "ms_per_step": round(fp4["us"] / 1e3, 5),

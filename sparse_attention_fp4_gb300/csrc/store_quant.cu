@@ -21,8 +21,9 @@
 //     multiply by fp32(1/sqrt(128)).
 //   * UE8M0 per 32-element block: smallest e with 6*2^e >= amax, from the
 //     exponent/mantissa bits of amax; e2m1 by the hardware RNE-satfinite convert,
-//     the sign of zero taken from the input.
+//     which keeps the sign of a value that rounds to zero.
 #include "launchers.cuh"
+#include "ptx.cuh"
 #include "schedule_build.cuh"
 
 #include <algorithm>
@@ -99,27 +100,28 @@ __device__ __forceinline__ uint32_t ue8m0_byte(float amax) {
   return (uint32_t)byte;
 }
 
-// Two fp32 -> one byte of e2m1 (lo nibble = first), RNE, satfinite, sign of zero kept.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+// The converts below round to nearest even, saturate to the largest finite value, and
+// keep the sign of an input that rounds to zero (e2m1 code 8, e4m3 byte 0x80), which is
+// the encoding's rule for negative values too small for the grid.
+// Eight fp32 -> one word of e2m1 (nibble i = value i).
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4, float v5, float v6,
+                                           float v7) {
   uint32_t out;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
-      "cvt.u32.u8 %0, t;\n\t}"
-      : "=r"(out) : "f"(lo), "f"(hi));
-  out &= 0x77u;
-  out |= (__float_as_uint(lo) >> 31) << 3;
-  out |= (__float_as_uint(hi) >> 31) << 7;
+  asm("{\n\t.reg .b8 a, b, c, d;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 a, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 d, %8, %7;\n\t"
+      "mov.b32 %0, {a, b, c, d};\n\t}"
+      : "=r"(out) : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
   return out;
 }
 
-// Two fp32 -> two bytes of e4m3 (byte 0 = first), RNE, satfinite, sign of zero kept.
+// Two fp32 -> two bytes of e4m3 (byte 0 = first).
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t t;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(t) : "f"(lo), "f"(hi));
-  uint32_t out = (uint32_t)t & 0x7F7Fu;
-  out |= (__float_as_uint(lo) >> 31) << 7;
-  out |= (__float_as_uint(hi) >> 31) << 15;
-  return out;
+  return (uint32_t)t;
 }
 
 // Quantise the half-warp's row (after the Hadamard) and return this lane's 4 payload
@@ -132,11 +134,10 @@ __device__ __forceinline__ uint32_t fp4_encode_lane(const float v[8], uint32_t& 
   amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
   scale_byte = ue8m0_byte(amax);
   const float inv = __uint_as_float((254u - scale_byte) << 23);  // 2^(127 - byte) = 2^-e
-  uint32_t word = 0;
+  float y[8];
 #pragma unroll
-  for (int e = 0; e < 8; e += 2)
-    word |= e2m1x2(__fmul_rn(v[e], inv), __fmul_rn(v[e + 1], inv)) << (4 * e);
-  return word;
+  for (int e = 0; e < 8; e++) y[e] = __fmul_rn(v[e], inv);
+  return e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
 }
 
 // ------------------------------------------------------------------ quarter-warp row transform
@@ -198,14 +199,8 @@ __device__ __forceinline__ void unpack(uint4 u, f2 v[4]) {
   v[3] = {__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u)};
 }
 
-// The lane's 32 elements of the bf16 row at `row`.
-__device__ __forceinline__ void load_raw(const uint16_t* row, int l, uint4 raw[4]) {
-#pragma unroll
-  for (int m = 0; m < 4; m++) raw[m] = __ldg(reinterpret_cast<const uint4*>(row + 32 * m + 8 * l));
-}
-
-// y <- RMSNorm(x) * w.
-__device__ __forceinline__ void rmsnorm(f2 x[4][4], const f2 w[4][4], float eps) {
+// y <- RMSNorm(x) * w, with w (fp32) read from shared memory at wl = w + 8 l.
+__device__ __forceinline__ void rmsnorm(f2 x[4][4], const float* wl, float eps) {
   float g[4];  // the sums of the lane's groups 4 m + l, left to right
 #pragma unroll
   for (int m = 0; m < 4; m++) {
@@ -234,7 +229,10 @@ __device__ __forceinline__ void rmsnorm(f2 x[4][4], const f2 w[4][4], float eps)
 #pragma unroll
   for (int m = 0; m < 4; m++)
 #pragma unroll
-    for (int j = 0; j < 4; j++) x[m][j] = mul2(mul2(x[m][j], rr), w[m][j]);
+    for (int j = 0; j < 4; j++) {
+      const float2 wv = *reinterpret_cast<const float2*>(wl + 32 * m + 2 * j);
+      x[m][j] = mul2(mul2(x[m][j], rr), f2{wv.x, wv.y});
+    }
 }
 
 // RoPE on dims 0..63: the lane's pairs (32 * 0 + 8 l + e, 32 * 1 + 8 l + e), with cos and
@@ -321,13 +319,10 @@ __device__ __forceinline__ uint32_t fp4_block(const f2 xm[4], uint32_t& scale_by
   scale_byte = ue8m0_byte(amax);
   const float inv = __uint_as_float((254u - scale_byte) << 23);  // 2^-e, exact scaling
   const f2 inv2 = {inv, inv};
-  uint32_t word = 0;
+  f2 y[4];
 #pragma unroll
-  for (int j = 0; j < 4; j++) {
-    const f2 y = mul2(xm[j], inv2);
-    word |= e2m1x2(y.x, y.y) << (8 * j);
-  }
-  return word;
+  for (int j = 0; j < 4; j++) y[j] = mul2(xm[j], inv2);
+  return e2m1x8(y[0].x, y[0].y, y[1].x, y[1].y, y[2].x, y[2].y, y[3].x, y[3].y);
 }
 
 }  // namespace qw
@@ -368,77 +363,118 @@ struct StoreArgs {
 };
 
 // The chain of one K row up to the Hadamard, on the quarter-warp mapping: x holds the
-// lane's 32 values on return.
-__device__ __forceinline__ void k_chain_qw(qw::f2 x[4][4], const uint4 raw[4], const qw::f2 w[4][4], float eps,
-                                           const uint16_t* cs_row, int l) {
+// lane's 32 values on return.  cs holds the lane's 8 cos and 8 sin of the row's position.
+__device__ __forceinline__ void k_chain_qw(qw::f2 x[4][4], const uint4 raw[4], const float* wl, float eps,
+                                           const uint4 cs[2], int l) {
 #pragma unroll
   for (int m = 0; m < 4; m++) qw::unpack(raw[m], x[m]);
-  qw::rmsnorm(x, w, eps);
-  const uint4 c = __ldg(reinterpret_cast<const uint4*>(cs_row + 8 * l));
-  const uint4 s = __ldg(reinterpret_cast<const uint4*>(cs_row + 32 + 8 * l));
-  qw::rope(x, c, s);
+  qw::rmsnorm(x, wl, eps);
+  qw::rope(x, cs[0], cs[1]);
   qw::hadamard(x, l);
 }
 
-__device__ __forceinline__ void load_norm_w(const uint16_t* norm_w, int l, qw::f2 w[4][4]) {
-  uint4 raw[4];
-  qw::load_raw(norm_w, l, raw);
-#pragma unroll
-  for (int m = 0; m < 4; m++) qw::unpack(raw[m], w[m]);
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Rows r = first, first + stride, ... (units of 8 rows a warp): every lane of a warp takes
-// the same number of iterations, as the shuffles need.  The row's raw K, slot and position
-// for the next iteration are loaded before the current row's arithmetic.
-template <bool kFp8>
+// Shared memory of a K-store CTA (256 threads): the norm weight in fp32, and a ring of
+// kDepth rows per thread -- its six 16-byte chunks (four of K, one of cos, one of sin),
+// chunk-major so that a warp's accesses hit consecutive banks.
+template <int kDepth>
+struct StoreSmem {
+  static constexpr size_t kW = 0, kRing = 512;
+  static constexpr size_t kBytes = kRing + 16 * 6 * 256 * kDepth;
+};
+
+// Rows u * 8 + (lane / 4) for units u = first, first + stride, ...: every lane of a warp
+// takes the same number of iterations, as the shuffles need.  Each lane copies its own
+// chunks of the next kDepth rows into its ring with cp.async while it computes the
+// current row; slot and position are read one row further ahead, so that the cos/sin
+// copy can be issued at once.  With three CTAs an SM and kDepth = 2, a 65,536-row store
+// has nearly every row in flight from the start: in-kernel timing put the launch at
+// ~12.5 us against ~17 us for loads one row ahead in registers, and ~7.4 us for the loads
+// alone.  All threads of the CTA must call this (one barrier).
+template <bool kFp8, int kDepth>
 __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_unit, int64_t unit_stride,
-                                             uint8_t* payload, uint8_t* scale, uint8_t* fp8_pages) {
-  const int lane = threadIdx.x & 31, l = lane & 3;
+                                             uint8_t* smem, uint8_t* payload, uint8_t* scale, uint8_t* fp8_pages) {
+  using L = StoreSmem<kDepth>;
+  float* w_s = reinterpret_cast<float*>(smem + L::kW);
+  const uint32_t ring = ptx::smem_addr(smem + L::kRing);
+  for (int i = threadIdx.x; i < kHeadDim; i += blockDim.x) w_s[i] = __uint_as_float((uint32_t)a.norm_w[i] << 16);
+  __syncthreads();
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, l = lane & 3;
   const int sub = lane >> 2;
   const bool reporter = l == 0;
-  qw::f2 w[4][4];
-  load_norm_w(a.norm_w, l, w);
   const int64_t n_units = (a.n_rows + 7) >> 3;
-  int64_t u = first_unit;
-  if (u >= n_units) return;  // uniform over the warp
-  int64_t n = u * 8 + sub;
-  bool in_range = n < a.n_rows;
-  uint4 raw[4] = {};
-  int32_t slot = -1, pos = 0;
-  if (in_range) {
-    slot = __ldg(a.slots + n);
-    pos = __ldg(a.positions + n);
-    qw::load_raw(a.k + n * kHeadDim, l, raw);
-  }
-  for (;;) {
-    const bool store = store_row_ok(in_range, slot, pos, a.num_pages, a.max_pos, reporter, a.status);
-    const int32_t cur_slot = slot;
-    const int32_t cur_pos = pos;
-    uint4 cur[4];
-#pragma unroll
-    for (int m = 0; m < 4; m++) cur[m] = raw[m];
-    // next row's loads
-    const int64_t un = u + unit_stride;
-    const bool more = un < n_units;
-    const int64_t nn = un * 8 + sub;
-    const bool next_in = more && nn < a.n_rows;
-    if (next_in) {
-      slot = __ldg(a.slots + nn);
-      pos = __ldg(a.positions + nn);
-      qw::load_raw(a.k + nn * kHeadDim, l, raw);
-    } else {
-      slot = -1;
-      pos = 0;
+  if (first_unit >= n_units) return;  // uniform over the warp
+  const float* wl = w_s + 8 * l;
+  auto chunk = [&](int d, int c) { return ring + (uint32_t)(((d * 6 + c) * 256 + tid) * 16); };
+  // slot and position of the row of unit u (none past the end)
+  auto head = [&](int64_t u, int32_t& slot, int32_t& pos) {
+    const int64_t n = u * 8 + sub;
+    slot = -1;
+    pos = 0;
+    if (u < n_units && n < a.n_rows) {
+      slot = __ldg(a.slots + n);
+      pos = __ldg(a.positions + n);
     }
+  };
+  // checks of the row of unit u and its chunk copies (one group); returns the slot to
+  // write, -1 for none
+  auto issue = [&](int d, int64_t u, int32_t slot, int32_t pos) -> int32_t {
+    const int64_t n = u * 8 + sub;
+    const bool in_range = u < n_units && n < a.n_rows;
+    const bool store = store_row_ok(in_range, slot, pos, a.num_pages, a.max_pos, reporter, a.status);
+    if (in_range) {
+      const uint16_t* src = a.k + n * kHeadDim + 8 * l;
+#pragma unroll
+      for (int m = 0; m < 4; m++) cp_async16(chunk(d, m), src + 32 * m);
+      const uint16_t* cs = a.cos_sin + (int64_t)pos * kRope + 8 * l;
+      cp_async16(chunk(d, 4), cs);
+      cp_async16(chunk(d, 5), cs + 32);
+    }
+    cp_async_commit();
+    return store ? slot : -1;
+  };
+  // the slots of the rows in the ring, oldest first (rotated each iteration)
+  int32_t ws[kDepth];
+  {
+    int32_t hs[kDepth], hp[kDepth];
+#pragma unroll
+    for (int d = 0; d < kDepth; d++) head(first_unit + d * unit_stride, hs[d], hp[d]);
+#pragma unroll
+    for (int d = 0; d < kDepth; d++) ws[d] = issue(d, first_unit + d * unit_stride, hs[d], hp[d]);
+  }
+  int32_t nslot, npos;
+  head(first_unit + kDepth * unit_stride, nslot, npos);
+  int d = 0;
+  for (int64_t u = first_unit; u < n_units; u += unit_stride) {
+    cp_async_wait<kDepth - 1>();
+    uint4 raw[4], cs[2];
+#pragma unroll
+    for (int m = 0; m < 4; m++) asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(raw[m].x), "=r"(raw[m].y), "=r"(raw[m].z), "=r"(raw[m].w)
+                                             : "r"(chunk(d, m)));
+#pragma unroll
+    for (int c = 0; c < 2; c++) asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                             : "=r"(cs[c].x), "=r"(cs[c].y), "=r"(cs[c].z), "=r"(cs[c].w)
+                                             : "r"(chunk(d, 4 + c)));
+    const int32_t slot = ws[0];
     qw::f2 x[4][4];
-    k_chain_qw(x, cur, w, a.eps, a.cos_sin + (int64_t)cur_pos * kRope, l);
-    const int64_t page = cur_slot >> 6;
-    const int j = cur_slot & 63;
+    k_chain_qw(x, raw, wl, a.eps, cs, l);
+    const int64_t page = slot >> 6;
+    const int j = slot & 63;
     if constexpr (!kFp8) {
       uint32_t sb[4], word[4];
 #pragma unroll
       for (int m = 0; m < 4; m++) word[m] = qw::fp4_block(x[m], sb[m]);
-      if (store) {
+      if (slot >= 0) {
 #pragma unroll
         for (int m = 0; m < 4; m++)
           *reinterpret_cast<uint32_t*>(payload + ((page * 4 + m) * kPage + j) * 16 + 4 * l) = word[m];
@@ -453,34 +489,45 @@ __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_u
         for (int jj = 0; jj < 4; jj++) amax = fmaxf(amax, fmaxf(fabsf(x[m][jj].x), fabsf(x[m][jj].y)));
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-      const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
       uint8_t* base = fp8_pages + page * (int64_t)FP4IDX_FP8_PAGE_BYTES;
 #pragma unroll
       for (int m = 0; m < 4; m++) {
         uint2 out;
-        out.x = e4m3x2(__fdiv_rn(x[m][0].x, s), __fdiv_rn(x[m][0].y, s)) |
-                (e4m3x2(__fdiv_rn(x[m][1].x, s), __fdiv_rn(x[m][1].y, s)) << 16);
-        out.y = e4m3x2(__fdiv_rn(x[m][2].x, s), __fdiv_rn(x[m][2].y, s)) |
-                (e4m3x2(__fdiv_rn(x[m][3].x, s), __fdiv_rn(x[m][3].y, s)) << 16);
-        if (store) *reinterpret_cast<uint2*>(base + j * kHeadDim + 32 * m + 8 * l) = out;
+        out.x = e4m3x2(__fdiv_rn(x[m][0].x, sc), __fdiv_rn(x[m][0].y, sc)) |
+                (e4m3x2(__fdiv_rn(x[m][1].x, sc), __fdiv_rn(x[m][1].y, sc)) << 16);
+        out.y = e4m3x2(__fdiv_rn(x[m][2].x, sc), __fdiv_rn(x[m][2].y, sc)) |
+                (e4m3x2(__fdiv_rn(x[m][3].x, sc), __fdiv_rn(x[m][3].y, sc)) << 16);
+        if (slot >= 0) *reinterpret_cast<uint2*>(base + j * kHeadDim + 32 * m + 8 * l) = out;
       }
-      if (store && l == 0) *reinterpret_cast<float*>(base + kPage * kHeadDim + j * 4) = s;
+      if (slot >= 0 && l == 0) *reinterpret_cast<float*>(base + kPage * kHeadDim + j * 4) = sc;
     }
-    if (!more) break;
-    u = un;
-    in_range = next_in;
+    // refill this ring entry with the row kDepth units on; read the next head
+#pragma unroll
+    for (int i = 0; i + 1 < kDepth; i++) ws[i] = ws[i + 1];
+    ws[kDepth - 1] = issue(d, u + kDepth * unit_stride, nslot, npos);
+    head(u + (kDepth + 1) * unit_stride, nslot, npos);
+    d = d + 1 == kDepth ? 0 : d + 1;
   }
+  cp_async_wait<0>();
 }
 
-__global__ void __launch_bounds__(256) store_k_kernel(const StoreArgs a, uint8_t* __restrict__ payload,
+constexpr int kStoreDepth = 2;         // rows in flight per thread in the K-store kernels
+constexpr int kPrepareStoreDepth = 1; // one row per thread in the step preparation
+
+__global__ void __launch_bounds__(256, 3) store_k_kernel(const StoreArgs a, uint8_t* __restrict__ payload,
                                                       uint8_t* __restrict__ scale) {
+  extern __shared__ __align__(16) uint8_t store_smem[];
   const int64_t warps = (int64_t)gridDim.x * 8;
-  store_k_rows<false>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, payload, scale, nullptr);
+  store_k_rows<false, kStoreDepth>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, store_smem, payload, scale,
+                                   nullptr);
 }
 
-__global__ void __launch_bounds__(256) store_k_fp8_kernel(const StoreArgs a, uint8_t* __restrict__ pages) {
+__global__ void __launch_bounds__(256, 3) store_k_fp8_kernel(const StoreArgs a, uint8_t* __restrict__ pages) {
+  extern __shared__ __align__(16) uint8_t store_smem[];
   const int64_t warps = (int64_t)gridDim.x * 8;
-  store_k_rows<true>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, nullptr, nullptr, pages);
+  store_k_rows<true, kStoreDepth>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, store_smem, nullptr,
+                                  nullptr, pages);
 }
 
 // Q quant of the 16 (row, head) vectors of block `block`.
@@ -560,14 +607,15 @@ struct PrepareParams {
 };
 
 __global__ void __launch_bounds__(256) prepare_step_kernel(const PrepareParams p) {
+  extern __shared__ __align__(16) uint8_t prep_smem[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x == 0) {
     build_schedule_block<256>(p.context_lens, p.row_seq, (int32_t)p.n_rows, p.num_ctas, p.schedule);
   } else if ((int64_t)blockIdx.x <= p.kb) {
     const StoreArgs a{p.k, p.n_new, p.positions, p.slots, p.norm_w, p.eps, p.cos_sin, p.max_pos, p.num_pages,
                       p.status};
-    store_k_rows<false>(a, ((int64_t)blockIdx.x - 1) * 8 + (threadIdx.x >> 5), p.kb * 8, p.payload, p.scale,
-                        nullptr);
+    store_k_rows<false, kPrepareStoreDepth>(a, ((int64_t)blockIdx.x - 1) * 8 + (threadIdx.x >> 5), p.kb * 8,
+                                            prep_smem, p.payload, p.scale, nullptr);
   } else {
     quant_q_block(blockIdx.x - 1 - p.kb, p.q, p.n_rows, p.q_positions, p.cos_sin, p.max_pos, p.q_payload,
                   p.q_scale, p.status);
@@ -718,7 +766,9 @@ template <class Kern>
 unsigned store_grid(Kern kernel, int64_t n_rows, cudaError_t* err) {
   const int64_t need = (n_rows + kStoreRowsPerBlock - 1) / kStoreRowsPerBlock;
   int fit = 0;
-  *err = resident_ctas(reinterpret_cast<const void*>(kernel), 256, 0, &fit);
+  *err = set_smem_attr_once(reinterpret_cast<const void*>(kernel), StoreSmem<kStoreDepth>::kBytes);
+  if (*err == cudaSuccess)
+    *err = resident_ctas(reinterpret_cast<const void*>(kernel), 256, StoreSmem<kStoreDepth>::kBytes, &fit);
   return (unsigned)std::max<int64_t>(1, std::min<int64_t>(need, fit));
 }
 
@@ -732,7 +782,7 @@ cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* pos
   const unsigned grid = store_grid(store_k_kernel, n_rows, &e);
   if (e != cudaSuccess) return e;
   const StoreArgs a{k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, num_pages, status};
-  store_k_kernel<<<grid, 256, 0, stream>>>(a, payload, scale);
+  store_k_kernel<<<grid, 256, StoreSmem<kStoreDepth>::kBytes, stream>>>(a, payload, scale);
   return cudaGetLastError();
 }
 
@@ -745,7 +795,7 @@ cudaError_t launch_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t*
   const unsigned grid = store_grid(store_k_fp8_kernel, n_rows, &e);
   if (e != cudaSuccess) return e;
   const StoreArgs a{k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, num_pages, status};
-  store_k_fp8_kernel<<<grid, 256, 0, stream>>>(a, pages);
+  store_k_fp8_kernel<<<grid, 256, StoreSmem<kStoreDepth>::kBytes, stream>>>(a, pages);
   return cudaGetLastError();
 }
 
@@ -793,7 +843,7 @@ cudaError_t launch_prepare_step(const uint16_t* k, int64_t n_new, const int32_t*
   p.status = status;
   p.kb = (n_new + kStoreRowsPerBlock - 1) / kStoreRowsPerBlock;
   const int64_t qb = (n_rows * kHeads + kRowsPerBlock - 1) / kRowsPerBlock;
-  prepare_step_kernel<<<(unsigned)(1 + p.kb + qb), 256, 0, stream>>>(p);
+  prepare_step_kernel<<<(unsigned)(1 + p.kb + qb), 256, StoreSmem<kPrepareStoreDepth>::kBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
