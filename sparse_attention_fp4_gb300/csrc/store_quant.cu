@@ -23,7 +23,6 @@
 //     exponent/mantissa bits of amax; e2m1 by the hardware RNE-satfinite convert,
 //     which keeps the sign of a value that rounds to zero.
 #include "launchers.cuh"
-#include "ptx.cuh"
 #include "schedule_build.cuh"
 
 #include <algorithm>
@@ -199,8 +198,8 @@ __device__ __forceinline__ void unpack(uint4 u, f2 v[4]) {
   v[3] = {__uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u)};
 }
 
-// y <- RMSNorm(x) * w, with w (fp32) read from shared memory at wl = w + 8 l.
-__device__ __forceinline__ void rmsnorm(f2 x[4][4], const float* wl, float eps) {
+// y <- RMSNorm(x) * w.
+__device__ __forceinline__ void rmsnorm(f2 x[4][4], const f2 w[4][4], float eps) {
   float g[4];  // the sums of the lane's groups 4 m + l, left to right
 #pragma unroll
   for (int m = 0; m < 4; m++) {
@@ -229,10 +228,7 @@ __device__ __forceinline__ void rmsnorm(f2 x[4][4], const float* wl, float eps) 
 #pragma unroll
   for (int m = 0; m < 4; m++)
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const float2 wv = *reinterpret_cast<const float2*>(wl + 32 * m + 2 * j);
-      x[m][j] = mul2(mul2(x[m][j], rr), f2{wv.x, wv.y});
-    }
+    for (int j = 0; j < 4; j++) x[m][j] = mul2(mul2(x[m][j], rr), w[m][j]);
 }
 
 // RoPE on dims 0..63: the lane's pairs (32 * 0 + 8 l + e, 32 * 1 + 8 l + e), with cos and
@@ -364,117 +360,93 @@ struct StoreArgs {
 
 // The chain of one K row up to the Hadamard, on the quarter-warp mapping: x holds the
 // lane's 32 values on return.  cs holds the lane's 8 cos and 8 sin of the row's position.
-__device__ __forceinline__ void k_chain_qw(qw::f2 x[4][4], const uint4 raw[4], const float* wl, float eps,
+__device__ __forceinline__ void k_chain_qw(qw::f2 x[4][4], const uint4 raw[4], const qw::f2 w[4][4], float eps,
                                            const uint4 cs[2], int l) {
 #pragma unroll
   for (int m = 0; m < 4; m++) qw::unpack(raw[m], x[m]);
-  qw::rmsnorm(x, wl, eps);
+  qw::rmsnorm(x, w, eps);
   qw::rope(x, cs[0], cs[1]);
   qw::hadamard(x, l);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void load_cs(const uint16_t* cos_sin, int32_t pos, int l, uint4 cs[2]) {
+  const uint16_t* row = cos_sin + (int64_t)pos * kRope;
+  cs[0] = __ldg(reinterpret_cast<const uint4*>(row + 8 * l));
+  cs[1] = __ldg(reinterpret_cast<const uint4*>(row + 32 + 8 * l));
 }
 
-// Shared memory of a K-store CTA (256 threads): the norm weight in fp32, and a ring of
-// kDepth rows per thread -- its six 16-byte chunks (four of K, one of cos, one of sin),
-// chunk-major so that a warp's accesses hit consecutive banks.
-template <int kDepth>
-struct StoreSmem {
-  static constexpr size_t kW = 0, kRing = 512;
-  static constexpr size_t kBytes = kRing + 16 * 6 * 256 * kDepth;
+// The lane's 32 norm weights in fp32 (elements 32 m + 8 l + e).
+__device__ __forceinline__ void load_norm_w(const uint16_t* norm_w, int l, qw::f2 w[4][4]) {
+  const uint16_t* row = norm_w + 8 * l;
+#pragma unroll
+  for (int m = 0; m < 4; m++) qw::unpack(__ldg(reinterpret_cast<const uint4*>(row + 32 * m)), w[m]);
+}
+
+// One row of the K store as a quarter-warp sees it: its raw K, cos/sin and destination.
+struct StoreRow {
+  uint4 raw[4];
+  uint4 cs[2];
+  int32_t slot;
+  bool store;
 };
 
+// Loads of row n except the table (the position decides which table row): slot and
+// position checked, raw K.  Rows past the end are not stored and read table row 0.
+__device__ __forceinline__ int32_t load_row_head(const StoreArgs& a, int64_t n, int l, bool reporter, StoreRow& r) {
+  const bool in_range = n < a.n_rows;
+  int32_t pos = 0;
+  r.slot = -1;
+  if (in_range) {
+    r.slot = __ldg(a.slots + n);
+    pos = __ldg(a.positions + n);
+    const uint16_t* row = a.k + n * kHeadDim + 8 * l;
+#pragma unroll
+    for (int m = 0; m < 4; m++) r.raw[m] = __ldg(reinterpret_cast<const uint4*>(row + 32 * m));
+  } else {
+#pragma unroll
+    for (int m = 0; m < 4; m++) r.raw[m] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  r.store = store_row_ok(in_range, r.slot, pos, a.num_pages, a.max_pos, reporter, a.status);
+  return pos;
+}
+
 // Rows u * 8 + (lane / 4) for units u = first, first + stride, ...: every lane of a warp
-// takes the same number of iterations, as the shuffles need.  Each lane copies its own
-// chunks of the next kDepth rows into its ring with cp.async while it computes the
-// current row; slot and position are read one row further ahead, so that the cos/sin
-// copy can be issued at once.  With three CTAs an SM and kDepth = 2, a 65,536-row store
-// has nearly every row in flight from the start: in-kernel timing put the launch at
-// ~12.5 us against ~17 us for loads one row ahead in registers, and ~7.4 us for the loads
-// alone.  All threads of the CTA must call this (one barrier).
-template <bool kFp8, int kDepth>
+// takes the same number of iterations, as the shuffles need.  Software pipeline, one row
+// deep: while row i is computed, row i+1's K, slot and position are in flight, and its
+// cos/sin load is issued once row i's Hadamard is done (the position has arrived by
+// then).  The norm weight stays in registers (124 a thread, two CTAs an SM).  Timed on
+// 65,536 rows after an L2 flush, this measured 16.3-16.6 us a launch against 18.0 us for
+// a variant that streams two rows ahead into shared memory with cp.async at three CTAs
+// an SM (the norm weight then read from shared memory).
+template <bool kFp8>
 __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_unit, int64_t unit_stride,
-                                             uint8_t* smem, uint8_t* payload, uint8_t* scale, uint8_t* fp8_pages) {
-  using L = StoreSmem<kDepth>;
-  float* w_s = reinterpret_cast<float*>(smem + L::kW);
-  const uint32_t ring = ptx::smem_addr(smem + L::kRing);
-  for (int i = threadIdx.x; i < kHeadDim; i += blockDim.x) w_s[i] = __uint_as_float((uint32_t)a.norm_w[i] << 16);
-  __syncthreads();
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, l = lane & 3;
+                                             uint8_t* payload, uint8_t* scale, uint8_t* fp8_pages) {
+  const int lane = threadIdx.x & 31, l = lane & 3;
   const int sub = lane >> 2;
   const bool reporter = l == 0;
   const int64_t n_units = (a.n_rows + 7) >> 3;
-  if (first_unit >= n_units) return;  // uniform over the warp
-  const float* wl = w_s + 8 * l;
-  auto chunk = [&](int d, int c) { return ring + (uint32_t)(((d * 6 + c) * 256 + tid) * 16); };
-  // slot and position of the row of unit u (none past the end)
-  auto head = [&](int64_t u, int32_t& slot, int32_t& pos) {
-    const int64_t n = u * 8 + sub;
-    slot = -1;
-    pos = 0;
-    if (u < n_units && n < a.n_rows) {
-      slot = __ldg(a.slots + n);
-      pos = __ldg(a.positions + n);
-    }
-  };
-  // checks of the row of unit u and its chunk copies (one group); returns the slot to
-  // write, -1 for none
-  auto issue = [&](int d, int64_t u, int32_t slot, int32_t pos) -> int32_t {
-    const int64_t n = u * 8 + sub;
-    const bool in_range = u < n_units && n < a.n_rows;
-    const bool store = store_row_ok(in_range, slot, pos, a.num_pages, a.max_pos, reporter, a.status);
-    if (in_range) {
-      const uint16_t* src = a.k + n * kHeadDim + 8 * l;
-#pragma unroll
-      for (int m = 0; m < 4; m++) cp_async16(chunk(d, m), src + 32 * m);
-      const uint16_t* cs = a.cos_sin + (int64_t)pos * kRope + 8 * l;
-      cp_async16(chunk(d, 4), cs);
-      cp_async16(chunk(d, 5), cs + 32);
-    }
-    cp_async_commit();
-    return store ? slot : -1;
-  };
-  // the slots of the rows in the ring, oldest first (rotated each iteration)
-  int32_t ws[kDepth];
-  {
-    int32_t hs[kDepth], hp[kDepth];
-#pragma unroll
-    for (int d = 0; d < kDepth; d++) head(first_unit + d * unit_stride, hs[d], hp[d]);
-#pragma unroll
-    for (int d = 0; d < kDepth; d++) ws[d] = issue(d, first_unit + d * unit_stride, hs[d], hp[d]);
-  }
-  int32_t nslot, npos;
-  head(first_unit + kDepth * unit_stride, nslot, npos);
-  int d = 0;
-  for (int64_t u = first_unit; u < n_units; u += unit_stride) {
-    cp_async_wait<kDepth - 1>();
-    uint4 raw[4], cs[2];
-#pragma unroll
-    for (int m = 0; m < 4; m++) asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                             : "=r"(raw[m].x), "=r"(raw[m].y), "=r"(raw[m].z), "=r"(raw[m].w)
-                                             : "r"(chunk(d, m)));
-#pragma unroll
-    for (int c = 0; c < 2; c++) asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                             : "=r"(cs[c].x), "=r"(cs[c].y), "=r"(cs[c].z), "=r"(cs[c].w)
-                                             : "r"(chunk(d, 4 + c)));
-    const int32_t slot = ws[0];
+  int64_t u = first_unit;
+  if (u >= n_units) return;  // uniform over the warp
+  qw::f2 w[4][4];
+  load_norm_w(a.norm_w, l, w);
+  StoreRow cur;
+  load_cs(a.cos_sin, load_row_head(a, u * 8 + sub, l, reporter, cur), l, cur.cs);
+  for (;;) {
+    const int64_t un = u + unit_stride;
+    const bool more = un < n_units;
+    StoreRow nxt;
+    int32_t npos = 0;
+    if (more) npos = load_row_head(a, un * 8 + sub, l, reporter, nxt);
     qw::f2 x[4][4];
-    k_chain_qw(x, raw, wl, a.eps, cs, l);
-    const int64_t page = slot >> 6;
-    const int j = slot & 63;
+    k_chain_qw(x, cur.raw, w, a.eps, cur.cs, l);
+    if (more) load_cs(a.cos_sin, npos, l, nxt.cs);
+    const int64_t page = cur.slot >> 6;
+    const int j = cur.slot & 63;
     if constexpr (!kFp8) {
       uint32_t sb[4], word[4];
 #pragma unroll
       for (int m = 0; m < 4; m++) word[m] = qw::fp4_block(x[m], sb[m]);
-      if (slot >= 0) {
+      if (cur.store) {
 #pragma unroll
         for (int m = 0; m < 4; m++)
           *reinterpret_cast<uint32_t*>(payload + ((page * 4 + m) * kPage + j) * 16 + 4 * l) = word[m];
@@ -498,36 +470,25 @@ __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_u
                 (e4m3x2(__fdiv_rn(x[m][1].x, sc), __fdiv_rn(x[m][1].y, sc)) << 16);
         out.y = e4m3x2(__fdiv_rn(x[m][2].x, sc), __fdiv_rn(x[m][2].y, sc)) |
                 (e4m3x2(__fdiv_rn(x[m][3].x, sc), __fdiv_rn(x[m][3].y, sc)) << 16);
-        if (slot >= 0) *reinterpret_cast<uint2*>(base + j * kHeadDim + 32 * m + 8 * l) = out;
+        if (cur.store) *reinterpret_cast<uint2*>(base + j * kHeadDim + 32 * m + 8 * l) = out;
       }
-      if (slot >= 0 && l == 0) *reinterpret_cast<float*>(base + kPage * kHeadDim + j * 4) = sc;
+      if (cur.store && l == 0) *reinterpret_cast<float*>(base + kPage * kHeadDim + j * 4) = sc;
     }
-    // refill this ring entry with the row kDepth units on; read the next head
-#pragma unroll
-    for (int i = 0; i + 1 < kDepth; i++) ws[i] = ws[i + 1];
-    ws[kDepth - 1] = issue(d, u + kDepth * unit_stride, nslot, npos);
-    head(u + (kDepth + 1) * unit_stride, nslot, npos);
-    d = d + 1 == kDepth ? 0 : d + 1;
+    if (!more) break;
+    u = un;
+    cur = nxt;
   }
-  cp_async_wait<0>();
 }
 
-constexpr int kStoreDepth = 2;         // rows in flight per thread in the K-store kernels
-constexpr int kPrepareStoreDepth = 1; // one row per thread in the step preparation
-
-__global__ void __launch_bounds__(256, 3) store_k_kernel(const StoreArgs a, uint8_t* __restrict__ payload,
+__global__ void __launch_bounds__(256) store_k_kernel(const StoreArgs a, uint8_t* __restrict__ payload,
                                                       uint8_t* __restrict__ scale) {
-  extern __shared__ __align__(16) uint8_t store_smem[];
   const int64_t warps = (int64_t)gridDim.x * 8;
-  store_k_rows<false, kStoreDepth>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, store_smem, payload, scale,
-                                   nullptr);
+  store_k_rows<false>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, payload, scale, nullptr);
 }
 
-__global__ void __launch_bounds__(256, 3) store_k_fp8_kernel(const StoreArgs a, uint8_t* __restrict__ pages) {
-  extern __shared__ __align__(16) uint8_t store_smem[];
+__global__ void __launch_bounds__(256) store_k_fp8_kernel(const StoreArgs a, uint8_t* __restrict__ pages) {
   const int64_t warps = (int64_t)gridDim.x * 8;
-  store_k_rows<true, kStoreDepth>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, store_smem, nullptr,
-                                  nullptr, pages);
+  store_k_rows<true>(a, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5), warps, nullptr, nullptr, pages);
 }
 
 // Q quant of the 16 (row, head) vectors of block `block`.
@@ -607,15 +568,14 @@ struct PrepareParams {
 };
 
 __global__ void __launch_bounds__(256) prepare_step_kernel(const PrepareParams p) {
-  extern __shared__ __align__(16) uint8_t prep_smem[];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x == 0) {
     build_schedule_block<256>(p.context_lens, p.row_seq, (int32_t)p.n_rows, p.num_ctas, p.schedule);
   } else if ((int64_t)blockIdx.x <= p.kb) {
     const StoreArgs a{p.k, p.n_new, p.positions, p.slots, p.norm_w, p.eps, p.cos_sin, p.max_pos, p.num_pages,
                       p.status};
-    store_k_rows<false, kPrepareStoreDepth>(a, ((int64_t)blockIdx.x - 1) * 8 + (threadIdx.x >> 5), p.kb * 8,
-                                            prep_smem, p.payload, p.scale, nullptr);
+    store_k_rows<false>(a, ((int64_t)blockIdx.x - 1) * 8 + (threadIdx.x >> 5), p.kb * 8, p.payload, p.scale,
+                        nullptr);
   } else {
     quant_q_block(blockIdx.x - 1 - p.kb, p.q, p.n_rows, p.q_positions, p.cos_sin, p.max_pos, p.q_payload,
                   p.q_scale, p.status);
@@ -766,9 +726,7 @@ template <class Kern>
 unsigned store_grid(Kern kernel, int64_t n_rows, cudaError_t* err) {
   const int64_t need = (n_rows + kStoreRowsPerBlock - 1) / kStoreRowsPerBlock;
   int fit = 0;
-  *err = set_smem_attr_once(reinterpret_cast<const void*>(kernel), StoreSmem<kStoreDepth>::kBytes);
-  if (*err == cudaSuccess)
-    *err = resident_ctas(reinterpret_cast<const void*>(kernel), 256, StoreSmem<kStoreDepth>::kBytes, &fit);
+  *err = resident_ctas(reinterpret_cast<const void*>(kernel), 256, 0, &fit);
   return (unsigned)std::max<int64_t>(1, std::min<int64_t>(need, fit));
 }
 
@@ -782,7 +740,7 @@ cudaError_t launch_store_k(const uint16_t* k, int64_t n_rows, const int32_t* pos
   const unsigned grid = store_grid(store_k_kernel, n_rows, &e);
   if (e != cudaSuccess) return e;
   const StoreArgs a{k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, num_pages, status};
-  store_k_kernel<<<grid, 256, StoreSmem<kStoreDepth>::kBytes, stream>>>(a, payload, scale);
+  store_k_kernel<<<grid, 256, 0, stream>>>(a, payload, scale);
   return cudaGetLastError();
 }
 
@@ -795,7 +753,7 @@ cudaError_t launch_store_k_fp8(const uint16_t* k, int64_t n_rows, const int32_t*
   const unsigned grid = store_grid(store_k_fp8_kernel, n_rows, &e);
   if (e != cudaSuccess) return e;
   const StoreArgs a{k, n_rows, positions, slots, norm_w, eps, cos_sin, max_pos, num_pages, status};
-  store_k_fp8_kernel<<<grid, 256, StoreSmem<kStoreDepth>::kBytes, stream>>>(a, pages);
+  store_k_fp8_kernel<<<grid, 256, 0, stream>>>(a, pages);
   return cudaGetLastError();
 }
 
@@ -843,7 +801,7 @@ cudaError_t launch_prepare_step(const uint16_t* k, int64_t n_new, const int32_t*
   p.status = status;
   p.kb = (n_new + kStoreRowsPerBlock - 1) / kStoreRowsPerBlock;
   const int64_t qb = (n_rows * kHeads + kRowsPerBlock - 1) / kRowsPerBlock;
-  prepare_step_kernel<<<(unsigned)(1 + p.kb + qb), 256, StoreSmem<kPrepareStoreDepth>::kBytes, stream>>>(p);
+  prepare_step_kernel<<<(unsigned)(1 + p.kb + qb), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
