@@ -274,6 +274,8 @@ __device__ __forceinline__ void select_own_row(const LogitsParams& p, const Sche
   }
 }
 
+// kSelC: the CTAs that select each row in the fused call (1 or 2); 0 for a launch without
+// the selection, which compiles out the epilogue's piece counting and the selecting tail.
 template <int kSelC>
 __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_constant__ CUtensorMap pay_map,
                                                                  const __grid_constant__ CUtensorMap sc_map,
@@ -603,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
             if (a >= tiles) continue;
             const int32_t tok = (i + a) * kTileTokens + m;
             // a row the launch selects (more than k tokens) and a tile holding some of them
-            const bool counted = p.k > 0 && L > p.k && (i + a) * kTileTokens < L;
+            const bool counted = kSelC > 0 && p.k > 0 && L > p.k && (i + a) * kTileTokens < L;
             if (counted && lane == r) pieces++;
             if (tok < L) {
               // sum_h w_h * ReLU(d_h): scalar ReLU, packed pair FMAs, eight partial sums
@@ -626,7 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
       // this warp's pieces of the item's rows are written: publish them (release at GPU
       // scope, after the warp's logits stores)
       __syncwarp();
-      if (ok && pieces > 0) ptx::gmem_red_release_add(sv.sel_cnt + r0 + lane, pieces);
+      if constexpr (kSelC > 0) {
+        if (ok && pieces > 0) ptx::gmem_red_release_add(sv.sel_cnt + r0 + lane, pieces);
+      }
     }
   }
 
@@ -634,10 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) logits_mxf4_kernel(const __grid_c
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == kWarpMma) ptx::tmem_dealloc(tmem, kTmemCols);
-  if (p.k > 0 && valid) {
-    __shared__ sel::Shared sel_sh;
-    __shared__ int32_t sel_go;
-    select_own_row<kSelC>(p, sv, reinterpret_cast<uint32_t*>(smem), sel_sh, &sel_go, *abort_flag != 0);
+  if constexpr (kSelC > 0) {
+    if (p.k > 0 && valid) {
+      __shared__ sel::Shared sel_sh;
+      __shared__ int32_t sel_go;
+      select_own_row<kSelC>(p, sv, reinterpret_cast<uint32_t*>(smem), sel_sh, &sel_go, *abort_flag != 0);
+    }
   }
 }
 
@@ -725,9 +731,11 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
   if (prm.k > 0 && n_rows > num_ctas) return cudaErrorInvalidValue;  // the selection needs a CTA per row
   // A pair of CTAs per row when the grid holds two for every row and the pairs (clusters
   // of two) can all be resident at once; else one CTA per row.
-  const int sel_c = prm.k > 0 && 2 * (int64_t)n_rows <= num_ctas && pairs_fit(num_ctas) ? 2 : 1;
-  const void* fn = sel_c == 2 ? reinterpret_cast<const void*>(logits_mxf4_kernel<2>)
-                              : reinterpret_cast<const void*>(logits_mxf4_kernel<1>);
+  // (no selection: the instantiation without the epilogue's piece counting and the tail)
+  const int sel_c = prm.k == 0 ? 0 : 2 * (int64_t)n_rows <= num_ctas && pairs_fit(num_ctas) ? 2 : 1;
+  const void* fn = sel_c == 2   ? reinterpret_cast<const void*>(logits_mxf4_kernel<2>)
+                   : sel_c == 1 ? reinterpret_cast<const void*>(logits_mxf4_kernel<1>)
+                                : reinterpret_cast<const void*>(logits_mxf4_kernel<0>);
   cudaError_t e = set_smem_attr_once(fn, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -754,7 +762,8 @@ cudaError_t launch_logits_mxf4(const uint8_t* q_payload, const uint8_t* q_scale,
     cfg.numAttrs = 1;
   }
   if (sel_c == 2) return cudaLaunchKernelEx(&cfg, logits_mxf4_kernel<2>, pay_map, sc_map, prm);
-  return cudaLaunchKernelEx(&cfg, logits_mxf4_kernel<1>, pay_map, sc_map, prm);
+  if (sel_c == 1) return cudaLaunchKernelEx(&cfg, logits_mxf4_kernel<1>, pay_map, sc_map, prm);
+  return cudaLaunchKernelEx(&cfg, logits_mxf4_kernel<0>, pay_map, sc_map, prm);
 }
 
 }  // namespace fp4idx
