@@ -8,7 +8,8 @@
 //
 // One CTA of 1,024 threads per row; when the rows are few (two CTAs per row still fit
 // on the GPU), a pair of CTAs per row in a thread-block cluster, each owning half of
-// the row's positions.  The two CTAs of a pair exchange only histogram counts, emit
+// the row's positions; when they are many (more than the SMs), one CTA of 512 threads
+// per row, two of them an SM, so that two rows' latency-bound phases overlap.  The two CTAs of a pair exchange only histogram counts, emit
 // totals and a short list of boundary keys, through distributed shared memory.  No
 // other hand-off between CTAs: a global candidate list, a fence and an arrival counter
 // each cost microseconds of latency on this path.
@@ -20,20 +21,20 @@
 namespace fp4idx {
 namespace {
 
-constexpr int kThreads = 1024;
 constexpr int kRes = 32768;  // keys a CTA keeps in shared memory
-using Sel = sel::Select<kThreads>;
 
-// Dynamic shared memory of the top-k kernel: Sel::smem_words<kC>(res) words.
+// Dynamic shared memory of the top-k kernel: Select<NT>::smem_words<kC>(res) words.
 extern __shared__ __align__(16) uint32_t topk_dyn[];
 
-// kC CTAs (a cluster) per row; each owns a contiguous slice of the row's groups.  spill +
-// row * sstride holds keys past res (sstride a multiple of 4).
-template <int kC>
-__global__ void __launch_bounds__(kThreads, 1)
+// kC CTAs (a cluster) of NT threads per row; each owns a contiguous slice of the row's
+// groups.  spill + row * sstride holds keys past res (sstride a multiple of 4).
+template <int kC, int NT, int kMinBlocks>
+__global__ void __launch_bounds__(NT, kMinBlocks)
     topk_row_kernel(const float* __restrict__ logits, int64_t stride, const int32_t* __restrict__ context_lens,
                     int32_t max_context, int32_t k, int32_t res, uint32_t* spill, int64_t sstride,
                     int32_t* __restrict__ out, int32_t* status) {
+  using Sel = sel::Select<NT>;
+  constexpr int kThreads = NT;
   __shared__ sel::Shared sh;
   const int64_t row = blockIdx.x / kC;
   const int rank = (int)(blockIdx.x % kC);
@@ -48,7 +49,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = rank * kThreads + tid; i < k; i += kC * kThreads) o[i] = i < L ? i : -1;
     return;
   }
-  Sel::row<kC, false>(logits + row * stride, L, k, o, spill + row * sstride, res, topk_dyn, sh, rank, status);
+  Sel::template row<kC, false>(logits + row * stride, L, k, o, spill + row * sstride, res, topk_dyn, sh, rank,
+                               status);
 }
 
 inline int64_t spill_stride(int32_t max_context) {
@@ -56,32 +58,28 @@ inline int64_t spill_stride(int32_t max_context) {
 }
 inline size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-std::atomic<bool> g_attr_done[2][64];
 std::atomic<int> g_sms[64];
 
-// Shared memory of a kC-CTA launch with `res` keys a CTA.
-template <int kC>
+// Shared memory of a kC-CTA launch of NT threads with `res` keys a CTA.
+template <int kC, int NT>
 constexpr size_t smem_bytes(int32_t res) {
-  return (size_t)Sel::smem_words<kC>(res) * sizeof(uint32_t);
+  return (size_t)sel::Select<NT>::template smem_words<kC>(res) * sizeof(uint32_t);
 }
 
-template <int kC>
-cudaError_t launch_rows(int dev, const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
+template <int kC, int NT, int kMinBlocks>
+cudaError_t launch_rows(const float* logits, int64_t stride, const int32_t* context_lens, int32_t n_rows,
                         int32_t max_context, int32_t k, void* workspace, int32_t* out, int32_t* status,
                         cudaStream_t stream) {
-  if (dev < 0 || dev >= 64 || !g_attr_done[kC - 1][dev].load()) {
-    const cudaError_t e = cudaFuncSetAttribute(topk_row_kernel<kC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem_bytes<kC>(kRes));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) g_attr_done[kC - 1][dev].store(true);
-  }
+  const void* fn = reinterpret_cast<const void*>(topk_row_kernel<kC, NT, kMinBlocks>);
+  const cudaError_t e = set_smem_attr_once(fn, smem_bytes<kC, NT>(kRes));
+  if (e != cudaSuccess) return e;
   // keys a CTA holds: its slice of the longest row, rounded to groups of four
   const int64_t groups = ((int64_t)max(max_context, 1) + 3) / 4;
   const int32_t res = (int32_t)min((int64_t)kRes, 4 * ((groups + kC - 1) / kC));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)n_rows * kC);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<kC>(res);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem_bytes<kC, NT>(res);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -90,8 +88,8 @@ cudaError_t launch_rows(int dev, const float* logits, int64_t stride, const int3
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = kC > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_row_kernel<kC>, logits, stride, context_lens, max_context, k, res,
-                            reinterpret_cast<uint32_t*>(workspace), spill_stride(max_context), out, status);
+  return cudaLaunchKernelEx(&cfg, topk_row_kernel<kC, NT, kMinBlocks>, logits, stride, context_lens, max_context, k,
+                            res, reinterpret_cast<uint32_t*>(workspace), spill_stride(max_context), out, status);
 }
 
 }  // namespace
@@ -117,10 +115,16 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
     if (dev >= 0 && dev < 64) g_sms[dev].store(sms);
   }
   // Few rows leave most SMs idle: then each row goes to a pair of CTAs (a cluster), which
-  // halves the passes over its keys.
+  // halves the passes over its keys.  Many rows queue on the SMs: then two CTAs of 512
+  // threads an SM overlap two rows' barrier- and latency-bound phases.
   if (2 * (int64_t)n_rows <= sms)
-    return launch_rows<2>(dev, logits, stride, context_lens, n_rows, max_context, k, workspace, out, status, stream);
-  return launch_rows<1>(dev, logits, stride, context_lens, n_rows, max_context, k, workspace, out, status, stream);
+    return launch_rows<2, 1024, 1>(logits, stride, context_lens, n_rows, max_context, k, workspace, out, status,
+                                   stream);
+  if ((int64_t)n_rows > sms)
+    return launch_rows<1, 512, 2>(logits, stride, context_lens, n_rows, max_context, k, workspace, out, status,
+                                  stream);
+  return launch_rows<1, 1024, 1>(logits, stride, context_lens, n_rows, max_context, k, workspace, out, status,
+                                 stream);
 }
 
 }  // namespace fp4idx

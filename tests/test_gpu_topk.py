@@ -99,6 +99,18 @@ def test_topk_chunk_boundaries(kind):
         assert np.array_equal(got[t], expected(rows[t], L, 2048)), (kind, t, L)
 
 
+@pytest.mark.parametrize("kind", ["normal", "dups", "signed_zeros"])
+def test_topk_many_rows(kind):
+    """More rows than SMs: one CTA of 512 threads per row, two of them an SM.  Lengths from
+    empty to past the keys a CTA keeps in shared memory."""
+    rng = np.random.default_rng(13 + len(kind))
+    lens = [int(x) for x in rng.integers(0, 40000, size=194)] + [0, 1, 2047, 2048, 2049, 65535]
+    rows = [_dist(rng, kind, max(L, 1)) for L in lens]
+    got = run(rows, lens, 2048)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, 2048)), (kind, t, L)
+
+
 def _sample_positions(L, n=1024):
     return (np.arange(n, dtype=np.int64) * L) // n
 
@@ -136,7 +148,8 @@ def _boundary_row(rng, L, k, n_band, band):
     return x
 
 
-@pytest.mark.parametrize("n_rows", [8, 100])  # a CTA pair per row, and one CTA per row
+# a CTA pair per row; one CTA per row; more rows than SMs: one 512-thread CTA per row
+@pytest.mark.parametrize("n_rows", [8, 100, 200])
 @pytest.mark.parametrize("n_band,band", [(2, [5.0, 5.0]), (2, [5.0, 5.0000005]), (3, [5.0, 5.0, 5.0]),
                                          (3, [5.0000005, 5.0, 5.0000005])])
 def test_topk_boundary_sub_bin(n_rows, n_band, band):
