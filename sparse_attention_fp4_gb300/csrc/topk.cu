@@ -114,10 +114,13 @@ cudaError_t launch_topk(const float* logits, int64_t stride, const int32_t* cont
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) g_sms[dev].store(sms);
   }
-  // Few rows leave most SMs idle: then each row goes to a pair of CTAs (a cluster), which
-  // halves the passes over its keys.  Many rows queue on the SMs: then two CTAs of 512
-  // threads an SM overlap two rows' barrier- and latency-bound phases.
-  if (2 * (int64_t)n_rows <= sms)
+  // Few long rows leave most SMs idle: then each row goes to a pair of CTAs (a cluster),
+  // which halves the passes over its keys.  For short rows the pair's cluster launch and
+  // exchanges cost more than they save (one row of 4,096: 10.2 us a launch alone against
+  // 12.3 us as a pair).  Many rows queue on the SMs: then two CTAs of 512 threads an SM
+  // overlap two rows' barrier- and latency-bound phases.
+  constexpr int32_t kPairMinContext = 8192;
+  if (2 * (int64_t)n_rows <= sms && max_context > kPairMinContext)
     return launch_rows<2, 1024, 1>(logits, stride, context_lens, n_rows, max_context, k, workspace, out, status,
                                    stream);
   if ((int64_t)n_rows > sms)

@@ -148,13 +148,14 @@ def _boundary_row(rng, L, k, n_band, band):
     return x
 
 
-# a CTA pair per row; one CTA per row; more rows than SMs: one 512-thread CTA per row
-@pytest.mark.parametrize("n_rows", [8, 100, 200])
+# a CTA pair per row (few rows longer than 8,192); one CTA per row (few short rows, or
+# more than half the SMs); more rows than SMs: one 512-thread CTA per row
+@pytest.mark.parametrize("n_rows,L", [(8, 16384), (8, 4096), (100, 4096), (200, 4096)])
 @pytest.mark.parametrize("n_band,band", [(2, [5.0, 5.0]), (2, [5.0, 5.0000005]), (3, [5.0, 5.0, 5.0]),
                                          (3, [5.0000005, 5.0, 5.0000005])])
-def test_topk_boundary_sub_bin(n_rows, n_band, band):
+def test_topk_boundary_sub_bin(n_rows, L, n_band, band):
     rng = np.random.default_rng(21 + n_band)
-    L, k = 4096, 2048
+    k = 2048
     lens = [L] * n_rows
     rows = [_boundary_row(rng, L, k, n_band, band) for _ in range(n_rows)]
     got = run(rows, lens, k)
