@@ -99,6 +99,18 @@ def test_topk_chunk_boundaries(kind):
         assert np.array_equal(got[t], expected(rows[t], L, 2048)), (kind, t, L)
 
 
+@pytest.mark.parametrize("longest", [8191, 8192, 8193])
+def test_topk_pair_threshold(longest):
+    """Few rows: one CTA per row while the longest row has at most 8,192 positions, a CTA
+    pair per row past that; the rows around the switch select the same either way."""
+    rng = np.random.default_rng(longest)
+    lens = [longest, 2049, 4097, 8000, 3000]
+    rows = [_dist(rng, kd, L) for kd, L in zip(["normal", "dups", "cauchy", "outliers", "normal"], lens)]
+    got = run(rows, lens, 2048)
+    for t, L in enumerate(lens):
+        assert np.array_equal(got[t], expected(rows[t], L, 2048)), (longest, t, L)
+
+
 @pytest.mark.parametrize("kind", ["normal", "dups", "signed_zeros"])
 def test_topk_many_rows(kind):
     """More rows than SMs: one CTA of 512 threads per row, two of them an SM.  Lengths from
