@@ -431,10 +431,12 @@ def time_step(st, steps, warmup, flush_l2, device, live_n=500, alone_n=200):
     clocks = sampler.stop()
     step_ms = [starts[i].elapsed_time(ends[i]) for i in range(K)]
 
-    # kernel times inside the step, from the instrumented graph (same flush and spin)
+    # kernel times inside the step, from the instrumented graph (same flush and spin); a
+    # fixed number of replays whatever K: event timestamps are coarse, so the mean needs
+    # many of them
     live = {n: [] for n in names}
     if marks:
-        for i in range(min(K, live_n)):
+        for i in range(live_n):
             flush_l2()
             torch.cuda._sleep(SPIN_CYCLES)
             gm.replay()
@@ -450,7 +452,7 @@ def time_step(st, steps, warmup, flush_l2, device, live_n=500, alone_n=200):
             fn()
         subs.append((name, sg))
     per_times = {name: [] for name, _ in subs}
-    for i in range(min(K, alone_n)):
+    for i in range(alone_n):
         for name, sg in subs:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -719,8 +721,12 @@ def run_reference(args):
     step = OracleStep(b)
     cores = oracle.max_threads()
     rows_per = 8
-    for i in range(3):  # warm-up: page in the oracle and its inputs
-        step.run(np.arange(i * rows_per, (i + 1) * rows_per) % b.n_rows)
+    warm = 0.0
+    for i in range(max(3, args.warmup)):  # warm-up: page in the oracle and its inputs
+        warm += step.run(np.arange(i * rows_per, (i + 1) * rows_per) % b.n_rows)
+    # a bounded sample: about a minute for the K timed steps, 1 to 8 rows each
+    rate = rows_per * max(3, args.warmup) / max(warm, 1e-9)
+    rows_per = int(max(1, min(8, rate * 60.0 / max(1, args.steps))))
     secs = 0.0
     for i in range(args.steps):
         secs += step.run(np.arange(i * rows_per, (i + 1) * rows_per) % b.n_rows)
