@@ -388,11 +388,18 @@ __device__ __forceinline__ void load_cs(const uint16_t* cos_sin, int32_t pos, in
   cs[1] = __ldg(reinterpret_cast<const uint4*>(row + 32 + 8 * l));
 }
 
-// The lane's 32 norm weights in fp32 (elements 32 m + 8 l + e).
-__device__ __forceinline__ void load_norm_w(const uint16_t* norm_w, int l, qw::f2 w[4][4]) {
-  const uint16_t* row = norm_w + 8 * l;
+// The lane's 32 norm weights (elements 32 m + 8 l + e) from the block's fp32 copy in
+// shared memory: eight 16-byte loads, each a broadcast to the warp's eight rows.
+__device__ __forceinline__ void norm_w_of_lane(const float* wsm, int l, qw::f2 w[4][4]) {
 #pragma unroll
-  for (int m = 0; m < 4; m++) qw::unpack(__ldg(reinterpret_cast<const uint4*>(row + 32 * m)), w[m]);
+  for (int m = 0; m < 4; m++) {
+    const float4 u0 = *reinterpret_cast<const float4*>(wsm + 32 * m + 8 * l);
+    const float4 u1 = *reinterpret_cast<const float4*>(wsm + 32 * m + 8 * l + 4);
+    w[m][0] = {u0.x, u0.y};
+    w[m][1] = {u0.z, u0.w};
+    w[m][2] = {u1.x, u1.y};
+    w[m][3] = {u1.z, u1.w};
+  }
 }
 
 // One row of the K store as a quarter-warp sees it: its raw K, cos/sin and destination.
@@ -427,10 +434,12 @@ __device__ __forceinline__ int32_t load_row_head(const StoreArgs& a, int64_t n, 
 // takes the same number of iterations, as the shuffles need.  Software pipeline, one row
 // deep: while row i is computed, row i+1's K, slot and position are in flight, and its
 // cos/sin load is issued once row i's Hadamard is done (the position has arrived by
-// then).  The norm weight stays in registers (124 a thread, two CTAs an SM).  Timed on
-// 65,536 rows after an L2 flush, this measured 16.3-16.6 us a launch against 18.0 us for
-// a variant that streams two rows ahead into shared memory with cp.async at three CTAs
-// an SM (the norm weight then read from shared memory).
+// then).  The norm weight is kept in shared memory as fp32 and read per row (118
+// registers a thread, two CTAs an SM): on 65,536 rows after an L2 flush that measured
+// 16.3-16.9 us a launch against 16.7-17.3 us with the weight held in 32 registers (124
+// a thread), 18.0 us for a variant that streams two rows ahead into shared memory with
+// cp.async at three CTAs an SM, and 21-22 us at three CTAs an SM with this pipeline
+// (80 registers, spilling).
 template <bool kFp8>
 __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_unit, int64_t unit_stride,
                                              uint8_t* payload, uint8_t* scale, uint8_t* fp8_pages) {
@@ -439,9 +448,10 @@ __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_u
   const bool reporter = l == 0;
   const int64_t n_units = (a.n_rows + 7) >> 3;
   int64_t u = first_unit;
-  if (u >= n_units) return;  // uniform over the warp
-  qw::f2 w[4][4];
-  load_norm_w(a.norm_w, l, w);
+  __shared__ __align__(16) float wsm[kHeadDim];  // the norm weight in fp32 (exact)
+  if (threadIdx.x < kHeadDim) wsm[threadIdx.x] = __uint_as_float((uint32_t)__ldg(a.norm_w + threadIdx.x) << 16);
+  __syncthreads();
+  if (u >= n_units) return;  // uniform over the warp, after the block's barrier
   StoreRow cur;
   load_cs(a.cos_sin, load_row_head(a, u * 8 + sub, l, reporter, cur), l, cur.cs);
   for (;;) {
@@ -450,7 +460,8 @@ __device__ __forceinline__ void store_k_rows(const StoreArgs& a, int64_t first_u
     StoreRow nxt;
     int32_t npos = 0;
     if (more) npos = load_row_head(a, un * 8 + sub, l, reporter, nxt);
-    qw::f2 x[4][4];
+    qw::f2 x[4][4], w[4][4];
+    norm_w_of_lane(wsm, l, w);
     k_chain_qw(x, cur.raw, w, a.eps, cur.cs, l);
     if (more) load_cs(a.cos_sin, npos, l, nxt.cs);
     const int64_t page = cur.slot >> 6;
