@@ -434,8 +434,8 @@ __device__ __forceinline__ int32_t load_row_head(const StoreArgs& a, int64_t n, 
 // takes the same number of iterations, as the shuffles need.  Software pipeline, one row
 // deep: while row i is computed, row i+1's K, slot and position are in flight, and its
 // cos/sin load is issued once row i's Hadamard is done (the position has arrived by
-// then).  The norm weight is kept in shared memory as fp32 and read per row (118
-// registers a thread, two CTAs an SM): on 65,536 rows after an L2 flush that measured
+// then).  The norm weight is kept in shared memory as fp32 and read per row (114
+// registers a thread in the FP4 kernel, two CTAs an SM): on 65,536 rows after an L2 flush that measured
 // 16.3-16.9 us a launch against 16.7-17.3 us with the weight held in 32 registers (124
 // a thread), 18.0 us for a variant that streams two rows ahead into shared memory with
 // cp.async at three CTAs an SM, and 21-22 us at three CTAs an SM with this pipeline
